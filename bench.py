@@ -1,0 +1,438 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE layer forward on GB300: tokens/s plus per-kernel roofline figures.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 2]
+
+One step = one pass of the whole forward (router projection, routing, dispatch, expert
+GEMM 1 + activation, expert GEMM 2 + gate, shared experts when present, combine) over one
+batch of the workload, inputs resident in HBM. The default workload is the grouped GShard
+top-2 layer (16 groups x 1024 tokens, 128 experts, capacity 16, d_model 1024, d_ff 4096,
+ReLU, random 2nd-expert dispatch). L2 is flushed (a 256 MiB write) before every timed
+step, outside the step's events. N > 1 (torchrun): every rank runs an independent replica
+on its own GPU (the forward has no exchange step on one GPU), value = tokens of all ranks
+divided by the slowest rank's time.
+
+--impl reference times the CPU oracle (plain numpy fp64, as it stands) on the host cores,
+each step one bounded sample of the same workload; under torchrun only rank 0 runs it.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer fwd tokens/s"
+UNIT = "tokens/s"
+FLUSH_BYTES = 256 << 20
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.md")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", type=int, default=2, help="workload preset (1..5)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def workload_desc(cfg: dict, n: int) -> dict:
+    d = {"workload": f"preset {n} {cfg['name']}: S={cfg['S']} tokens, G={cfg['G']} groups, "
+                     f"E={cfg['E']} experts, k={cfg['k']}, M={cfg['M']}, H={cfg['H']}, "
+                     f"{cfg['act']}, {cfg['dtype']}"}
+    if cfg["capacity_factor"] > 0:
+        d["workload"] += f", capacity factor {cfg['capacity_factor']}"
+    else:
+        d["workload"] += ", dropless"
+    if cfg["random_routing"]:
+        d["workload"] += ", random 2nd-expert dispatch"
+    if cfg["n_shared"]:
+        d["workload"] += f", {cfg['n_shared']} shared experts H={cfg['H_shared']}"
+    if cfg.get("bias"):
+        d["workload"] += ", skewed router bias"
+    d.update(S=cfg["S"], G=cfg["G"], E=cfg["E"], k=cfg["k"], M=cfg["M"], H=cfg["H"])
+    return d
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return dict(hbm=float(j["hbm_gbs"]), tc=float(j["bf16_tflops"]),
+                    tc_sustained=float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm=6800.0, tc=1900.0, tc_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        for r in rows:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                "sw_power_cap"), r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(rows),
+                "reasons": sorted(reasons)}
+
+
+def traffic_for(kernel: str, config: int):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None when the
+    kernel source changed since the capture."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return None
+    for line in lines:
+        if line.startswith("|") and f"| {kernel} |" in line and f"| {config} |" in line:
+            cells = [c.strip() for c in line.strip("|").split("|")]
+            # | kernel | config | dram bytes per launch | source sha1 |
+            try:
+                sha = cells[3]
+                src = os.path.join(ROOT, "top_gating_expert_gb300", "csrc", cells[4])
+                with open(src, "rb") as f:
+                    if hashlib.sha1(f.read()).hexdigest()[:12] != sha:
+                        return None
+                return float(cells[2])
+            except Exception:
+                return None
+    return None
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from top_gating_expert_gb300 import _native as N
+    from top_gating_expert_gb300 import moe
+    from top_gating_expert_gb300.inputs import CONFIGS, make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    n = args.config
+    cfg = CONFIGS[n]
+    inp = make_inputs(cfg, preset_number=n)
+    layer = moe.MoeLayer(cfg, inp.host, device=dev)
+    c = layer.cfg
+    x = inp.host["x"].to(dev)
+    u = inp.host["u"].to(dev) if cfg["random_routing"] else None
+    bias = layer.bias
+    residual = x if n == 5 else None
+    R_max = moe.rows_max(c)
+    dt = moe.torch_dtype(c)
+    ws, out, logits = layer.ws, layer.route_out, layer.logits
+    x_perm = torch.empty((R_max, c.M), dtype=dt, device=dev)
+    h_perm = torch.empty((R_max, c.H), dtype=dt, device=dev)
+    y_perm = torch.empty((R_max, c.M), dtype=dt, device=dev)
+    y = torch.empty((c.S, c.M), dtype=dt, device=dev)
+    shared = c.n_shared > 0
+    if shared:
+        Hc = c.n_shared * c.H_shared
+        h_sh = torch.empty((c.S, Hc), dtype=dt, device=dev)
+        s_out = torch.empty((c.S, c.M), dtype=dt, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    names = ["router", "route", "dispatch", "expert_up", "expert_down"] + \
+            (["shared_ffn"] if shared else []) + ["combine"]
+    launches = {"router": 1, "route": 3, "dispatch": 1, "expert_up": 1, "expert_down": 1,
+                "shared_ffn": 2, "combine": 1}
+
+    def step(evs=None):
+        def mark(i):
+            if evs is not None:
+                evs[i].record()
+        mark(0)
+        moe.router(c, x, layer.W_g, bias, logits, ws); mark(1)
+        moe.route(c, logits, u, out, ws); mark(2)
+        moe.dispatch(c, x, out, x_perm); mark(3)
+        moe.expert_up(c, x_perm, out.expert_offsets, layer.W_in_packed, h_perm, ws); mark(4)
+        moe.expert_down(c, h_perm, out.expert_offsets, out.w_perm, layer.W_out, y_perm, ws); mark(5)
+        i = 6
+        if shared:
+            moe.shared_ffn(c, x, layer.Ws_in_packed, layer.Ws_out_packed, h_sh, s_out, ws); mark(i)
+            i += 1
+        moe.combine(c, y_perm, out, s_out if shared else None, residual, y); mark(i)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    rc = moe.device_status(ws)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} after warm-up")
+
+    clocks = ClockSampler(local_rank)
+    time.sleep(0.3)
+    nev = len(names) + 1
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    barrier()
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        step(events[s])
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    rc = moe.device_status(ws)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} in the timed region")
+
+    step_ms = [events[s][0].elapsed_time(events[s][-1]) for s in range(args.steps)]
+    per_kernel = {nm: statistics.mean(events[s][i].elapsed_time(events[s][i + 1])
+                                      for s in range(args.steps)) for i, nm in enumerate(names)}
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---- e2e through the public API from pinned host buffers
+    x_host = inp.host["x"].pin_memory()
+    u_host = inp.host["u"].pin_memory() if u is not None else None
+    y_host = torch.empty((c.S, c.M), dtype=dt).pin_memory()
+    loss_host = torch.empty(2, dtype=torch.float32).pin_memory()
+    for _ in range(args.warmup):
+        layer.forward_from_host(x_host, u_host, y_host, loss_host)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    barrier()
+    for s in range(args.steps):
+        flush.zero_()
+        e2e_ev[s][0].record()
+        layer.forward_from_host(x_host, u_host, y_host, loss_host)
+        e2e_ev[s][1].record()
+    barrier()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = x_host.numel() * x_host.element_size() + (u_host.numel() * 4 if u_host is not None else 0)
+    d2h = y_host.numel() * y_host.element_size() + 8
+
+    if rank != 0:
+        return None
+
+    # ---- roofline figures per kernel
+    offs = out.expert_offsets.cpu().numpy()
+    R = int(offs[-1])
+    used = int((offs[1:] > offs[:-1]).sum())
+    eb = 2 if cfg["dtype"] == "bf16" else 4
+    S, E, M, H, k = c.S, c.E, c.M, c.H, c.k
+    f1 = 2 if cfg["act"] == "swiglu" else 1
+    P = peaks()
+    algo = {  # (bytes, flops) per launch, algorithmic
+        "router": (S * M * eb + E * M * eb + S * E * 4 + (E * 4 if bias is not None else 0),
+                   2.0 * S * M * E),
+        "route": (S * E * 4 + S * 4 + S * k * (4 + 4 + 4 + 1 + 4) + R * 8, 0.0),
+        "dispatch": (2 * R * M * eb + R * 4, 0.0),
+        "expert_up": (used * f1 * H * M * eb + R * M * eb + R * H * eb, 2.0 * f1 * R * M * H),
+        "expert_down": (used * M * H * eb + R * H * eb + R * M * eb + R * 4, 2.0 * R * M * H),
+        "combine": (R * M * eb + S * M * eb + S * k * 4 + (S * M * eb if residual is not None else 0),
+                    0.0),
+    }
+    if shared:
+        Hc = c.n_shared * c.H_shared
+        algo["shared_ffn"] = ((f1 + 1) * Hc * M * eb + 2 * S * M * eb + 2 * S * Hc * eb,
+                              2.0 * (f1 + 1) * S * M * Hc)
+    kernels = []
+    for nm in names:
+        ms = per_kernel[nm]
+        b, fl = algo[nm]
+        gbs = b / (ms * 1e-3) / 1e9
+        ent = {"name": nm, "ms": round(ms, 5), "launches": launches[nm], "bytes": int(b),
+               "GB/s": round(gbs, 1), "hbm_frac": round(gbs / P["hbm"], 4)}
+        if fl:
+            tf = fl / (ms * 1e-3) / 1e12
+            ent.update({"flops": fl, "TFLOP/s": round(tf, 2),
+                        "tensor_frac_sustained": round(tf / P["tc_sustained"], 4),
+                        "tensor_frac_burst": round(tf / P["tc"], 4)})
+        kernels.append(ent)
+    dom = max(("expert_up", "expert_down"), key=lambda nm: per_kernel[nm])
+    db, dfl = algo[dom]
+    dms = per_kernel[dom]
+    # which roofline binds the dominant GEMM: the larger of byte-time and flop-time
+    byte_t, flop_t = db / (P["hbm"] * 1e9), dfl / (P["tc_sustained"] * 1e12)
+    if byte_t >= flop_t:
+        achieved = db / (dms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": P["hbm"], "unit": "GB/s",
+                "frac": round(achieved / P["hbm"], 4)}
+    else:
+        achieved = dfl / (dms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": P["tc_sustained"],
+                "unit": "TFLOP/s", "frac": round(achieved / P["tc_sustained"], 4)}
+    roof.update({"kernel": dom, "peak_source": P["source"] + (" (sustained bf16)" if roof["bound"] == "tensor" else " (copy)"),
+                 "traffic": traffic_for(dom, n), "algorithmic_bytes": int(db),
+                 "algorithmic_flops": dfl})
+
+    tokens = S * args.steps * world
+    value = tokens / (total_ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg["dtype"], "data": "synthetic",
+        "config": dict(workload_desc(cfg, n), parallelism=f"replicas x{world}",
+                       l2="flushed: 256 MiB write before every timed step, outside its events",
+                       rows=R, kept_fraction=round(R / (S * k), 4)),
+        "roofline": roof,
+        "kernels": kernels,
+        "e2e": {"value": round(S * args.steps * world / (e2e_ms * 1e-3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "MoeLayer.forward_from_host -> moe_layer_forward"},
+        "gpu_launches": args.steps * sum(launches[nm] for nm in names),
+        "clocks": clk,
+        "wall_s_timed_region": round(t_wall, 4),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, n, inp)
+    return line
+
+
+# ------------------------------------------------------------------ the oracle on the host
+def _sample_cfg(cfg: dict, tokens: int) -> dict:
+    """A bounded sample of the workload: whole groups when grouped, else a token prefix."""
+    s = dict(cfg)
+    if cfg["G"] > 1:
+        g = max(1, tokens // (cfg["S"] // cfg["G"]))
+        s["G"] = g
+        s["S"] = g * (cfg["S"] // cfg["G"])
+    else:
+        s["S"] = min(cfg["S"], tokens)
+    return s
+
+
+def _oracle_step(cfg, sample_cfg, arrays):
+    from oracle import moe_oracle as O
+    S = sample_cfg["S"]
+    a = dict(arrays)
+    a["x"] = arrays["x"][:S]
+    a["u"] = arrays["u"][:S]
+    y, _, _ = O.layer_forward(a, sample_cfg)
+    return y
+
+
+def cpu_baseline(cfg, n, inp, tokens=2048):
+    sc = _sample_cfg(cfg, tokens)
+    t = time.perf_counter()
+    _oracle_step(cfg, sc, inp.np)
+    dt = time.perf_counter() - t
+    return {"value": round(sc["S"] / dt, 2), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"{sc['S']} tokens ({sc['G']} group(s)) of preset {n}, one oracle layer "
+                      f"forward (numpy fp64), {dt:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from top_gating_expert_gb300.inputs import CONFIGS, make_inputs
+    n = args.config
+    cfg = CONFIGS[n]
+    inp = make_inputs(cfg, preset_number=n)
+    sc = _sample_cfg(cfg, 1024)
+    for _ in range(args.warmup):
+        _oracle_step(cfg, sc, inp.np)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(cfg, sc, inp.np)
+    dt = time.perf_counter() - t
+    value = sc["S"] * args.steps / dt
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"each step: {sc['S']} tokens ({sc['G']} group(s)) of preset {n}, one oracle layer "
+              f"forward (numpy fp64) on {cores} host cores")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(workload_desc(cfg, n), parallelism="host cores (oracle)"),
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        line = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,275 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) Mixture-of-Experts layer forward.
+ *
+ * One GPU computes one MoE layer forward:
+ *   router projection -> softmax / top-k gates -> random 2nd-expert dispatch ->
+ *   per-(group, expert) capacity slots -> expert-contiguous rows -> gather ->
+ *   grouped expert FFN (GEMM1 + activation, GEMM2 + gate) -> combine back to token order,
+ * plus the load-balancing (aux) loss and the router z-loss.
+ *
+ * Sources, by page title and section:
+ *   GShard summary page ("GShard: Scaling Giant Models with Conditional Computation and
+ *     Automatic Sharding"): "MoE Transformer", "Top-2 gating" (Expert capacity, Local
+ *     group dispatching, Auxiliary loss, Random routing), and the dispatch path listing
+ *     "token hidden states -> router scores -> top-k -> capacity / token position
+ *     assignment -> dispatch -> local experts -> combine".
+ *   "04 · 路由、负载均衡与专家并行" (MegaBlocks router and parallelism): §2 router
+ *     (bias-free linear, softmax, top-k, z-loss), §3 load-balancing loss, §6 shared expert.
+ *   "Lec16 Systems for MoE Models": "Switch Transformer" (Softmax(KeepTopK)), "共享专家
+ *     vs. 路由专家", "MoE 训练中的负载均衡", "DeepSeek V3 MoE" (SwiGLU), "MoE Kernel 优化"
+ *     (fused gating kernel, dense token-to-expert table).
+ *
+ * Conventions (every entry point):
+ *   - Pointers named x, W_*, logits, y, *_perm, ws and the fields of moe_route_out_t are
+ *     DEVICE pointers owned by the caller. The library allocates no device memory,
+ *     frees nothing and keeps no pointer after a call returns.
+ *   - moe_config_t pointers are HOST pointers, read during the call only.
+ *   - Calls are asynchronous and ordered on `stream` (NULL = the legacy default stream);
+ *     none synchronises except moe_get_device_status.
+ *   - Row-major tensors; weights in the [out, in] (K-major) layout of a linear layer:
+ *     W_g [E, M]; W_in, W_up [E, H, M]; W_out [E, M, H]; shared Ws_in, Ws_up
+ *     [n_shared, H_shared, M]; Ws_out [n_shared, M, H_shared].
+ *   - Element type of x, weights, x_perm, h, y_perm, y, residual: float (MOE_F32) or
+ *     bf16 (MOE_BF16, raw 16-bit storage). logits, gate, w_perm, bias, u, losses: float.
+ *   - Return value: MOE_OK (0) or a negative MOE_ERR_* code. Host-side checks (shapes,
+ *     nulls, workspace size) fail before anything is launched. Errors found on the
+ *     device (non-finite logits, a bounded wait that ran out, bad device indices) are
+ *     recorded in the workspace's status word and reported by moe_get_device_status.
+ *   - No C++ exception crosses this boundary.
+ */
+#ifndef TOP_GATING_EXPERT_GB300_MOE_H
+#define TOP_GATING_EXPERT_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t */
+
+/* element types and activations */
+enum { MOE_F32 = 0, MOE_BF16 = 1 };
+enum { MOE_ACT_RELU = 0, MOE_ACT_SWIGLU = 1 };
+
+/* status codes */
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1, /* shape, divisibility, null pointer, bad enum            */
+  MOE_ERR_UNSUPPORTED = -2, /* valid but not built: dtype/act/size combination         */
+  MOE_ERR_WORKSPACE = -3,   /* ws too small or misaligned                              */
+  MOE_ERR_CUDA = -4,        /* a CUDA runtime call or a kernel launch failed            */
+  MOE_ERR_TIMEOUT = -5,     /* device: a bounded wait ran out (kernel returned early)   */
+  MOE_ERR_NONFINITE = -6,   /* device: a router logit was NaN or infinite               */
+  MOE_ERR_DEVICE_DATA = -7  /* device: an index or offset read on the device was invalid */
+};
+
+/* drop_reason values */
+enum { MOE_KEPT = 0, MOE_DROP_CAPACITY = 1, MOE_DROP_RANDOM = 2 };
+
+/* workspace kinds for moe_workspace_bytes */
+enum { MOE_WS_STEP = 0, MOE_WS_LAYER = 1 };
+
+/*
+ * Layer configuration. Parameter names follow the pages' problem statement: S tokens,
+ * G groups (GShard "Local group dispatching": S/G consecutive tokens per group), E routed
+ * experts, M = d_model, H = d_ff, k = experts per token, capacity factor, shared experts.
+ *   S >= 1, G >= 1, S % G == 0; 1 <= E <= 256; 1 <= k <= min(E, 8).
+ *   capacity_factor > 0: capacity mode, C = ceil(capacity_factor * k * (S/G) / E) per
+ *     (group, expert) (GShard "Local group dispatching": 2N/(G*E) at factor 1, k = 2);
+ *     capacity_factor <= 0: dropless (no assignment is dropped).
+ *   random_routing: 0/1; 1 needs k == 2 and a non-null u (GShard "Random routing").
+ *   n_shared >= 0 always-on shared experts of hidden size H_shared, each added with
+ *     weight 1 (Lec16 "共享专家 vs. 路由专家").
+ *   bf16: M % 64 == 0, H % 64 == 0 (H % 128 == 0 for SwiGLU), n_shared*H_shared likewise.
+ *   f32: M <= 1024, H <= 4096 (the plain-FMA path for small layers).
+ */
+typedef struct {
+  int32_t S, G, E, M, H, k;
+  float capacity_factor;
+  int32_t random_routing;
+  int32_t n_shared, H_shared;
+  int32_t act;   /* MOE_ACT_* */
+  int32_t dtype; /* MOE_F32 / MOE_BF16 */
+} moe_config_t;
+
+/*
+ * Routing outputs (all device pointers, caller-allocated). R_max = moe_rows_max().
+ *   expert_id   int32 [S, k]  chosen experts, largest logit first; equal logits rank
+ *                             the lower expert index first.
+ *   gate        float [S, k]  Softmax over the k selected logits (= the full softmax's
+ *                             top-k probabilities renormalised); 0 where not kept.
+ *   pos         int32 [S, k]  slot in the (group, expert) queue, -1 when not kept.
+ *                             Queue order: all 1st choices of the group in token order,
+ *                             then all 2nd choices, ...; random-skipped choices take no slot.
+ *   drop_reason uint8 [S, k]  MOE_KEPT / MOE_DROP_CAPACITY / MOE_DROP_RANDOM.
+ *   row         int32 [S, k]  row of the assignment in the expert-contiguous buffers,
+ *                             -1 when not kept.
+ *   counts      int32 [G, E]  kept assignments per (group, expert).
+ *   counts_routed int32 [G, E] top-k choices per (group, expert) before random routing
+ *                             and capacity (the f_e of the aux loss).
+ *   expert_offsets int32 [E+1] first row of each expert; expert_offsets[E] = R rows used.
+ *                             Inside an expert: group by group, each in slot order.
+ *   token_of    int32 [R_max] token of each row (rows >= R untouched).
+ *   w_perm      float [R_max] gate of each row.
+ *   aux_loss    float [1]     E * sum_e f_e * P_e per group, mean over groups; f_e =
+ *                             counts_routed / (S/G * k), P_e = mean softmax probability.
+ *   z_loss      float [1]     mean over tokens of logsumexp(logits)^2.
+ */
+typedef struct {
+  int32_t* expert_id;
+  float* gate;
+  int32_t* pos;
+  uint8_t* drop_reason;
+  int32_t* row;
+  int32_t* counts;
+  int32_t* counts_routed;
+  int32_t* expert_offsets;
+  int32_t* token_of;
+  float* w_perm;
+  float* aux_loss;
+  float* z_loss;
+} moe_route_out_t;
+
+/* ---------------------------------------------------------------- host-only queries */
+
+/* Human-readable name of a status code (static storage). */
+const char* moe_status_string(int status);
+
+/* ABI version of this library (major * 100 + minor). */
+int moe_abi_version(void);
+
+/* MOE_OK if the configuration is valid and built, else the reason. Host only. */
+int moe_validate_config(const moe_config_t* cfg);
+
+/* Capacity per (group, expert); *C = -1 in dropless mode. Host only. */
+int moe_capacity(const moe_config_t* cfg, int32_t* C);
+
+/* Upper bound on kept assignments: min(S*k, G*E*C) in capacity mode, S*k dropless. */
+int moe_rows_max(const moe_config_t* cfg, int64_t* R_max);
+
+/*
+ * Workspace bytes. MOE_WS_STEP: what moe_router, moe_route, moe_expert_* and
+ * moe_shared_ffn need (status word + routing scratch). MOE_WS_LAYER: what
+ * moe_layer_forward needs (the step workspace plus logits, x_perm, h, y_perm and the
+ * shared-expert buffers). Workspaces must be 256-byte aligned and zero-filled once
+ * before first use (the status word lives in their first bytes).
+ */
+int moe_workspace_bytes(const moe_config_t* cfg, int kind, size_t* bytes);
+
+/* Element counts of the packed weight buffers (see moe_pack_weights). */
+int moe_packed_sizes(const moe_config_t* cfg, int64_t* w_in_packed_elems,
+                     int64_t* ws_in_packed_elems, int64_t* ws_out_packed_elems);
+
+/* ---------------------------------------------------------------- weight packing */
+
+/*
+ * Packs the routed experts' first-layer weights once, before any forward.
+ *   ReLU:   W_in_packed [E, H, M] = W_in (W_up unused, may be NULL).
+ *   SwiGLU: W_in_packed [E, 2H, M]; rows come in blocks of 256: block b holds W_in rows
+ *           128b..128b+127 then W_up rows 128b..128b+127, so one 256-wide GEMM tile sees
+ *           a gate column and its up column (Lec16 "DeepSeek V3 MoE":
+ *           (Swish(x W1) * (x W2)) W3 with W1 = W_in, W2 = W_up, W3 = W_out).
+ * W_in_packed must not alias W_in or W_up.
+ */
+int moe_pack_weights(const moe_config_t* cfg, const void* W_in, const void* W_up,
+                     void* W_in_packed, moe_stream_t stream);
+
+/*
+ * Packs the n_shared shared experts as ONE expert whose hidden units are all of theirs
+ * (a sum of FFNs is one FFN over the concatenated hidden dimension):
+ *   Ws_in_packed  [n_shared*H_shared (x2 for SwiGLU, interleaved as above), M]
+ *   Ws_out_packed [M, n_shared*H_shared]
+ */
+int moe_pack_shared_weights(const moe_config_t* cfg, const void* Ws_in, const void* Ws_up,
+                            const void* Ws_out, void* Ws_in_packed, void* Ws_out_packed,
+                            moe_stream_t stream);
+
+/* ---------------------------------------------------------------- the forward steps */
+
+/*
+ * Router projection (MegaBlocks §2: a linear layer without bias; Lec16 "Switch
+ * Transformer": G(x) = Softmax(x W_g)). logits [S, E] float = x [S, M] . W_g[E, M]^T
+ * accumulated in fp32, plus bias[e] when bias (float [E]) is non-null.
+ */
+int moe_router(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
+               float* logits, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Routing from logits [S, E] (float): softmax and logsumexp, top-k and gates, random
+ * 2nd-expert dispatch (keep iff u[t] < 2 / (1 + exp(l1 - l2)) in fp64, u float [S]),
+ * capacity slots, expert-contiguous rows, aux and z losses. Fills every field of *out.
+ * Integer outputs are a pure function of the logits and u (bit-exact, deterministic).
+ * Non-finite logits set MOE_ERR_NONFINITE in the status word.
+ */
+int moe_route(const moe_config_t* cfg, const float* logits, const float* u,
+              const moe_route_out_t* out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Gather: x_perm[r, :] = x[token_of[r], :] for r < expert_offsets[E]. x_perm [R_max, M]. */
+int moe_dispatch(const moe_config_t* cfg, const void* x, const moe_route_out_t* r,
+                 void* x_perm, moe_stream_t stream);
+
+/*
+ * Grouped GEMM 1 with the activation fused in its epilogue, over the ragged expert
+ * segments given by expert_offsets (device):
+ *   ReLU:   h[r, :] = relu(x_perm[r] . W_in[e]^T)                    h_perm [R_max, H]
+ *   SwiGLU: h[r, :] = silu(x_perm[r] . W_in[e]^T) * (x_perm[r] . W_up[e]^T)
+ * fp32 accumulation; h stored in the element type (bf16 rounds once).
+ */
+int moe_expert_up(const moe_config_t* cfg, const void* x_perm, const int32_t* expert_offsets,
+                  const void* W_in_packed, void* h_perm, void* ws, size_t ws_bytes,
+                  moe_stream_t stream);
+
+/* Grouped GEMM 2 with the gate fused in its epilogue:
+ *   y_perm[r, :] = w_perm[r] * (h_perm[r] . W_out[e]^T)                 y_perm [R_max, M] */
+int moe_expert_down(const moe_config_t* cfg, const void* h_perm, const int32_t* expert_offsets,
+                    const float* w_perm, const void* W_out, void* y_perm, void* ws,
+                    size_t ws_bytes, moe_stream_t stream);
+
+/* moe_expert_up followed by moe_expert_down; h_perm is caller scratch [R_max, H]. */
+int moe_expert_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* expert_offsets,
+                   const float* w_perm, const void* W_in_packed, const void* W_out,
+                   void* h_perm, void* y_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The shared experts on every token (weight 1 each):
+ *   shared_out [S, M] = FFN_shared(x) with the packed weights; h_shared [S, n_shared*H_shared]
+ *   is caller scratch. */
+int moe_shared_ffn(const moe_config_t* cfg, const void* x, const void* Ws_in_packed,
+                   const void* Ws_out_packed, void* h_shared, void* shared_out, void* ws,
+                   size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Combine (scatter back to token order): for every token t,
+ *   y[t] = sum over kept choices j, in ascending j, of y_perm[row[t, j]]
+ *          (+ shared_out[t] if non-null) (+ residual[t] if non-null),
+ * summed in fp32 and rounded once. A token with nothing kept gets 0 (+ residual): the
+ * GShard overflow token passes through the residual connection.
+ */
+int moe_combine(const moe_config_t* cfg, const void* y_perm, const moe_route_out_t* r,
+                const void* shared_out, const void* residual, void* y, moe_stream_t stream);
+
+/*
+ * The whole layer: moe_router, moe_route, moe_dispatch, moe_expert_ffn, moe_shared_ffn
+ * (when n_shared > 0) and moe_combine, with the intermediates carved from ws
+ * (MOE_WS_LAYER bytes). logits_out (float [S, E]) receives the router logits when
+ * non-null. W_in_packed / Ws_*_packed come from the pack calls above; bias, u, residual
+ * and the shared weights may be NULL when unused.
+ */
+int moe_layer_forward(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
+                      const void* W_in_packed, const void* W_out, const void* Ws_in_packed,
+                      const void* Ws_out_packed, const float* u, const void* residual, void* y,
+                      float* logits_out, const moe_route_out_t* r, void* ws, size_t ws_bytes,
+                      moe_stream_t stream);
+
+/*
+ * Synchronises `stream`, reads the status word in ws, clears it, and returns MOE_OK or
+ * the device error recorded since the last call (MOE_ERR_TIMEOUT, MOE_ERR_NONFINITE or
+ * MOE_ERR_DEVICE_DATA; MOE_ERR_CUDA if the synchronisation itself failed).
+ */
+int moe_get_device_status(void* ws, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TOP_GATING_EXPERT_GB300_MOE_H */

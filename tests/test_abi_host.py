@@ -1,0 +1,101 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports every function
+include/moe.h declares, and its host-only queries and argument checks behave."""
+
+import ctypes
+import math
+
+import pytest
+
+from top_gating_expert_gb300 import _native as N
+from top_gating_expert_gb300.inputs import CONFIGS, preset
+
+
+def test_exports_every_declared_symbol(native_lib):
+    declared = N.declared_symbols()
+    assert len(declared) >= 19
+    missing = [s for s in declared if not hasattr(native_lib, s)]
+    assert not missing, missing
+    # and the binding declares a prototype for each
+    assert set(declared) == set(N._PROTOTYPES), set(declared) ^ set(N._PROTOTYPES)
+
+
+def test_status_strings(native_lib):
+    for code, name in N.STATUS_NAMES.items():
+        assert native_lib.moe_status_string(code).decode().startswith(name)
+    assert native_lib.moe_abi_version() == 100
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_presets_validate_and_capacity(native_lib, n):
+    from top_gating_expert_gb300 import moe
+    cfg = CONFIGS[n]
+    assert moe.validate(cfg) == 0
+    want_C = None if cfg["capacity_factor"] <= 0 else math.ceil(
+        cfg["capacity_factor"] * cfg["k"] * (cfg["S"] // cfg["G"]) / cfg["E"])
+    assert moe.capacity(cfg) == want_C
+    sk = cfg["S"] * cfg["k"]
+    assert moe.rows_max(cfg) == (sk if want_C is None else min(sk, cfg["G"] * cfg["E"] * want_C))
+    step = moe.workspace_bytes(cfg, N.MOE_WS_STEP)
+    layer = moe.workspace_bytes(cfg, N.MOE_WS_LAYER)
+    assert 0 < step < layer
+    R = moe.rows_max(cfg)
+    eb = 2 if cfg["dtype"] == "bf16" else 4
+    assert layer >= step + R * (2 * cfg["M"] + cfg["H"]) * eb
+
+
+def test_capacity_values(native_lib):
+    from top_gating_expert_gb300 import moe
+    assert moe.capacity(CONFIGS[1]) == 64
+    assert moe.capacity(CONFIGS[2]) == 16
+    assert moe.capacity(CONFIGS[5]) == 2560
+    assert moe.capacity(CONFIGS[3]) is None
+
+
+BAD = [
+    dict(S=100, G=3),             # S % G != 0
+    dict(E=0), dict(E=300),       # expert count
+    dict(k=0), dict(k=9),         # k range
+    dict(k=3, random_routing=1),  # random routing needs k == 2
+    dict(random_routing=2),
+    dict(n_shared=1, H_shared=0),
+]
+
+
+@pytest.mark.parametrize("over", BAD)
+def test_invalid_configs_rejected(native_lib, over):
+    from top_gating_expert_gb300 import moe
+    cfg = preset(2, **over)
+    assert moe.validate(cfg) == -1
+
+
+@pytest.mark.parametrize("over", [dict(M=1000), dict(H=4000), dict(act="swiglu", H=4160)])
+def test_unsupported_shapes(native_lib, over):
+    from top_gating_expert_gb300 import moe
+    assert moe.validate(preset(2, **over)) == -2
+
+
+def test_compute_entry_points_check_arguments_on_host(native_lib):
+    """Null pointers and short workspaces fail before any launch (no GPU needed)."""
+    from top_gating_expert_gb300 import moe
+    c = moe.make_config(CONFIGS[2])
+    L = native_lib
+    out = N.MoeRouteOut()
+    assert L.moe_route(ctypes.byref(c), None, None, ctypes.byref(out), None, 0, None) == -1
+    fake = ctypes.c_void_p(1 << 20)
+    out2 = N.MoeRouteOut(**{f: (1 << 20) for f in N.ROUTE_FIELDS})
+    # workspace too small
+    assert L.moe_route(ctypes.byref(c), fake, fake, ctypes.byref(out2), fake, 16, None) == -3
+    # misaligned workspace
+    need = moe.workspace_bytes(c, N.MOE_WS_STEP)
+    assert L.moe_route(ctypes.byref(c), fake, fake, ctypes.byref(out2), ctypes.c_void_p((1 << 20) + 8),
+                       need, None) == -3
+    assert L.moe_router(ctypes.byref(c), None, fake, None, fake, fake, need, None) == -1
+    assert L.moe_dispatch(ctypes.byref(c), fake, None, fake, None) == -1
+    assert L.moe_combine(ctypes.byref(c), fake, ctypes.byref(out2), None, None, None, None) == -1
+    assert L.moe_expert_ffn(ctypes.byref(c), None, fake, fake, fake, fake, fake, fake, fake, need,
+                            None) == -1
+    assert L.moe_layer_forward(ctypes.byref(c), fake, fake, None, fake, fake, None, None, fake, None,
+                               fake, None, ctypes.byref(out2), fake, 16, None) == -3
+    assert L.moe_get_device_status(None, None) == -1
+    # shared-expert calls need shared experts
+    assert L.moe_shared_ffn(ctypes.byref(c), fake, fake, fake, fake, fake, fake, need, None) == -1

@@ -1,0 +1,194 @@
+"""GPU parity of dispatch, the grouped expert GEMMs, the shared experts and combine, element
+by element against the oracle at sizes that span many tiles, every N-tile width the GEMM
+instantiates, ragged expert segments and ragged M tails."""
+
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from gpu_util import (RTOL, LOGIT_RTOL, assert_close, compare_route, oracle_cfg, route_np, to_np)
+from top_gating_expert_gb300 import _native as N
+from top_gating_expert_gb300 import moe
+from top_gating_expert_gb300.inputs import make_inputs, preset
+
+pytestmark = pytest.mark.gpu
+
+
+def _cfg(**kw):
+    base = dict(S=4096, G=1, E=8, M=512, H=2048, k=2, capacity_factor=0.0, random_routing=0,
+                n_shared=0, H_shared=0, act="relu", dtype="bf16", bias=False)
+    base.update(kw)
+    return base
+
+
+CASES = {
+    # BN 256 (GEMM1 and GEMM2), dropless, K = 512 -> 8 k-blocks (ring wraps twice)
+    "relu_E8_dropless": _cfg(),
+    # SwiGLU (BN 256 packed), GEMM2 N = 384 -> BN 128; capacity + random routing; 2 groups
+    "swiglu_E6_capacity_rr": _cfg(S=3000, G=2, E=6, M=384, H=640, capacity_factor=1.0,
+                                  random_routing=1, act="swiglu"),
+    # BN 64 on both GEMMs, k = 4, skewed bias so some experts are nearly empty
+    "relu_E16_k4_bn64": _cfg(S=2500, E=16, M=192, H=320, k=4, capacity_factor=1.25, bias=True),
+    # shared experts (dense segment) + routed SwiGLU, k = 6
+    "shared_swiglu_k6": _cfg(S=2048, E=16, M=256, H=256, k=6, act="swiglu", n_shared=2,
+                             H_shared=192),
+    # the fp32 path (plain FMA), tiny GShard top-2 with random routing
+    "f32_tiny": preset(1),
+    "f32_swiglu_shared": _cfg(S=200, G=2, E=4, M=32, H=128, k=2, capacity_factor=1.0,
+                              act="swiglu", dtype="f32", n_shared=1, H_shared=128),
+}
+
+
+@pytest.fixture(scope="module", params=sorted(CASES))
+def run(request, native_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    name = request.param
+    cfg = CASES[name]
+    inp = make_inputs(cfg, seed=zlib.crc32(name.encode()) % 10000)
+    dev = "cuda"
+    d = {k: v.to(dev) for k, v in inp.host.items()}
+    R_max = moe.rows_max(cfg)
+    dt = moe.torch_dtype(cfg)
+    ws = moe.workspace(cfg, N.MOE_WS_STEP, dev)
+    out = moe.RouteOutputs.allocate(cfg, dev)
+    logits = torch.empty((cfg["S"], cfg["E"]), dtype=torch.float32, device=dev)
+    moe.router(cfg, d["x"], d["W_g"], d.get("bias"), logits, ws)
+    moe.route(cfg, logits, d["u"] if cfg["random_routing"] else None, out, ws)
+    x_perm = torch.full((R_max, cfg["M"]), float("nan"), dtype=dt, device=dev)
+    moe.dispatch(cfg, d["x"], out, x_perm)
+    W_in_p = moe.pack_weights(cfg, d["W_in"], d.get("W_up"))
+    h_perm = torch.full((R_max, cfg["H"]), float("nan"), dtype=dt, device=dev)
+    y_perm = torch.full((R_max, cfg["M"]), float("nan"), dtype=dt, device=dev)
+    moe.expert_up(cfg, x_perm, out.expert_offsets, W_in_p, h_perm, ws)
+    moe.expert_down(cfg, h_perm, out.expert_offsets, out.w_perm, d["W_out"], y_perm, ws)
+    shared_out = None
+    if cfg["n_shared"]:
+        ps_in, ps_out = moe.pack_shared_weights(cfg, d["Ws_in"], d.get("Ws_up"), d["Ws_out"])
+        h_sh = torch.empty((cfg["S"], cfg["n_shared"] * cfg["H_shared"]), dtype=dt, device=dev)
+        shared_out = torch.empty((cfg["S"], cfg["M"]), dtype=dt, device=dev)
+        moe.shared_ffn(cfg, d["x"], ps_in, ps_out, h_sh, shared_out, ws)
+    y = torch.empty((cfg["S"], cfg["M"]), dtype=dt, device=dev)
+    moe.combine(cfg, y_perm, out, shared_out, None, y)
+    y_res = torch.empty_like(y)
+    moe.combine(cfg, y_perm, out, shared_out, d["x"], y_res)
+    status = moe.device_status(ws)
+    return dict(name=name, cfg=cfg, inp=inp, logits=to_np(logits), route=route_np(out),
+                x_perm=to_np(x_perm), h_perm=to_np(h_perm), y_perm=to_np(y_perm),
+                shared_out=None if shared_out is None else to_np(shared_out), y=to_np(y),
+                y_res=to_np(y_res), status=status, dev=d, W_in_p=W_in_p, out=out, ws=ws)
+
+
+def test_status_ok(run):
+    assert run["status"] == 0
+
+
+def test_router_logits(run):
+    cfg, a = run["cfg"], run["inp"].np
+    ref = O.router_logits(a["x"], a["W_g"], a.get("bias"))
+    assert_close(run["logits"], ref, LOGIT_RTOL[cfg["dtype"]], "logits")
+
+
+def test_route_bit_exact(run):
+    cfg = run["cfg"]
+    o = O.route(run["logits"], oracle_cfg(cfg), run["inp"].np["u"])
+    compare_route(run["route"], o, run["name"])
+
+
+def test_dispatch_exact(run):
+    r = run["route"]
+    R = int(r["expert_offsets"][-1])
+    want = O.dispatch(run["inp"].np["x"], r["token_of"][:R])
+    assert np.array_equal(run["x_perm"][:R], want)
+
+
+def _expert_rows(run):
+    cfg, a, r = run["cfg"], run["inp"].np, run["route"]
+    off = r["expert_offsets"]
+    for e in range(cfg["E"]):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi > lo:
+            yield e, lo, hi, a["x"][r["token_of"][lo:hi]]
+
+
+def test_expert_up_gemm(run):
+    cfg, a = run["cfg"], run["inp"].np
+    for e, lo, hi, xr in _expert_rows(run):
+        A = O._f64(xr) @ O._f64(a["W_in"][e]).T
+        if cfg["act"] == "relu":
+            ref = np.maximum(A, 0)
+        else:
+            ref = A / (1 + np.exp(-A)) * (O._f64(xr) @ O._f64(a["W_up"][e]).T)
+        assert_close(run["h_perm"][lo:hi], ref, RTOL[cfg["dtype"]], f"h expert {e}")
+
+
+def test_expert_down_gemm(run):
+    cfg, a, r = run["cfg"], run["inp"].np, run["route"]
+    for e, lo, hi, xr in _expert_rows(run):
+        W_up = a["W_up"][e] if cfg["act"] == "swiglu" else None
+        ref = O.expert_ffn(xr, a["W_in"][e], a["W_out"][e], cfg["act"], W_up)
+        ref = ref * r["w_perm"][lo:hi, None].astype(np.float64)
+        assert_close(run["y_perm"][lo:hi], ref, RTOL[cfg["dtype"]], f"y_perm expert {e}")
+
+
+def test_shared_experts(run):
+    cfg, a = run["cfg"], run["inp"].np
+    if not cfg["n_shared"]:
+        pytest.skip("no shared experts")
+    ref = O.shared_ffn(O._f64(a["x"]), a, cfg)
+    assert_close(run["shared_out"], ref, RTOL[cfg["dtype"]], "shared_out")
+
+
+def test_combine_is_exact_sum_of_gpu_rows(run):
+    """combine alone: the fp32 sum of the GPU's own y_perm rows (+ shared, + residual),
+    rounded once, equals the fp64 sum to within one rounding of the output type."""
+    cfg, r = run["cfg"], run["route"]
+    S = cfg["S"]
+    ref = np.zeros((S, cfg["M"]))
+    for j in range(cfg["k"]):
+        rows = r["row"][:, j]
+        keep = rows >= 0
+        ref[keep] += run["y_perm"][rows[keep]]
+    if run["shared_out"] is not None:
+        ref += run["shared_out"]
+    mag = np.zeros_like(ref)  # sum of |terms|: bounds the fp32 summation error
+    for j in range(cfg["k"]):
+        rows = r["row"][:, j]
+        keep = rows >= 0
+        mag[keep] += np.abs(run["y_perm"][rows[keep]])
+    if run["shared_out"] is not None:
+        mag += np.abs(run["shared_out"])
+    ulp = 2.0 ** -8 if cfg["dtype"] == "bf16" else 2.0 ** -23  # output rounding, relative
+    sum_err = (cfg["k"] + 3) * 2.0 ** -24
+    err = np.abs(run["y"] - ref)
+    assert np.all(err <= ulp * np.abs(ref) + sum_err * mag), err.max()
+    dropped = np.all(r["row"] < 0, axis=1)
+    if run["shared_out"] is None:
+        assert np.all(run["y"][dropped] == 0)
+    x = run["inp"].np["x"]
+    ref_res = ref + x
+    mag_res = mag + np.abs(x)
+    assert np.all(np.abs(run["y_res"] - ref_res) <= ulp * np.abs(ref_res) + sum_err * mag_res)
+
+
+def test_layer_output_vs_oracle(run):
+    cfg = run["cfg"]
+    y_ref, o, _ = O.layer_forward(run["inp"].np, oracle_cfg(cfg), logits=run["logits"])
+    assert_close(run["y"], y_ref, RTOL[cfg["dtype"]], "y")
+    y_ref_res = y_ref + O._f64(run["inp"].np["x"])
+    assert_close(run["y_res"], y_ref_res, RTOL[cfg["dtype"]], "y + residual")
+
+
+def test_layer_forward_equals_step_calls(run):
+    """moe_layer_forward launches the same kernels: identical bits."""
+    cfg, d = run["cfg"], run["dev"]
+    layer = moe.MoeLayer(cfg, {k: run["inp"].host[k] for k in run["inp"].host})
+    y = layer.forward(d["x"], d["u"] if cfg["random_routing"] else None)
+    assert moe.device_status(layer.ws) == 0
+    assert np.array_equal(to_np(y), run["y"])
+    assert np.array_equal(to_np(layer.logits), run["logits"])
+    y2 = layer.forward(d["x"], d["u"] if cfg["random_routing"] else None, residual=d["x"])
+    assert np.array_equal(to_np(y2), run["y_res"])

@@ -1,0 +1,69 @@
+"""The five workload presets at full size, through moe_layer_forward (the call the
+benchmark times): routing bit-exact over all tokens against the oracle routed from the
+GPU's own logits, sampled token outputs within tolerance, logits against the oracle's own
+fp64 logits on a sample, and the tokens whose routing a near-tie changes counted apart."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from gpu_util import (LOGIT_RTOL, RTOL, assert_close, compare_route, near_tie_tokens, oracle_cfg,
+                      route_np, to_np)
+from top_gating_expert_gb300 import moe
+from top_gating_expert_gb300.inputs import CONFIGS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_preset_full_size(n, native_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    cfg = CONFIGS[n]
+    inp = make_inputs(cfg, preset_number=n)
+    layer = moe.MoeLayer(cfg, inp.host)
+    dev = layer.device
+    x = inp.host["x"].to(dev)
+    u = inp.host["u"].to(dev) if cfg["random_routing"] else None
+    residual = x if n == 5 else None  # the overflow workload: dropped tokens pass through
+    y = layer.forward(x, u, residual)
+    assert moe.device_status(layer.ws) == 0
+    y = to_np(y)
+    logits = to_np(layer.logits)
+    g = route_np(layer.route_out)
+    ocfg = oracle_cfg(cfg)
+    a = inp.np
+
+    # (i) routing from the GPU's logits: bit-exact for every token
+    o = O.route(logits, ocfg, a["u"])
+    compare_route(g, o, f"preset {n}")
+
+    # sampled tokens: random ones, the first and last, and (if any) fully dropped ones
+    rng = np.random.default_rng(n)
+    S = cfg["S"]
+    sample = set(rng.choice(S, size=min(S, 48), replace=False).tolist()) | {0, S - 1}
+    dropped = np.nonzero(np.all(o["pos"] < 0, axis=1))[0]
+    sample |= set(dropped[:8].tolist())
+    sample = np.array(sorted(sample))
+
+    # router logits against the oracle's own fp64 projection on the sample
+    ref_logits = O.router_logits(a["x"][sample], a["W_g"], a.get("bias"))
+    assert_close(logits[sample], ref_logits, LOGIT_RTOL[cfg["dtype"]], "logits")
+
+    # layer output on the sample (oracle routed from the GPU logits)
+    y_ref, _, _ = O.layer_forward(a, ocfg, logits=logits, tokens=sample,
+                                  residual=None if residual is None else a["x"])
+    assert_close(y[sample], y_ref, RTOL[cfg["dtype"]], f"y preset {n}")
+    if len(dropped) and residual is not None:
+        assert np.array_equal(y[dropped], a["x"][dropped])  # pure pass-through
+
+    # (ii) the oracle's own routing: tokens that differ must sit on a near-tie
+    own = O.route(O.router_logits(a["x"], a["W_g"], a.get("bias")), ocfg, a["u"])
+    differ = np.nonzero(np.any(own["expert_id"] != o["expert_id"], axis=1))[0]
+    loose = set(near_tie_tokens(logits, cfg["k"], gap=1e-4).tolist())
+    assert set(differ.tolist()) <= loose, sorted(set(differ.tolist()) - loose)[:10]
+    cascade = np.nonzero(np.any((own["pos"] >= 0) != (o["pos"] >= 0), axis=1))[0]
+    print(f"preset {n}: kept {float((o['pos'] >= 0).mean()):.4f}, near-tie tokens (gap<1e-6) "
+          f"{len(near_tie_tokens(logits, cfg['k']))}, ids changed by near-ties {len(differ)}, "
+          f"drop status changed (incl. cascades) {len(cascade)}")

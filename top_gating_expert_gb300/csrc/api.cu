@@ -1,0 +1,376 @@
+// The C ABI of include/moe.h: argument checks, workspace carving and the order of launches.
+// Every check that can fail does so on the host, before anything is launched.
+#include <math.h>
+#include <string.h>
+
+#include "internal.h"
+
+namespace moe {
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+  return n;
+}
+
+namespace {
+
+int validate(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->S < 1 || c->G < 1 || c->S % c->G != 0) return MOE_ERR_INVALID_ARG;
+  if (c->E < 1 || c->E > 256) return MOE_ERR_INVALID_ARG;
+  if (c->k < 1 || c->k > 8 || c->k > c->E) return MOE_ERR_INVALID_ARG;
+  if (c->M < 1 || c->H < 1) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->act != MOE_ACT_RELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  if (c->random_routing != 0 && c->random_routing != 1) return MOE_ERR_INVALID_ARG;
+  if (c->random_routing && c->k != 2) return MOE_ERR_INVALID_ARG;
+  if (!isfinite(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
+  if (c->n_shared < 0 || (c->n_shared > 0 && c->H_shared < 1)) return MOE_ERR_INVALID_ARG;
+  if (int64_t(c->S) * c->k > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+  const int64_t Hs = int64_t(c->n_shared) * c->H_shared;
+  const bool swiglu = c->act == MOE_ACT_SWIGLU;
+  if (c->dtype == MOE_BF16) {
+    if (c->M % 64 || c->H % (swiglu ? 128 : 64)) return MOE_ERR_UNSUPPORTED;
+    if (Hs % (swiglu ? 128 : 64)) return MOE_ERR_UNSUPPORTED;
+  } else {
+    if (c->M % 4) return MOE_ERR_UNSUPPORTED;  // 16-byte rows for dispatch / combine
+    if (swiglu && (c->H % 128 || Hs % 128)) return MOE_ERR_UNSUPPORTED;
+    if (c->n_shared > 0 && c->H_shared % 4) return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+int capacity_of(const moe_config_t& c, int* C) {
+  if (c.capacity_factor <= 0.f) {
+    *C = -1;
+    return MOE_OK;
+  }
+  const double v = ceil(double(c.capacity_factor) * c.k * (c.S / c.G) / c.E);
+  if (!(v >= 1.0) || v > double(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
+  *C = int(v);
+  return MOE_OK;
+}
+
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws || !aligned256(ws)) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+int check_route_out(const moe_config_t& c, const moe_route_out_t* r) {
+  if (!r || !r->expert_id || !r->gate || !r->pos || !r->drop_reason || !r->row || !r->counts ||
+      !r->counts_routed || !r->expert_offsets || !r->token_of || !r->w_perm || !r->aux_loss ||
+      !r->z_loss)
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+struct Prep {
+  int C = -1;
+  int64_t R_max = 0;
+  WsLayout L;
+};
+
+int prepare(const moe_config_t* cfg, Prep* p) {
+  int rc = validate(cfg);
+  if (rc != MOE_OK) return rc;
+  rc = capacity_of(*cfg, &p->C);
+  if (rc != MOE_OK) return rc;
+  p->R_max = rows_max(*cfg, p->C);
+  p->L = ws_layout(*cfg, p->C);
+  return MOE_OK;
+}
+
+unsigned* status_of(void* ws, const WsLayout& L) {
+  return reinterpret_cast<unsigned*>(static_cast<char*>(ws) + L.status);
+}
+
+// GEMM 1 (+ activation) over `groups` row segments (offsets) or one dense segment.
+int up_proj(const moe_config_t& c, const void* A, int64_t a_rows, const int32_t* offsets,
+            int groups, int rows_dense, int H, const void* W_packed, void* h, unsigned* status,
+            cudaStream_t st) {
+  const bool swiglu = c.act == MOE_ACT_SWIGLU;
+  if (c.dtype == MOE_F32)
+    return launch_ffn_up_f32(c, H, static_cast<const float*>(A), offsets, groups, rows_dense,
+                             a_rows, static_cast<const float*>(W_packed), static_cast<float*>(h),
+                             status, st);
+  GemmDesc d;
+  d.epi = swiglu ? EPI_SWIGLU : EPI_RELU;
+  d.A = A; d.a_rows = a_rows; d.K = c.M;
+  d.N = swiglu ? 2 * H : H;
+  d.B = W_packed; d.b_rows = int64_t(groups) * d.N;
+  d.offsets = offsets; d.groups = groups; d.rows_dense = rows_dense;
+  d.out = h; d.ldo = H;
+  d.status = status;
+  return launch_gemm_bf16(d, st);
+}
+
+// GEMM 2 (x row scale) over the same segments.
+int down_proj(const moe_config_t& c, const void* h, int64_t a_rows, const int32_t* offsets,
+              int groups, int rows_dense, int H, const float* row_scale, const void* W_out, void* y,
+              unsigned* status, cudaStream_t st) {
+  if (c.dtype == MOE_F32)
+    return launch_ffn_down_f32(c, H, static_cast<const float*>(h), offsets, groups, rows_dense,
+                               a_rows, row_scale, static_cast<const float*>(W_out),
+                               static_cast<float*>(y), status, st);
+  GemmDesc d;
+  d.epi = EPI_SCALE;
+  d.A = h; d.a_rows = a_rows; d.K = H;
+  d.N = c.M;
+  d.B = W_out; d.b_rows = int64_t(groups) * c.M;
+  d.offsets = offsets; d.groups = groups; d.rows_dense = rows_dense;
+  d.out = y; d.ldo = c.M;
+  d.row_scale = row_scale;
+  d.status = status;
+  return launch_gemm_bf16(d, st);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument (shape, divisibility, null pointer)";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: valid configuration not supported by this build";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace too small or not 256-byte aligned";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or kernel launch failed";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded device wait ran out";
+    case MOE_ERR_NONFINITE: return "MOE_ERR_NONFINITE: non-finite router logits";
+    case MOE_ERR_DEVICE_DATA: return "MOE_ERR_DEVICE_DATA: invalid index or offset on the device";
+  }
+  return "unknown status";
+}
+
+int moe_abi_version(void) { return 100; }
+
+int moe_validate_config(const moe_config_t* cfg) {
+  Prep p;
+  return prepare(cfg, &p);
+}
+
+int moe_capacity(const moe_config_t* cfg, int32_t* C) {
+  if (!C) return MOE_ERR_INVALID_ARG;
+  Prep p;
+  const int rc = prepare(cfg, &p);
+  if (rc == MOE_OK) *C = p.C;
+  return rc;
+}
+
+int moe_rows_max(const moe_config_t* cfg, int64_t* R_max) {
+  if (!R_max) return MOE_ERR_INVALID_ARG;
+  Prep p;
+  const int rc = prepare(cfg, &p);
+  if (rc == MOE_OK) *R_max = p.R_max;
+  return rc;
+}
+
+int moe_workspace_bytes(const moe_config_t* cfg, int kind, size_t* bytes) {
+  if (!bytes || (kind != MOE_WS_STEP && kind != MOE_WS_LAYER)) return MOE_ERR_INVALID_ARG;
+  Prep p;
+  const int rc = prepare(cfg, &p);
+  if (rc == MOE_OK) *bytes = kind == MOE_WS_STEP ? p.L.step_bytes : p.L.layer_bytes;
+  return rc;
+}
+
+int moe_packed_sizes(const moe_config_t* cfg, int64_t* w_in_packed, int64_t* ws_in_packed,
+                     int64_t* ws_out_packed) {
+  Prep p;
+  const int rc = prepare(cfg, &p);
+  if (rc != MOE_OK) return rc;
+  const int64_t f = cfg->act == MOE_ACT_SWIGLU ? 2 : 1;
+  const int64_t Hs = int64_t(cfg->n_shared) * cfg->H_shared;
+  if (w_in_packed) *w_in_packed = int64_t(cfg->E) * f * cfg->H * cfg->M;
+  if (ws_in_packed) *ws_in_packed = f * Hs * cfg->M;
+  if (ws_out_packed) *ws_out_packed = Hs * cfg->M;
+  return MOE_OK;
+}
+
+int moe_pack_weights(const moe_config_t* cfg, const void* W_in, const void* W_up, void* W_in_packed,
+                     moe_stream_t stream) {
+  Prep p;
+  int rc = prepare(cfg, &p);
+  if (rc != MOE_OK) return rc;
+  const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
+  if (!W_in || !W_in_packed || (swiglu && !W_up)) return MOE_ERR_INVALID_ARG;
+  if (W_in_packed == W_in || W_in_packed == W_up) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(W_in) || !aligned16(W_in_packed) || (swiglu && !aligned16(W_up)))
+    return MOE_ERR_INVALID_ARG;
+  return launch_pack_in(*cfg, cfg->E, cfg->H, W_in, W_up, W_in_packed, stream);
+}
+
+int moe_pack_shared_weights(const moe_config_t* cfg, const void* Ws_in, const void* Ws_up,
+                            const void* Ws_out, void* Ws_in_packed, void* Ws_out_packed,
+                            moe_stream_t stream) {
+  Prep p;
+  int rc = prepare(cfg, &p);
+  if (rc != MOE_OK) return rc;
+  if (cfg->n_shared < 1) return MOE_ERR_INVALID_ARG;
+  const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
+  if (!Ws_in || !Ws_out || !Ws_in_packed || !Ws_out_packed || (swiglu && !Ws_up))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(Ws_in) || !aligned16(Ws_out) || !aligned16(Ws_in_packed) ||
+      !aligned16(Ws_out_packed) || (swiglu && !aligned16(Ws_up)))
+    return MOE_ERR_INVALID_ARG;
+  rc = launch_pack_in(*cfg, 1, cfg->n_shared * cfg->H_shared, Ws_in, Ws_up, Ws_in_packed, stream);
+  if (rc != MOE_OK) return rc;
+  return launch_pack_out_cat(*cfg, Ws_out, Ws_out_packed, stream);
+}
+
+int moe_router(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
+               float* logits, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Prep p;
+  int rc = prepare(cfg, &p);
+  if (rc != MOE_OK) return rc;
+  if (!x || !W_g || !logits) return MOE_ERR_INVALID_ARG;
+  if ((rc = check_ws(ws, ws_bytes, p.L.step_bytes)) != MOE_OK) return rc;
+  if (cfg->dtype == MOE_F32)
+    return launch_router_f32(*cfg, static_cast<const float*>(x), static_cast<const float*>(W_g),
+                             bias, logits, stream);
+  GemmDesc d;
+  d.epi = EPI_F32_BIAS;
+  d.A = x; d.a_rows = cfg->S; d.K = cfg->M;
+  d.B = W_g; d.b_rows = cfg->E; d.N = cfg->E;
+  d.offsets = nullptr; d.groups = 1; d.rows_dense = cfg->S;
+  d.out = logits; d.ldo = cfg->E;
+  d.bias = bias; d.n_valid = cfg->E;
+  d.status = status_of(ws, p.L);
+  return launch_gemm_bf16(d, stream);
+}
+
+int moe_route(const moe_config_t* cfg, const float* logits, const float* u,
+              const moe_route_out_t* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Prep p;
+  int rc = prepare(cfg, &p);
+  if (rc != MOE_OK) return rc;
+  if (!logits || (cfg->random_routing && !u)) return MOE_ERR_INVALID_ARG;
+  if ((rc = check_route_out(*cfg, out)) != MOE_OK) return rc;
+  if ((rc = check_ws(ws, ws_bytes, p.L.step_bytes)) != MOE_OK) return rc;
+  return launch_route(*cfg, p.C, logits, cfg->random_routing ? u : nullptr, *out,
+                      static_cast<char*>(ws), p.L, stream);
+}
+
+int moe_dispatch(const moe_config_t* cfg, const void* x, const moe_route_out_t* r, void* x_perm,
+                 moe_stream_t stream) {
+  Prep p;
+  int rc = prepare(cfg, &p);
+  if (rc != MOE_OK) return rc;
+  if (!x || !x_perm || !r || !r->token_of || !r->expert_offsets) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
+  return launch_dispatch(*cfg, p.R_max, x, r->token_of, r->expert_offsets, x_perm, stream);
+}
+
+int moe_expert_up(const moe_config_t* cfg, const void* x_perm, const int32_t* expert_offsets,
+                  const void* W_in_packed, void* h_perm, void* ws, size_t ws_bytes,
+                  moe_stream_t stream) {
+  Prep p;
+  int rc = prepare(cfg, &p);
+  if (rc != MOE_OK) return rc;
+  if (!x_perm || !expert_offsets || !W_in_packed || !h_perm) return MOE_ERR_INVALID_ARG;
+  if ((rc = check_ws(ws, ws_bytes, p.L.step_bytes)) != MOE_OK) return rc;
+  return up_proj(*cfg, x_perm, p.R_max, expert_offsets, cfg->E, 0, cfg->H, W_in_packed, h_perm,
+                 status_of(ws, p.L), stream);
+}
+
+int moe_expert_down(const moe_config_t* cfg, const void* h_perm, const int32_t* expert_offsets,
+                    const float* w_perm, const void* W_out, void* y_perm, void* ws, size_t ws_bytes,
+                    moe_stream_t stream) {
+  Prep p;
+  int rc = prepare(cfg, &p);
+  if (rc != MOE_OK) return rc;
+  if (!h_perm || !expert_offsets || !w_perm || !W_out || !y_perm) return MOE_ERR_INVALID_ARG;
+  if ((rc = check_ws(ws, ws_bytes, p.L.step_bytes)) != MOE_OK) return rc;
+  return down_proj(*cfg, h_perm, p.R_max, expert_offsets, cfg->E, 0, cfg->H, w_perm, W_out, y_perm,
+                   status_of(ws, p.L), stream);
+}
+
+int moe_expert_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* expert_offsets,
+                   const float* w_perm, const void* W_in_packed, const void* W_out, void* h_perm,
+                   void* y_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  int rc = moe_expert_up(cfg, x_perm, expert_offsets, W_in_packed, h_perm, ws, ws_bytes, stream);
+  if (rc != MOE_OK) return rc;
+  return moe_expert_down(cfg, h_perm, expert_offsets, w_perm, W_out, y_perm, ws, ws_bytes, stream);
+}
+
+int moe_shared_ffn(const moe_config_t* cfg, const void* x, const void* Ws_in_packed,
+                   const void* Ws_out_packed, void* h_shared, void* shared_out, void* ws,
+                   size_t ws_bytes, moe_stream_t stream) {
+  Prep p;
+  int rc = prepare(cfg, &p);
+  if (rc != MOE_OK) return rc;
+  if (cfg->n_shared < 1) return MOE_ERR_INVALID_ARG;
+  if (!x || !Ws_in_packed || !Ws_out_packed || !h_shared || !shared_out) return MOE_ERR_INVALID_ARG;
+  if ((rc = check_ws(ws, ws_bytes, p.L.step_bytes)) != MOE_OK) return rc;
+  const int Hc = cfg->n_shared * cfg->H_shared;
+  unsigned* st = status_of(ws, p.L);
+  rc = up_proj(*cfg, x, cfg->S, nullptr, 1, cfg->S, Hc, Ws_in_packed, h_shared, st, stream);
+  if (rc != MOE_OK) return rc;
+  return down_proj(*cfg, h_shared, cfg->S, nullptr, 1, cfg->S, Hc, nullptr, Ws_out_packed,
+                   shared_out, st, stream);
+}
+
+int moe_combine(const moe_config_t* cfg, const void* y_perm, const moe_route_out_t* r,
+                const void* shared_out, const void* residual, void* y, moe_stream_t stream) {
+  Prep p;
+  int rc = prepare(cfg, &p);
+  if (rc != MOE_OK) return rc;
+  if (!y_perm || !r || !r->row || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(y) || (shared_out && !aligned16(shared_out)) ||
+      (residual && !aligned16(residual)))
+    return MOE_ERR_INVALID_ARG;
+  return launch_combine(*cfg, y_perm, r->row, shared_out, residual, y, p.R_max, stream);
+}
+
+int moe_layer_forward(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
+                      const void* W_in_packed, const void* W_out, const void* Ws_in_packed,
+                      const void* Ws_out_packed, const float* u, const void* residual, void* y,
+                      float* logits_out, const moe_route_out_t* r, void* ws, size_t ws_bytes,
+                      moe_stream_t stream) {
+  Prep p;
+  int rc = prepare(cfg, &p);
+  if (rc != MOE_OK) return rc;
+  if (!x || !W_g || !W_in_packed || !W_out || !y) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_shared > 0 && (!Ws_in_packed || !Ws_out_packed)) return MOE_ERR_INVALID_ARG;
+  if ((rc = check_route_out(*cfg, r)) != MOE_OK) return rc;
+  if ((rc = check_ws(ws, ws_bytes, p.L.layer_bytes)) != MOE_OK) return rc;
+  char* w = static_cast<char*>(ws);
+  float* logits = logits_out ? logits_out : reinterpret_cast<float*>(w + p.L.logits);
+  void* x_perm = w + p.L.x_perm;
+  void* h_perm = w + p.L.h_perm;
+  void* y_perm = w + p.L.y_perm;
+  void* shared_out = cfg->n_shared > 0 ? static_cast<void*>(w + p.L.s_out) : nullptr;
+  if ((rc = moe_router(cfg, x, W_g, bias, logits, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  if ((rc = moe_route(cfg, logits, u, r, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  if ((rc = moe_dispatch(cfg, x, r, x_perm, stream)) != MOE_OK) return rc;
+  if ((rc = moe_expert_ffn(cfg, x_perm, r->expert_offsets, r->w_perm, W_in_packed, W_out, h_perm,
+                           y_perm, ws, ws_bytes, stream)) != MOE_OK)
+    return rc;
+  if (cfg->n_shared > 0 &&
+      (rc = moe_shared_ffn(cfg, x, Ws_in_packed, Ws_out_packed, w + p.L.h_shared, shared_out, ws,
+                           ws_bytes, stream)) != MOE_OK)
+    return rc;
+  return moe_combine(cfg, y_perm, r, shared_out, residual, y, stream);
+}
+
+int moe_get_device_status(void* ws, moe_stream_t stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (word != 0 && cudaMemset(ws, 0, sizeof(word)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (word & kStatusTimeout) return MOE_ERR_TIMEOUT;
+  if (word & kStatusNonfinite) return MOE_ERR_NONFINITE;
+  if (word & kStatusDeviceData) return MOE_ERR_DEVICE_DATA;
+  return MOE_OK;
+}
+
+}  // extern "C"

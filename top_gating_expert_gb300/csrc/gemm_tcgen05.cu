@@ -1,0 +1,576 @@
+// Grouped bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+//   D[r, n] = sum_k A[r, k] * B[g * N + n, k]   for the rows r of group g,
+//
+// A [rows, K] and B [groups * N, K] both row-major (K-major, the [out, in] layout of a
+// linear layer), fp32 accumulation in tensor memory, a fused epilogue:
+//   EPI_F32_BIAS  fp32 out (+ per-column bias)          -- router logits
+//   EPI_RELU      bf16 out = relu(D)                    -- expert GEMM 1, ReLU expert
+//   EPI_SWIGLU    bf16 out = silu(D_gate) * D_up        -- expert GEMM 1, SwiGLU expert
+//   EPI_SCALE     bf16 out = row_scale[r] * D           -- expert GEMM 2 (gate weighting)
+//
+// GShard summary page, "MoE Transformer": each expert is a two-layer FFN of the dense
+// FFN's shape, weighted by its gate in the combination. Lec16 Systems for MoE Models,
+// "DeepSeek V3 MoE": SwiGLU experts. MegaBlocks router chapter §4: the experts' rows come
+// in expert-contiguous segments of uneven length (here read from device offsets, so the
+// host never synchronises to size the grid).
+//
+// Structure (one CTA per SM, persistent over output tiles of 128 x BN):
+//   warp 0      one thread issues TMA loads of A (128 x 64) and B (BN x 64) tiles into a
+//               ring of shared-memory stages (128-byte swizzle), signalling `full` barriers;
+//   warp 1      allocates tensor memory; one thread issues tcgen05.mma (M=128, N=BN,
+//               K=16 per instruction) into one of two TMEM accumulators and commits to the
+//               stage's `empty` barrier and, per tile, to the accumulator's `tfull` barrier;
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..),
+//               apply the fused epilogue, store, then arrive on the accumulator's `tempty`
+//               barrier so the MMA warp can reuse it while the next tile's loads stream in.
+// Tiles are ordered group by group, then by N tile, then by M tile, so the CTAs that run
+// at the same time share each weight tile through L2.
+//
+// Every wait is bounded: after kWaitLimitNs a waiting thread sets the status word's
+// timeout bit and a CTA-wide abort flag; every role then stops, the producer waits for its
+// loads in flight, the MMA thread for its MMAs, and TMEM is freed before the CTA exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // bf16 elements per 128-byte swizzled row
+constexpr int kThreads = 192;
+constexpr int kMaxGroups = 256;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+template <int BN>
+struct Cfg {
+  static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + 16 + 2 * (kMaxGroups + 1) * 4;
+};
+
+struct KParams {
+  const int32_t* offsets;
+  int groups;
+  int rows_dense;
+  int64_t rows_cap;
+  int N, K, n_tiles;
+  void* out;
+  int64_t ldo;
+  const float* row_scale;
+  const float* bias;
+  int n_valid;
+  unsigned* status;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of parity `parity` to complete; false on abort or timeout.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Wait that ignores the abort flag (used only to drain work already issued).
+__device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzled layout TMA
+// writes (8-row x 128-byte atoms, 1024 bytes apart).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = uint64_t((saddr & 0x3FFFFu) >> 4);  // start address, 16-byte units
+  d |= uint64_t(1) << 16;                          // leading-dimension offset (unused here)
+  d |= uint64_t(1024 >> 4) << 32;                  // stride-dimension offset: 8 rows
+  d |= uint64_t(1) << 46;                          // descriptor version
+  d |= uint64_t(2) << 61;                          // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+// 32 lanes x 16 consecutive fp32 columns of tensor memory.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void store_bf16x16(void* dst, const uint32_t (&p)[8]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(p[0], p[1], p[2], p[3]);
+  d[1] = make_uint4(p[4], p[5], p[6], p[7]);
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const KParams p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int* s_total = reinterpret_cast<int*>(s_tmem + 2);
+  int* s_tstart = reinterpret_cast<int*>(s_tmem + 4);  // [groups+1] first m-tile of each group
+  int* s_off = s_tstart + (kMaxGroups + 1);            // [groups+1] first row of each group
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * C::STAGES;
+  const uint32_t tfull0 = empty0 + 8 * C::STAGES;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain_bar = tempty0 + 16;
+  const int G = p.offsets ? p.groups : 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 4);
+    }
+    mbar_init(drain_bar, 1);
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(s_tmem), C::TMEM_COLS);
+  if (warp == 2) {
+    // m-tile prefix over the groups, from the device row offsets
+    bool bad = false;
+    int run = 0;
+    for (int base = 0; base < G; base += 32) {
+      const int g = base + lane;
+      int cnt = 0;
+      if (g < G) {
+        const int lo = p.offsets ? p.offsets[g] : 0;
+        const int hi = p.offsets ? p.offsets[g + 1] : p.rows_dense;
+        if (lo < 0 || hi < lo || int64_t(hi) > p.rows_cap) bad = true;
+        else cnt = (hi - lo + BM - 1) / BM;
+        s_off[g] = lo;
+        if (g == G - 1) s_off[G] = hi;
+      }
+      int v = cnt;
+      for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += n;
+      }
+      if (g < G) s_tstart[g + 1] = run + v;
+      run += __shfl_sync(0xffffffffu, v, 31);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      s_tstart[0] = 0;
+      *s_total = bad ? 0 : run * p.n_tiles;
+      if (bad) atomicOr(p.status, kStatusDeviceData);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int total = *s_total;
+  const int kblocks = p.K / BK;
+
+  // tile t -> group g, first row m0, valid rows, n tile
+  auto decode = [&](int t, int& g, int& m0, int& rows, int& nt) {
+    int lo = 0, hi = G;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_tstart[mid] * p.n_tiles <= t) lo = mid;
+      else hi = mid;
+    }
+    g = lo;
+    const int local = t - s_tstart[g] * p.n_tiles;
+    const int mt = s_tstart[g + 1] - s_tstart[g];
+    nt = local / mt;
+    const int m_t = local % mt;
+    m0 = s_off[g] + m_t * BM;
+    rows = min(BM, s_off[g + 1] - m0);
+  };
+
+  if (warp == 0) {
+    // ---------------- TMA producer: the whole warp walks the schedule, lane 0 issues
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, issued_par = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int g, m0, rows, nt;
+      decode(t, g, m0, rows, nt);
+      const int brow = g * p.N + nt * BN;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        ok = __all_sync(0xffffffffu, wait_bounded(empty0 + 8 * stage, phase ^ 1u, s_abort, p.status));
+        if (!ok) break;
+        if (lane == 0) {
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_expect_tx(fb, C::STAGE_BYTES);
+          tma_load_2d(smem_u32(sA + stage * C::A_BYTES), &tmA, kb * BK, m0, fb);
+          tma_load_2d(smem_u32(sB + stage * C::B_BYTES), &tmB, kb * BK, brow, fb);
+        }
+        __syncwarp();
+        issued |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok && lane == 0) {  // let every load in flight land before the CTA exits
+      for (int s = 0; s < C::STAGES; ++s)
+        if ((issued >> s) & 1u) wait_drain(full0 + 8 * s, (issued_par >> s) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: the whole warp waits, lane 0 issues
+    constexpr uint32_t kIdesc = idesc_bf16(BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true, any = false;
+    int i = 0;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
+      const int acc = i & 1;
+      const uint32_t use = uint32_t(i >> 1) & 1u;
+      ok = __all_sync(0xffffffffu, wait_bounded(tempty0 + 8 * acc, use ^ 1u, s_abort, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d = tmem_base + uint32_t(acc * BN);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        ok = __all_sync(0xffffffffu, wait_bounded(full0 + 8 * stage, phase, s_abort, p.status));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), kIdesc,
+                     (kb | kk) != 0 ? 1u : 0u);
+          mma_commit(empty0 + 8 * stage);
+        }
+        __syncwarp();
+        any = true;
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok && lane == 0) mma_commit(tfull0 + 8 * acc);
+      __syncwarp();
+    }
+    if (!ok && any && lane == 0) {  // every MMA issued must finish before TMEM is freed
+      mma_commit(drain_bar);
+      wait_drain(drain_bar, 0u);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue warps 2..5
+    const int q = warp & 3;  // TMEM lanes 32q..32q+31 = tile rows
+    int i = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
+      const int acc = i & 1;
+      const uint32_t use = uint32_t(i >> 1) & 1u;
+      const bool ok = __all_sync(0xffffffffu, wait_bounded(tfull0 + 8 * acc, use, s_abort, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      int g, m0, rows, nt;
+      decode(t, g, m0, rows, nt);
+      const int r = q * 32 + lane;
+      const bool valid = r < rows;
+      const int64_t grow = int64_t(m0) + r;
+      const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
+      if constexpr (EPI == EPI_F32_BIAS) {
+        float* out = static_cast<float*>(p.out) + grow * p.ldo;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tbase + c0, v);
+          tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = nt * BN + c0 + j;
+              if (n < p.n_valid) out[n] = __uint_as_float(v[j]) + (p.bias ? p.bias[n] : 0.f);
+            }
+          }
+        }
+      } else if constexpr (EPI == EPI_SWIGLU) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + nt * (BN / 2);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN / 2; c0 += 16) {
+          uint32_t gv[16], uv[16];
+          tmem_ld16(tbase + c0, gv);
+          tmem_ld16(tbase + BN / 2 + c0, uv);
+          tmem_ld_wait();
+          if (valid) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float g0 = __uint_as_float(gv[2 * j]), g1 = __uint_as_float(gv[2 * j + 1]);
+              const float h0 = g0 / (1.f + __expf(-g0)) * __uint_as_float(uv[2 * j]);
+              const float h1 = g1 / (1.f + __expf(-g1)) * __uint_as_float(uv[2 * j + 1]);
+              pk[j] = pack_bf16x2(h0, h1);
+            }
+            store_bf16x16(out + c0, pk);
+          }
+        }
+      } else {
+        float scale = 1.f;
+        if (EPI == EPI_SCALE && valid && p.row_scale) scale = p.row_scale[grow];
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + nt * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t v0[16], v1[16];
+          tmem_ld16(tbase + c0, v0);
+          tmem_ld16(tbase + c0 + 16, v1);
+          tmem_ld_wait();
+          if (valid) {
+            uint32_t pk0[8], pk1[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float a0 = __uint_as_float(v0[2 * j]), a1 = __uint_as_float(v0[2 * j + 1]);
+              float b0 = __uint_as_float(v1[2 * j]), b1 = __uint_as_float(v1[2 * j + 1]);
+              if (EPI == EPI_RELU) {
+                a0 = fmaxf(a0, 0.f); a1 = fmaxf(a1, 0.f); b0 = fmaxf(b0, 0.f); b1 = fmaxf(b1, 0.f);
+              } else {
+                a0 *= scale; a1 *= scale; b0 *= scale; b1 *= scale;
+              }
+              pk0[j] = pack_bf16x2(a0, a1);
+              pk1[j] = pack_bf16x2(b0, b1);
+            }
+            store_bf16x16(out + c0, pk0);
+            store_bf16x16(out + c0 + 16, pk1);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, K] matrix; box = 64 columns x box_rows rows.
+int make_map(CUtensorMap* m, const void* base, int64_t rows, int K, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0) return MOE_ERR_INVALID_ARG;
+  cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(K) * 2};
+  cuuint32_t box[2] = {cuuint32_t(BK), cuuint32_t(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+template <int BN, int EPI>
+int run_gemm(const GemmDesc& d, cudaStream_t st) {
+  using C = Cfg<BN>;
+  CUtensorMap ta, tb;
+  int rc = make_map(&ta, d.A, d.a_rows, d.K, BM);
+  if (rc != MOE_OK) return rc;
+  rc = make_map(&tb, d.B, d.b_rows, d.K, BN);
+  if (rc != MOE_OK) return rc;
+  KParams p;
+  p.offsets = d.offsets;
+  p.groups = d.groups;
+  p.rows_dense = d.rows_dense;
+  p.rows_cap = d.a_rows;
+  p.N = d.N;
+  p.K = d.K;
+  p.n_tiles = (d.N + BN - 1) / BN;
+  p.out = d.out;
+  p.ldo = d.ldo;
+  p.row_scale = d.row_scale;
+  p.bias = d.bias;
+  p.n_valid = d.n_valid;
+  p.status = d.status;
+  auto kern = grouped_gemm_kernel<BN, EPI>;
+  MOE_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+  const int64_t m_tiles =
+      d.offsets ? (d.a_rows + BM - 1) / BM + d.groups : (int64_t(d.rows_dense) + BM - 1) / BM;
+  int64_t grid = m_tiles * p.n_tiles;
+  if (grid > num_sms()) grid = num_sms();
+  if (grid < 1) grid = 1;
+  kern<<<unsigned(grid), kThreads, C::SMEM, st>>>(ta, tb, p);
+  MOE_CUDA_CHECK(cudaGetLastError());
+  return MOE_OK;
+}
+
+}  // namespace
+
+int launch_gemm_bf16(const GemmDesc& d, cudaStream_t st) {
+  if (d.K < BK || d.K % BK != 0 || d.N < 1) return MOE_ERR_UNSUPPORTED;
+  if (d.offsets && (d.groups < 1 || d.groups > kMaxGroups)) return MOE_ERR_UNSUPPORTED;
+  if (d.a_rows < 1 || d.a_rows > INT32_MAX || d.b_rows < 1) return MOE_ERR_INVALID_ARG;
+  switch (d.epi) {
+    case EPI_F32_BIAS:
+      if (d.N <= 16) return run_gemm<16, EPI_F32_BIAS>(d, st);
+      if (d.N <= 32) return run_gemm<32, EPI_F32_BIAS>(d, st);
+      if (d.N <= 64) return run_gemm<64, EPI_F32_BIAS>(d, st);
+      if (d.N <= 128) return run_gemm<128, EPI_F32_BIAS>(d, st);
+      if (d.N <= 256) return run_gemm<256, EPI_F32_BIAS>(d, st);
+      return MOE_ERR_UNSUPPORTED;
+    case EPI_SWIGLU:
+      if (d.N % 256 != 0) return MOE_ERR_UNSUPPORTED;
+      return run_gemm<256, EPI_SWIGLU>(d, st);
+    case EPI_RELU:
+      if (d.N % 256 == 0) return run_gemm<256, EPI_RELU>(d, st);
+      if (d.N % 128 == 0) return run_gemm<128, EPI_RELU>(d, st);
+      if (d.N % 64 == 0) return run_gemm<64, EPI_RELU>(d, st);
+      return MOE_ERR_UNSUPPORTED;
+    case EPI_SCALE:
+      if (d.N % 256 == 0) return run_gemm<256, EPI_SCALE>(d, st);
+      if (d.N % 128 == 0) return run_gemm<128, EPI_SCALE>(d, st);
+      if (d.N % 64 == 0) return run_gemm<64, EPI_SCALE>(d, st);
+      return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
+}  // namespace moe

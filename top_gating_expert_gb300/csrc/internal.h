@@ -1,0 +1,123 @@
+// Internal declarations shared by the CUDA translation units of the MoE library.
+// Not part of the public ABI (that is include/moe.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// Bits of the device status word (first 4 bytes of every workspace).
+constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusNonfinite = 2u;
+constexpr unsigned kStatusDeviceData = 4u;
+
+// Tokens per routing chunk (one CTA of the routing kernels).
+constexpr int kRouteChunk = 256;
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Byte offsets of every region carved from a workspace.
+struct WsLayout {
+  int n_cpg = 0;     // routing chunks per group
+  int n_chunks = 0;  // G * n_cpg
+  size_t status = 0, done = 0, hist = 0, hroute = 0, ppart = 0, zpart = 0, rank = 0,
+         gbase = 0, gaux = 0, gz = 0;
+  size_t step_bytes = 0;
+  size_t logits = 0, x_perm = 0, h_perm = 0, y_perm = 0, h_shared = 0, s_out = 0;
+  size_t layer_bytes = 0;
+};
+
+inline int64_t rows_max(const moe_config_t& c, int C) {
+  int64_t sk = int64_t(c.S) * c.k;
+  if (C < 0) return sk;
+  int64_t cap = int64_t(c.G) * c.E * C;
+  return cap < sk ? cap : sk;
+}
+
+inline size_t elem_bytes(const moe_config_t& c) { return c.dtype == MOE_BF16 ? 2 : 4; }
+
+inline WsLayout ws_layout(const moe_config_t& c, int C) {
+  WsLayout L;
+  const int Sg = c.S / c.G;
+  L.n_cpg = (Sg + kRouteChunk - 1) / kRouteChunk;
+  L.n_chunks = c.G * L.n_cpg;
+  size_t o = 0;
+  L.status = o; L.done = o + 4; o += 256;
+  L.hist = o;   o = align256(o + size_t(L.n_chunks) * c.k * c.E * 4);
+  L.hroute = o; o = align256(o + size_t(L.n_chunks) * c.E * 4);
+  L.ppart = o;  o = align256(o + size_t(L.n_chunks) * c.E * 4);
+  L.zpart = o;  o = align256(o + size_t(L.n_chunks) * 4);
+  L.rank = o;   o = align256(o + size_t(c.S) * c.k * 4);
+  L.gbase = o;  o = align256(o + size_t(c.G) * c.E * 4);
+  L.gaux = o;   o = align256(o + size_t(c.G) * 4);
+  L.gz = o;     o = align256(o + size_t(c.G) * 4);
+  L.step_bytes = o;
+  const int64_t R = rows_max(c, C);
+  const size_t eb = elem_bytes(c);
+  const size_t Hs = size_t(c.n_shared) * c.H_shared;
+  L.logits = o; o = align256(o + size_t(c.S) * c.E * 4);
+  L.x_perm = o; o = align256(o + size_t(R) * c.M * eb);
+  L.h_perm = o; o = align256(o + size_t(R) * c.H * eb);
+  L.y_perm = o; o = align256(o + size_t(R) * c.M * eb);
+  L.h_shared = o; o = align256(o + size_t(c.S) * Hs * eb);
+  L.s_out = o;  o = align256(o + (Hs ? size_t(c.S) * c.M * eb : 0));
+  L.layer_bytes = o;
+  return L;
+}
+
+// ------------------------------------------------------------------ launchers
+// route.cu
+int launch_route(const moe_config_t& c, int C, const float* logits, const float* u,
+                 const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st);
+
+// permute.cu
+int launch_dispatch(const moe_config_t& c, int64_t R_max, const void* x, const int32_t* token_of,
+                    const int32_t* offsets, void* x_perm, cudaStream_t st);
+int launch_combine(const moe_config_t& c, const void* y_perm, const int32_t* row,
+                   const void* shared_out, const void* residual, void* y, int64_t R_max,
+                   cudaStream_t st);
+int launch_pack_in(const moe_config_t& c, int groups, int H, const void* W_in, const void* W_up,
+                   void* packed, cudaStream_t st);
+int launch_pack_out_cat(const moe_config_t& c, const void* Ws_out, void* packed, cudaStream_t st);
+
+// gemm_tcgen05.cu : bf16 GEMM D = A . B^T over ragged row groups, tcgen05 + TMA.
+enum GemmEpilogue { EPI_F32_BIAS = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_SCALE = 3 };
+struct GemmDesc {
+  int epi = EPI_RELU;
+  const void* A = nullptr; int64_t a_rows = 0; int K = 0;  // A [a_rows, K] bf16, row-major
+  const void* B = nullptr; int64_t b_rows = 0;             // B [b_rows, K] bf16, row-major
+  int N = 0;                       // B rows per group = GEMM N of each group
+  const int32_t* offsets = nullptr;  // device [groups+1] row offsets into A; null = dense
+  int groups = 1;
+  int rows_dense = 0;              // rows of the single group when offsets is null
+  void* out = nullptr; int64_t ldo = 0;  // output element stride between rows
+  const float* row_scale = nullptr;      // EPI_SCALE: per-row factor (null = 1)
+  const float* bias = nullptr;           // EPI_F32_BIAS: per-column bias (nullable)
+  int n_valid = 0;                       // EPI_F32_BIAS: columns stored
+  unsigned* status = nullptr;
+};
+int launch_gemm_bf16(const GemmDesc& d, cudaStream_t st);
+
+// simt_f32.cu : plain-FMA fp32 path for small layers.
+int launch_router_f32(const moe_config_t& c, const float* x, const float* W_g, const float* bias,
+                      float* logits, cudaStream_t st);
+int launch_ffn_up_f32(const moe_config_t& c, int H, const float* A, const int32_t* offsets,
+                      int groups, int rows_dense, int64_t rows_cap, const float* W_packed,
+                      float* h, unsigned* status, cudaStream_t st);
+int launch_ffn_down_f32(const moe_config_t& c, int H, const float* h, const int32_t* offsets,
+                        int groups, int rows_dense, int64_t rows_cap, const float* row_scale,
+                        const float* W_out, float* y, unsigned* status, cudaStream_t st);
+
+int num_sms();
+
+}  // namespace moe
+
+#define MOE_CUDA_CHECK(call)                       \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return MOE_ERR_CUDA;    \
+  } while (0)

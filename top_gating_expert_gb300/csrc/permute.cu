@@ -1,0 +1,236 @@
+// Dispatch (gather into expert-contiguous rows), combine (gate-weighted scatter back to
+// token order) and the one-time weight packing.
+//
+// GShard summary page: the dispatch path "dispatch -> local expert computation -> combine
+// -> residual"; "Expert capacity": an overflow token gets no expert computation and passes
+// through the residual connection. MegaBlocks router chapter §4: ops.gather / ops.scatter
+// move token rows into and out of expert order. Lec16 Systems for MoE Models, "共享专家 vs.
+// 路由专家": output = SharedFFN(h) + sum_i g_i Expert_i(h).
+//
+// All three are HBM-bound row copies: 16-byte vector accesses, one warp per row, a grid
+// of a few CTAs per SM striding over rows, so every warp keeps several 16-byte loads in
+// flight and every access is fully coalesced.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint4 ld_nc(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// x_perm[r] = x[token_of[r]] for r < offsets[E]; `units` 16-byte units per row.
+__global__ void __launch_bounds__(kThreads) dispatch_kernel(const uint4* __restrict__ x,
+                                                            const int32_t* __restrict__ token_of,
+                                                            const int32_t* __restrict__ offsets,
+                                                            int E, int S, int units, int64_t R_max,
+                                                            uint4* __restrict__ x_perm) {
+  int64_t R = offsets[E];
+  R = R < 0 ? 0 : (R > R_max ? R_max : R);
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
+  for (int64_t r = warp0; r < R; r += nwarps) {
+    const int t = token_of[r];
+    if (unsigned(t) >= unsigned(S)) continue;
+    const uint4* src = x + int64_t(t) * units;
+    uint4* dst = x_perm + r * units;
+    int q = lane;
+    for (; q + 96 < units; q += 128) {
+      const uint4 a = ld_nc(src + q), b = ld_nc(src + q + 32), c = ld_nc(src + q + 64),
+                  d = ld_nc(src + q + 96);
+      st_stream(dst + q, a);
+      st_stream(dst + q + 32, b);
+      st_stream(dst + q + 64, c);
+      st_stream(dst + q + 96, d);
+    }
+    for (; q < units; q += 32) st_stream(dst + q, ld_nc(src + q));
+  }
+}
+
+template <bool kBF16>
+struct Vec8 {  // 16 bytes of elements, widened to fp32
+  static constexpr int n = kBF16 ? 8 : 4;
+  float v[8];
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+  }
+  __device__ __forceinline__ void add(const uint4& u) {
+    if constexpr (kBF16) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        v[2 * i] += f.x;
+        v[2 * i + 1] += f.y;
+      }
+    } else {
+      v[0] += __uint_as_float(u.x);
+      v[1] += __uint_as_float(u.y);
+      v[2] += __uint_as_float(u.z);
+      v[3] += __uint_as_float(u.w);
+    }
+  }
+  __device__ __forceinline__ uint4 pack() const {
+    uint4 u;
+    if constexpr (kBF16) {
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    } else {
+      u.x = __float_as_uint(v[0]);
+      u.y = __float_as_uint(v[1]);
+      u.z = __float_as_uint(v[2]);
+      u.w = __float_as_uint(v[3]);
+    }
+    return u;
+  }
+};
+
+// y[t] = sum_{j kept, ascending} y_perm[row[t,j]] (+ shared[t]) (+ residual[t]); fp32 sum,
+// one rounding.
+template <bool kBF16>
+__global__ void __launch_bounds__(kThreads) combine_kernel(
+    const uint4* __restrict__ y_perm, const int32_t* __restrict__ row, int k, int S, int units,
+    int64_t R_max, const uint4* __restrict__ shared, const uint4* __restrict__ residual,
+    uint4* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
+  for (int64_t t = warp0; t < S; t += nwarps) {
+    int rows[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      rows[j] = -1;
+      if (j < k) {
+        const int r = row[t * k + j];
+        rows[j] = (r >= 0 && r < R_max) ? r : -1;
+      }
+    }
+    for (int q = lane; q < units; q += 32) {
+      Vec8<kBF16> acc;
+      acc.zero();
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (rows[j] >= 0) acc.add(ld_nc(y_perm + int64_t(rows[j]) * units + q));
+      if (shared) acc.add(ld_nc(shared + t * units + q));
+      if (residual) acc.add(ld_nc(residual + t * units + q));
+      st_stream(y + t * units + q, acc.pack());
+    }
+  }
+}
+
+// Packed first-layer weights. ReLU: a copy. SwiGLU: blocks of 256 rows, 128 rows of W_in
+// then the same 128 rows of W_up.
+__global__ void __launch_bounds__(kThreads) pack_in_kernel(const uint4* __restrict__ W_in,
+                                                           const uint4* __restrict__ W_up,
+                                                           int64_t dst_rows, int H, int swiglu,
+                                                           int units, uint4* __restrict__ dst) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
+  const int NR = swiglu ? 2 * H : H;
+  for (int64_t p = warp0; p < dst_rows; p += nwarps) {
+    const int64_t e = p / NR;
+    const int pl = int(p % NR);
+    const uint4* src;
+    if (swiglu) {
+      const int b = pl / 256, i = pl % 256;
+      src = (i < 128) ? W_in + (e * H + b * 128 + i) * units
+                      : W_up + (e * H + b * 128 + (i - 128)) * units;
+    } else {
+      src = W_in + (e * H + pl) * units;
+    }
+    for (int q = lane; q < units; q += 32) dst[p * units + q] = src[q];
+  }
+}
+
+// Ws_out [n_shared, M, Hs] -> [M, n_shared*Hs] (the shared experts' hidden units side by side).
+__global__ void __launch_bounds__(kThreads) pack_out_cat_kernel(const uint4* __restrict__ src,
+                                                                int n_shared, int M, int hs_units,
+                                                                uint4* __restrict__ dst) {
+  const int64_t total = int64_t(n_shared) * M * hs_units;
+  for (int64_t idx = int64_t(blockIdx.x) * kThreads + threadIdx.x; idx < total;
+       idx += int64_t(gridDim.x) * kThreads) {
+    const int q = int(idx % hs_units);
+    const int64_t sm = idx / hs_units;  // s * M + m
+    const int s = int(sm / M), m = int(sm % M);
+    dst[(int64_t(m) * n_shared + s) * hs_units + q] = src[idx];
+  }
+}
+
+unsigned grid_for(int64_t warps_needed) {
+  const int64_t cap = int64_t(num_sms()) * 8;
+  int64_t blocks = (warps_needed * 32 + kThreads - 1) / kThreads;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return unsigned(blocks);
+}
+
+}  // namespace
+
+int launch_dispatch(const moe_config_t& c, int64_t R_max, const void* x, const int32_t* token_of,
+                    const int32_t* offsets, void* x_perm, cudaStream_t st) {
+  const int units = int(c.M * elem_bytes(c) / 16);
+  dispatch_kernel<<<grid_for(R_max), kThreads, 0, st>>>(
+      static_cast<const uint4*>(x), token_of, offsets, c.E, c.S, units, R_max,
+      static_cast<uint4*>(x_perm));
+  MOE_CUDA_CHECK(cudaGetLastError());
+  return MOE_OK;
+}
+
+int launch_combine(const moe_config_t& c, const void* y_perm, const int32_t* row,
+                   const void* shared_out, const void* residual, void* y, int64_t R_max,
+                   cudaStream_t st) {
+  const int units = int(c.M * elem_bytes(c) / 16);
+  const unsigned grid = grid_for(c.S);
+  if (c.dtype == MOE_BF16)
+    combine_kernel<true><<<grid, kThreads, 0, st>>>(
+        static_cast<const uint4*>(y_perm), row, c.k, c.S, units, R_max,
+        static_cast<const uint4*>(shared_out), static_cast<const uint4*>(residual),
+        static_cast<uint4*>(y));
+  else
+    combine_kernel<false><<<grid, kThreads, 0, st>>>(
+        static_cast<const uint4*>(y_perm), row, c.k, c.S, units, R_max,
+        static_cast<const uint4*>(shared_out), static_cast<const uint4*>(residual),
+        static_cast<uint4*>(y));
+  MOE_CUDA_CHECK(cudaGetLastError());
+  return MOE_OK;
+}
+
+int launch_pack_in(const moe_config_t& c, int groups, int H, const void* W_in, const void* W_up,
+                   void* packed, cudaStream_t st) {
+  const int swiglu = c.act == MOE_ACT_SWIGLU;
+  const int units = int(c.M * elem_bytes(c) / 16);
+  const int64_t rows = int64_t(groups) * (swiglu ? 2 * H : H);
+  pack_in_kernel<<<grid_for(rows), kThreads, 0, st>>>(static_cast<const uint4*>(W_in),
+                                                     static_cast<const uint4*>(W_up), rows, H,
+                                                     swiglu, units, static_cast<uint4*>(packed));
+  MOE_CUDA_CHECK(cudaGetLastError());
+  return MOE_OK;
+}
+
+int launch_pack_out_cat(const moe_config_t& c, const void* Ws_out, void* packed, cudaStream_t st) {
+  const int hs_units = int(c.H_shared * elem_bytes(c) / 16);
+  const int64_t total = int64_t(c.n_shared) * c.M * hs_units;
+  pack_out_cat_kernel<<<grid_for((total + 31) / 32), kThreads, 0, st>>>(
+      static_cast<const uint4*>(Ws_out), c.n_shared, c.M, hs_units, static_cast<uint4*>(packed));
+  MOE_CUDA_CHECK(cudaGetLastError());
+  return MOE_OK;
+}
+
+}  // namespace moe

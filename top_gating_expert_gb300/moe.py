@@ -1,0 +1,266 @@
+"""Python binding of the MoE C ABI (include/moe.h): argument marshalling only.
+
+Every step of the forward runs in the library's CUDA kernels; torch supplies device
+memory and the current stream. Importing this module does not need a GPU; calling a
+compute function does, and raises if the library is missing.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _native as N
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = N.lib().moe_status_string(status)
+        super().__init__(f"{where}: {msg.decode() if msg else status}")
+
+
+def _check(rc: int, where: str):
+    if rc != N.MOE_OK:
+        raise MoeError(rc, where)
+
+
+def make_config(cfg: dict) -> N.MoeConfig:
+    """A moe_config_t from a workload dict (keys as in top_gating_expert_gb300.inputs)."""
+    return N.MoeConfig(
+        S=cfg["S"], G=cfg["G"], E=cfg["E"], M=cfg["M"], H=cfg["H"], k=cfg["k"],
+        capacity_factor=float(cfg.get("capacity_factor", 0.0)),
+        random_routing=int(cfg.get("random_routing", 0)),
+        n_shared=int(cfg.get("n_shared", 0)), H_shared=int(cfg.get("H_shared", 0)),
+        act=N.MOE_ACT_SWIGLU if cfg["act"] == "swiglu" else N.MOE_ACT_RELU,
+        dtype=N.MOE_BF16 if cfg["dtype"] == "bf16" else N.MOE_F32)
+
+
+def _cfg(c) -> N.MoeConfig:
+    return c if isinstance(c, N.MoeConfig) else make_config(c)
+
+
+def torch_dtype(cfg) -> torch.dtype:
+    return torch.bfloat16 if _cfg(cfg).dtype == N.MOE_BF16 else torch.float32
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ------------------------------------------------------------------ host-only queries
+def validate(cfg) -> int:
+    return N.lib().moe_validate_config(ctypes.byref(_cfg(cfg)))
+
+
+def capacity(cfg):
+    C = N.c_int32()
+    _check(N.lib().moe_capacity(ctypes.byref(_cfg(cfg)), ctypes.byref(C)), "moe_capacity")
+    return None if C.value < 0 else C.value
+
+
+def rows_max(cfg) -> int:
+    R = N.c_int64()
+    _check(N.lib().moe_rows_max(ctypes.byref(_cfg(cfg)), ctypes.byref(R)), "moe_rows_max")
+    return R.value
+
+
+def workspace_bytes(cfg, kind: int = N.MOE_WS_LAYER) -> int:
+    b = N.c_size_t()
+    _check(N.lib().moe_workspace_bytes(ctypes.byref(_cfg(cfg)), kind, ctypes.byref(b)),
+           "moe_workspace_bytes")
+    return b.value
+
+
+def packed_sizes(cfg):
+    a, b, c = N.c_int64(), N.c_int64(), N.c_int64()
+    _check(N.lib().moe_packed_sizes(ctypes.byref(_cfg(cfg)), ctypes.byref(a), ctypes.byref(b),
+                                    ctypes.byref(c)), "moe_packed_sizes")
+    return a.value, b.value, c.value
+
+
+def workspace(cfg, kind: int = N.MOE_WS_LAYER, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace (torch allocations are 512-byte aligned)."""
+    return torch.zeros(workspace_bytes(cfg, kind), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------ routing outputs
+@dataclass
+class RouteOutputs:
+    expert_id: torch.Tensor
+    gate: torch.Tensor
+    pos: torch.Tensor
+    drop_reason: torch.Tensor
+    row: torch.Tensor
+    counts: torch.Tensor
+    counts_routed: torch.Tensor
+    expert_offsets: torch.Tensor
+    token_of: torch.Tensor
+    w_perm: torch.Tensor
+    aux_loss: torch.Tensor
+    z_loss: torch.Tensor
+
+    @classmethod
+    def allocate(cls, cfg, device="cuda") -> "RouteOutputs":
+        c = _cfg(cfg)
+        R = rows_max(c)
+        z = lambda shape, dt: torch.zeros(shape, dtype=dt, device=device)
+        return cls(expert_id=z((c.S, c.k), torch.int32), gate=z((c.S, c.k), torch.float32),
+                   pos=z((c.S, c.k), torch.int32), drop_reason=z((c.S, c.k), torch.uint8),
+                   row=z((c.S, c.k), torch.int32), counts=z((c.G, c.E), torch.int32),
+                   counts_routed=z((c.G, c.E), torch.int32),
+                   expert_offsets=z((c.E + 1,), torch.int32), token_of=z((R,), torch.int32),
+                   w_perm=z((R,), torch.float32), aux_loss=z((1,), torch.float32),
+                   z_loss=z((1,), torch.float32))
+
+    def struct(self) -> N.MoeRouteOut:
+        return N.MoeRouteOut(**{f: getattr(self, f).data_ptr() for f in N.ROUTE_FIELDS})
+
+
+# ------------------------------------------------------------------ weight packing
+def pack_weights(cfg, W_in, W_up=None, stream=None) -> torch.Tensor:
+    c = _cfg(cfg)
+    n_in, _, _ = packed_sizes(c)
+    packed = torch.empty(n_in, dtype=W_in.dtype, device=W_in.device)
+    _check(N.lib().moe_pack_weights(ctypes.byref(c), _ptr(W_in), _ptr(W_up), _ptr(packed),
+                                    _stream(stream)), "moe_pack_weights")
+    return packed
+
+
+def pack_shared_weights(cfg, Ws_in, Ws_up, Ws_out, stream=None):
+    c = _cfg(cfg)
+    _, n_in, n_out = packed_sizes(c)
+    p_in = torch.empty(n_in, dtype=Ws_in.dtype, device=Ws_in.device)
+    p_out = torch.empty(n_out, dtype=Ws_in.dtype, device=Ws_in.device)
+    _check(N.lib().moe_pack_shared_weights(ctypes.byref(c), _ptr(Ws_in), _ptr(Ws_up), _ptr(Ws_out),
+                                           _ptr(p_in), _ptr(p_out), _stream(stream)),
+           "moe_pack_shared_weights")
+    return p_in, p_out
+
+
+# ------------------------------------------------------------------ forward steps
+def router(cfg, x, W_g, bias, logits, ws, stream=None):
+    _check(N.lib().moe_router(ctypes.byref(_cfg(cfg)), _ptr(x), _ptr(W_g), _ptr(bias), _ptr(logits),
+                              _ptr(ws), ws.numel(), _stream(stream)), "moe_router")
+
+
+def route(cfg, logits, u, out: RouteOutputs, ws, stream=None):
+    s = out.struct()
+    _check(N.lib().moe_route(ctypes.byref(_cfg(cfg)), _ptr(logits), _ptr(u), ctypes.byref(s),
+                             _ptr(ws), ws.numel(), _stream(stream)), "moe_route")
+
+
+def dispatch(cfg, x, out: RouteOutputs, x_perm, stream=None):
+    s = out.struct()
+    _check(N.lib().moe_dispatch(ctypes.byref(_cfg(cfg)), _ptr(x), ctypes.byref(s), _ptr(x_perm),
+                                _stream(stream)), "moe_dispatch")
+
+
+def expert_up(cfg, x_perm, expert_offsets, W_in_packed, h_perm, ws, stream=None):
+    _check(N.lib().moe_expert_up(ctypes.byref(_cfg(cfg)), _ptr(x_perm), _ptr(expert_offsets),
+                                 _ptr(W_in_packed), _ptr(h_perm), _ptr(ws), ws.numel(),
+                                 _stream(stream)), "moe_expert_up")
+
+
+def expert_down(cfg, h_perm, expert_offsets, w_perm, W_out, y_perm, ws, stream=None):
+    _check(N.lib().moe_expert_down(ctypes.byref(_cfg(cfg)), _ptr(h_perm), _ptr(expert_offsets),
+                                   _ptr(w_perm), _ptr(W_out), _ptr(y_perm), _ptr(ws), ws.numel(),
+                                   _stream(stream)), "moe_expert_down")
+
+
+def expert_ffn(cfg, x_perm, expert_offsets, w_perm, W_in_packed, W_out, h_perm, y_perm, ws,
+               stream=None):
+    _check(N.lib().moe_expert_ffn(ctypes.byref(_cfg(cfg)), _ptr(x_perm), _ptr(expert_offsets),
+                                  _ptr(w_perm), _ptr(W_in_packed), _ptr(W_out), _ptr(h_perm),
+                                  _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_expert_ffn")
+
+
+def shared_ffn(cfg, x, Ws_in_packed, Ws_out_packed, h_shared, shared_out, ws, stream=None):
+    _check(N.lib().moe_shared_ffn(ctypes.byref(_cfg(cfg)), _ptr(x), _ptr(Ws_in_packed),
+                                  _ptr(Ws_out_packed), _ptr(h_shared), _ptr(shared_out), _ptr(ws),
+                                  ws.numel(), _stream(stream)), "moe_shared_ffn")
+
+
+def combine(cfg, y_perm, out: RouteOutputs, shared_out, residual, y, stream=None):
+    s = out.struct()
+    _check(N.lib().moe_combine(ctypes.byref(_cfg(cfg)), _ptr(y_perm), ctypes.byref(s),
+                               _ptr(shared_out), _ptr(residual), _ptr(y), _stream(stream)),
+           "moe_combine")
+
+
+def layer_forward(cfg, x, W_g, bias, W_in_packed, W_out, Ws_in_packed, Ws_out_packed, u, residual,
+                  y, logits_out, out: RouteOutputs, ws, stream=None):
+    s = out.struct()
+    _check(N.lib().moe_layer_forward(
+        ctypes.byref(_cfg(cfg)), _ptr(x), _ptr(W_g), _ptr(bias), _ptr(W_in_packed), _ptr(W_out),
+        _ptr(Ws_in_packed), _ptr(Ws_out_packed), _ptr(u), _ptr(residual), _ptr(y), _ptr(logits_out),
+        ctypes.byref(s), _ptr(ws), ws.numel(), _stream(stream)), "moe_layer_forward")
+
+
+def device_status(ws, stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the device status recorded in ws."""
+    return N.lib().moe_get_device_status(_ptr(ws), _stream(stream))
+
+
+# ------------------------------------------------------------------ a layer object
+class MoeLayer:
+    """Weights resident on one GPU (packed once), a workspace and routing outputs.
+
+    ``forward`` runs moe_layer_forward on device tensors; ``forward_from_host`` copies
+    the step's inputs from (pinned) host tensors, runs the layer and copies y and the two
+    losses back."""
+
+    def __init__(self, cfg: dict, weights: dict, device="cuda"):
+        self.cfg_dict = cfg
+        self.cfg = make_config(cfg)
+        _check(validate(self.cfg), "moe_validate_config")
+        dt = torch_dtype(self.cfg)
+        dev = torch.device(device)
+        to = lambda t: None if t is None else t.to(device=dev, dtype=dt).contiguous()
+        self.W_g = to(weights["W_g"])
+        W_in, W_up = to(weights["W_in"]), to(weights.get("W_up"))
+        self.W_out = to(weights["W_out"])
+        self.W_in_packed = pack_weights(self.cfg, W_in, W_up)
+        del W_in, W_up
+        self.bias = None if weights.get("bias") is None else weights["bias"].to(dev, torch.float32)
+        self.Ws_in_packed = self.Ws_out_packed = None
+        if self.cfg.n_shared > 0:
+            self.Ws_in_packed, self.Ws_out_packed = pack_shared_weights(
+                self.cfg, to(weights["Ws_in"]), to(weights.get("Ws_up")), to(weights["Ws_out"]))
+        self.ws = workspace(self.cfg, N.MOE_WS_LAYER, dev)
+        self.route_out = RouteOutputs.allocate(self.cfg, dev)
+        self.logits = torch.zeros((self.cfg.S, self.cfg.E), dtype=torch.float32, device=dev)
+        self.y = torch.empty((self.cfg.S, self.cfg.M), dtype=dt, device=dev)
+        self.device = dev
+
+    def forward(self, x, u=None, residual=None, stream=None):
+        layer_forward(self.cfg, x, self.W_g, self.bias, self.W_in_packed, self.W_out,
+                      self.Ws_in_packed, self.Ws_out_packed, u, residual, self.y, self.logits,
+                      self.route_out, self.ws, stream)
+        return self.y
+
+    def forward_from_host(self, x_host, u_host=None, y_host=None, losses_host=None, stream=None):
+        """x_host (and u_host) pinned CPU tensors; y_host / losses_host pinned outputs."""
+        if not hasattr(self, "_x_dev"):
+            self._x_dev = torch.empty_like(x_host, device=self.device)
+            self._u_dev = None if u_host is None else torch.empty_like(u_host, device=self.device)
+            self._loss_dev = torch.empty(2, dtype=torch.float32, device=self.device)
+        self._x_dev.copy_(x_host, non_blocking=True)
+        if u_host is not None:
+            self._u_dev.copy_(u_host, non_blocking=True)
+        self.forward(self._x_dev, self._u_dev if u_host is not None else None, stream=stream)
+        if y_host is not None:
+            y_host.copy_(self.y, non_blocking=True)
+        if losses_host is not None:
+            self._loss_dev[0:1].copy_(self.route_out.aux_loss)
+            self._loss_dev[1:2].copy_(self.route_out.z_loss)
+            losses_host.copy_(self._loss_dev, non_blocking=True)
+        return y_host
