@@ -371,7 +371,12 @@ def _oracle_step(cfg, sample_cfg, arrays):
     return y
 
 
-def cpu_baseline(cfg, n, inp, tokens=2048):
+def cpu_baseline(cfg, n, inp, target_flops=4e11):
+    """The oracle on a bounded sample: about `target_flops` of fp64 expert-FFN work."""
+    f1 = 3 if cfg["act"] == "swiglu" else 2
+    per_token = 2.0 * f1 * cfg["M"] * cfg["H"] * cfg["k"] + \
+        2.0 * f1 * cfg["M"] * cfg.get("n_shared", 0) * cfg.get("H_shared", 0)
+    tokens = int(max(256, min(cfg["S"], target_flops / per_token)))
     sc = _sample_cfg(cfg, tokens)
     t = time.perf_counter()
     _oracle_step(cfg, sc, inp.np)

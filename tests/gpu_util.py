@@ -36,7 +36,7 @@ def tol_check(gpu, ref, rtol):
     rms = np.sqrt(np.mean(r2 * r2, axis=1, keepdims=True))
     err = np.abs(g2 - r2)
     bad = int(np.count_nonzero(err > rtol * (np.abs(r2) + rms)))
-    big = np.abs(r2) >= rms
+    big = (np.abs(r2) >= rms) & (np.abs(r2) > 0)
     maxrel = float((err[big] / np.abs(r2[big])).max()) if big.any() else 0.0
     return bad, maxrel
 

@@ -402,16 +402,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
       if constexpr (EPI == EPI_F32_BIAS) {
         float* out = static_cast<float*>(p.out) + grow * p.ldo;
+        const bool vec = (p.ldo & 3) == 0;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 16) {
           uint32_t v[16];
           tmem_ld16(tbase + c0, v);
           tmem_ld_wait();
           if (valid) {
+            const int nb = nt * BN + c0;
+            float f[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int n = nt * BN + c0 + j;
-              if (n < p.n_valid) out[n] = __uint_as_float(v[j]) + (p.bias ? p.bias[n] : 0.f);
+            for (int j = 0; j < 16; ++j)
+              f[j] = __uint_as_float(v[j]) + ((p.bias && nb + j < p.n_valid) ? p.bias[nb + j] : 0.f);
+            if (vec && nb + 16 <= p.n_valid) {
+              float4* d = reinterpret_cast<float4*>(out + nb);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) d[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (nb + j < p.n_valid) out[nb + j] = f[j];
             }
           }
         }

@@ -15,8 +15,8 @@ constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned kStatusNonfinite = 2u;
 constexpr unsigned kStatusDeviceData = 4u;
 
-// Tokens per routing chunk (one CTA of the routing kernels).
-constexpr int kRouteChunk = 256;
+// Tokens per routing chunk (one CTA of the routing kernels, one thread per token).
+constexpr int kRouteChunk = 128;
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 

@@ -102,8 +102,9 @@ struct Vec8 {  // 16 bytes of elements, widened to fp32
 };
 
 // y[t] = sum_{j kept, ascending} y_perm[row[t,j]] (+ shared[t]) (+ residual[t]); fp32 sum,
-// one rounding.
-template <bool kBF16>
+// one rounding. One warp per token; each lane owns 16-byte units q, q+32, ...; for two
+// units at a time every row's loads are issued before any is added (KMAX >= k rows).
+template <bool kBF16, int KMAX>
 __global__ void __launch_bounds__(kThreads) combine_kernel(
     const uint4* __restrict__ y_perm, const int32_t* __restrict__ row, int k, int S, int units,
     int64_t R_max, const uint4* __restrict__ shared, const uint4* __restrict__ residual,
@@ -111,25 +112,51 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   for (int64_t t = warp0; t < S; t += nwarps) {
-    int rows[8];
+    int rows[KMAX];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
       rows[j] = -1;
       if (j < k) {
-        const int r = row[t * k + j];
+        const int r = __ldg(row + t * k + j);
         rows[j] = (r >= 0 && r < R_max) ? r : -1;
       }
     }
-    for (int q = lane; q < units; q += 32) {
-      Vec8<kBF16> acc;
-      acc.zero();
+    for (int q0 = lane; q0 < units; q0 += 64) {
+      const int q1 = q0 + 32;
+      const bool has1 = q1 < units;
+      uint4 v0[KMAX], v1[KMAX];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (rows[j] >= 0) acc.add(ld_nc(y_perm + int64_t(rows[j]) * units + q));
-      if (shared) acc.add(ld_nc(shared + t * units + q));
-      if (residual) acc.add(ld_nc(residual + t * units + q));
-      st_stream(y + t * units + q, acc.pack());
+      for (int j = 0; j < KMAX; ++j) {
+        const uint4* src = y_perm + int64_t(rows[j] < 0 ? 0 : rows[j]) * units;
+        v0[j] = rows[j] >= 0 ? __ldg(src + q0) : zero;
+        v1[j] = (rows[j] >= 0 && has1) ? __ldg(src + q1) : zero;
+      }
+      const uint4 s0 = shared ? __ldg(shared + t * units + q0) : zero;
+      const uint4 s1 = (shared && has1) ? __ldg(shared + t * units + q1) : zero;
+      const uint4 r0 = residual ? __ldg(residual + t * units + q0) : zero;
+      const uint4 r1 = (residual && has1) ? __ldg(residual + t * units + q1) : zero;
+      Vec8<kBF16> a0, a1;
+      a0.zero();
+      a1.zero();
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (rows[j] >= 0) {
+          a0.add(v0[j]);
+          a1.add(v1[j]);
+        }
+      }
+      if (shared) {
+        a0.add(s0);
+        a1.add(s1);
+      }
+      if (residual) {
+        a0.add(r0);
+        a1.add(r1);
+      }
+      __stcs(y + t * units + q0, a0.pack());
+      if (has1) __stcs(y + t * units + q1, a1.pack());
     }
   }
 }
@@ -193,21 +220,26 @@ int launch_dispatch(const moe_config_t& c, int64_t R_max, const void* x, const i
   return MOE_OK;
 }
 
+template <bool kBF16>
+void combine_dispatch_k(int k, unsigned grid, cudaStream_t st, const uint4* yp, const int32_t* row,
+                        int S, int units, int64_t R_max, const uint4* sh, const uint4* res,
+                        uint4* y) {
+  if (k <= 2) combine_kernel<kBF16, 2><<<grid, kThreads, 0, st>>>(yp, row, k, S, units, R_max, sh, res, y);
+  else if (k <= 4) combine_kernel<kBF16, 4><<<grid, kThreads, 0, st>>>(yp, row, k, S, units, R_max, sh, res, y);
+  else combine_kernel<kBF16, 8><<<grid, kThreads, 0, st>>>(yp, row, k, S, units, R_max, sh, res, y);
+}
+
 int launch_combine(const moe_config_t& c, const void* y_perm, const int32_t* row,
                    const void* shared_out, const void* residual, void* y, int64_t R_max,
                    cudaStream_t st) {
   const int units = int(c.M * elem_bytes(c) / 16);
   const unsigned grid = grid_for(c.S);
-  if (c.dtype == MOE_BF16)
-    combine_kernel<true><<<grid, kThreads, 0, st>>>(
-        static_cast<const uint4*>(y_perm), row, c.k, c.S, units, R_max,
-        static_cast<const uint4*>(shared_out), static_cast<const uint4*>(residual),
-        static_cast<uint4*>(y));
-  else
-    combine_kernel<false><<<grid, kThreads, 0, st>>>(
-        static_cast<const uint4*>(y_perm), row, c.k, c.S, units, R_max,
-        static_cast<const uint4*>(shared_out), static_cast<const uint4*>(residual),
-        static_cast<uint4*>(y));
+  auto yp = static_cast<const uint4*>(y_perm);
+  auto sh = static_cast<const uint4*>(shared_out);
+  auto res = static_cast<const uint4*>(residual);
+  auto yo = static_cast<uint4*>(y);
+  if (c.dtype == MOE_BF16) combine_dispatch_k<true>(c.k, grid, st, yp, row, c.S, units, R_max, sh, res, yo);
+  else combine_dispatch_k<false>(c.k, grid, st, yp, row, c.S, units, R_max, sh, res, yo);
   MOE_CUDA_CHECK(cudaGetLastError());
   return MOE_OK;
 }

@@ -11,18 +11,21 @@
 // mean(logsumexp(logits)^2); §3: load-balancing loss.
 //
 // Three launches, all on one stream:
-//   1. route_topk_kernel   one CTA per chunk of 256 tokens of one group. A sub-warp per
-//      token computes max / sum-exp / top-k / gates / random-routing decision; the CTA then
-//      ranks its candidates per (choice rank j, expert) with warp match + a scan over warps,
-//      and writes per-chunk histograms, routed counts, softmax-probability partial sums and
-//      logsumexp^2 partial sums.
+//   1. route_topk_kernel   one CTA per chunk of 128 tokens of one group. The chunk's logits
+//      are staged into padded shared memory with coalesced loads; TPT consecutive threads
+//      share a token, each keeping a sorted top-k of its slice of the experts (larger logit
+//      first, lower index on ties), merged by K rounds of a TPT-lane shuffle arg-best; then
+//      max, sum-exp, gates and the random-routing decision. The CTA ranks its candidates per
+//      (choice rank j, expert) with warp match + a scan over warps, and writes per-chunk
+//      histograms, routed counts, per-expert softmax-probability sums and the
+//      logsumexp^2 sum (fixed summation orders: deterministic).
 //   2. route_scan_kernel   one CTA per group: exclusive scan of the chunk histograms in
 //      (choice rank, chunk) order -- the GShard queue order -- giving each chunk's first slot
-//      per (j, expert); kept counts per (group, expert); per-group aux-loss term. The last
+//      per (j, expert); kept counts per (group, expert); the group's aux-loss term. The last
 //      CTA to finish (atomic ticket, no waiting) forms expert_offsets, the per-(group,
-//      expert) first rows, and the two loss scalars.
+//      expert) first rows and the two loss scalars.
 //   3. route_finalize_kernel  one thread per assignment: slot, keep/drop, row, inverse map.
-// Every integer output is a pure function of the logits and u: no atomics decide an order.
+// Every integer output is a pure function of the logits and u: no atomic decides an order.
 #include <float.h>
 #include <math.h>
 
@@ -31,10 +34,12 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = kRouteChunk;  // one token per thread in the rank phase
+constexpr int kThreads = kRouteChunk;  // one token per thread
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 8;
+constexpr int kScanThreads = 1024;
+constexpr int kBatch = 16;  // loads kept in flight per thread in the column scans
 
 struct RouteArgs {
   const float* logits;
@@ -65,209 +70,266 @@ struct RouteArgs {
   float* gz;        // [G]
 };
 
-template <int VPL>
-__global__ void __launch_bounds__(kThreads) route_topk_kernel(RouteArgs a) {
-  __shared__ uint8_t s_id[kRouteChunk * kMaxK];
-  __shared__ uint8_t s_cand[kRouteChunk];
+// GShard random routing: keep the 2nd choice iff u < 2 * g2 with g2 = 1 / (1 + exp(l1 - l2)),
+// the decision of the fp64 evaluation. fp32 decides whenever u lies outside a margin that
+// bounds the fp32 threshold's error: d = l1 - l2 carries <= 2^-24 relative error, expf <= 2
+// ulp, the add and the division <= 1/2 ulp each, so the relative error of the fp32
+// threshold is below (6 + d) * 2^-24; the margin is (8 + d) * 2^-23. Inside it (or when the
+// threshold underflows) the fp64 expression decides.
+__device__ __forceinline__ bool rr_keep(float l1, float l2, float u) {
+  const float d = l1 - l2;
+  const float thr = 2.f / (1.f + expf(d));
+  if (thr > 1e-30f) {
+    const float margin = thr * (8.f + d) * 1.1920929e-7f;
+    if (u < thr - margin) return true;
+    if (u > thr + margin) return false;
+  }
+  return double(u) < 2.0 / (1.0 + exp(double(l1) - double(l2)));
+}
+
+// Larger logit first; equal logits: lower expert index first.
+__device__ __forceinline__ bool ranks_before(float v, int i, float w, int j) {
+  return v > w || (v == w && i < j);
+}
+
+// TPT threads per token (consecutive lanes), each owning experts sub, sub+TPT, ...
+template <int K, int TPT>
+__global__ void __launch_bounds__(kThreads * TPT) route_topk_kernel(RouteArgs a) {
+  constexpr int kT = kThreads * TPT;
+  extern __shared__ float s_log[];  // [kThreads][E + TPT] (padded: conflict-free lanes)
+  __shared__ float s_m[kThreads], s_inv[kThreads], s_pp[kT];
+  __shared__ uint8_t s_id[kThreads * kMaxK];
+  __shared__ uint8_t s_cand[kThreads];
   __shared__ int s_wc[kWarps][kMaxE];
-  __shared__ float s_pacc[kWarps][kMaxE];
-  __shared__ float s_z[kWarps];
   __shared__ int s_route[kMaxE];
+  __shared__ float s_z[kT / 32];
 
   const int c = blockIdx.x;
   const int g = c / a.n_cpg, cc = c % a.n_cpg;
-  const int t0 = g * a.Sg + cc * kRouteChunk;
-  const int nt = min(kRouteChunk, a.Sg - cc * kRouteChunk);
+  const int t0 = g * a.Sg + cc * kThreads;
+  const int nt = min(kThreads, a.Sg - cc * kThreads);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int E = a.E, k = a.k;
+  const int E = a.E, ld = E + TPT;
 
   if (c == 0 && tid == 0) *a.done = 0u;  // ticket counter of route_scan_kernel
-  for (int e = tid; e < E; e += kThreads) s_route[e] = 0;
+  for (int e = tid; e < E; e += kT) s_route[e] = 0;
+
+  // stage the chunk's logits (contiguous rows t0..t0+nt-1) into padded shared memory
+  const float* __restrict__ src = a.logits + size_t(t0) * E;
+  const int n = nt * E;
+  if ((E & 3) == 0 && (ld & 3) == 0) {
+    const float4* __restrict__ src4 = reinterpret_cast<const float4*>(src);
+#pragma unroll 4
+    for (int q = tid; q < n / 4; q += kT) {
+      const int idx = q * 4, r = idx / E, col = idx - r * E;
+      *reinterpret_cast<float4*>(s_log + r * ld + col) = __ldg(src4 + q);
+    }
+  } else {
+#pragma unroll 4
+    for (int q = tid; q < n; q += kT) {
+      const int r = q / E;
+      s_log[r * ld + (q - r * E)] = __ldg(src + q);
+    }
+  }
   __syncthreads();
 
-  // A sub-warp of W lanes handles one token; lane sl holds experts sl, sl+W, ...
-  int W = 32;
-  if (VPL == 1) {
-    W = 1;
-    while (W < E) W <<= 1;
-  }
-  const int sub = lane / W, sl = lane % W, spw = 32 / W;
-  const unsigned sub_mask = (W == 32) ? 0xffffffffu : (((1u << W) - 1u) << (sub * W));
-
-  float pacc[VPL];
-#pragma unroll
-  for (int v = 0; v < VPL; ++v) pacc[v] = 0.f;
+  // token i = tid / TPT; this thread's experts: sub, sub + TPT, ...
+  const int i = tid / TPT, sub = tid % TPT;
+  const bool tok = i < nt;
+  const unsigned tmask = TPT == 32 ? 0xffffffffu : (((1u << TPT) - 1u) << (lane & ~(TPT - 1)));
   float zacc = 0.f;
-
-  for (int i = warp * spw + sub; i < nt; i += kWarps * spw) {
-    const int t = t0 + i;
-    const float* lrow = a.logits + size_t(t) * E;
-    float val[VPL];
+  {
+    float* rowp = s_log + i * ld;
+    float top[K];
+    int id[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      top[j] = -INFINITY;
+      id[j] = 0x7fffffff;
+    }
+    float m = -INFINITY;
     bool bad = false;
-#pragma unroll
-    for (int v = 0; v < VPL; ++v) {
-      const int e = sl + v * W;
-      float x = -INFINITY;
-      if (e < E) {
-        x = __ldg(lrow + e);
-        if (!isfinite(x)) {
+    if (tok) {
+      for (int e = sub; e < E; e += TPT) {
+        float v = rowp[e];
+        if (!isfinite(v)) {
           bad = true;
-          x = -INFINITY;
+          v = -INFINITY;
+          rowp[e] = v;
         }
-      }
-      val[v] = x;
-    }
-    if (bad) atomicOr(a.status, kStatusNonfinite);
-
-    // softmax pieces
-    float mx = -INFINITY;
+        m = fmaxf(m, v);
+        // local sorted list; experts arrive in increasing index, so an equal logit ranks
+        // after the ones already held. Once placed, the rest shift down one slot.
+        if (ranks_before(v, e, top[K - 1], id[K - 1])) {
+          float cv = v;
+          int ci = e;
+          bool placed = false;
 #pragma unroll
-    for (int v = 0; v < VPL; ++v) mx = fmaxf(mx, val[v]);
-    for (int off = W >> 1; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(sub_mask, mx, off, W));
-    if (mx == -INFINITY) mx = 0.f;  // only when every logit was non-finite (already flagged)
-    float ex[VPL], sum = 0.f;
-#pragma unroll
-    for (int v = 0; v < VPL; ++v) {
-      ex[v] = expf(val[v] - mx);
-      sum += ex[v];
-    }
-    for (int off = W >> 1; off > 0; off >>= 1) sum += __shfl_xor_sync(sub_mask, sum, off, W);
-    const float inv = sum > 0.f ? 1.f / sum : 0.f;
-#pragma unroll
-    for (int v = 0; v < VPL; ++v) pacc[v] += ex[v] * inv;
-    if (sl == 0) {
-      const float lse = mx + logf(sum);
-      zacc += lse * lse;
-    }
-
-    // top-k: k rounds of a sub-warp argmax (larger value first, then lower index)
-    unsigned chosen = 0u;
-    int ids[kMaxK];
-    float top[kMaxK];
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j < k) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-          const int e = sl + v * W;
-          if (e < E && !((chosen >> v) & 1u) && (val[v] > bv || (val[v] == bv && e < bi))) {
-            bv = val[v];
-            bi = e;
+          for (int j = 0; j < K; ++j) {
+            if (placed || ranks_before(cv, ci, top[j], id[j])) {
+              const float tv = top[j];
+              const int ti = id[j];
+              top[j] = cv;
+              id[j] = ci;
+              cv = tv;
+              ci = ti;
+              placed = true;
+            }
           }
         }
-        for (int off = W >> 1; off > 0; off >>= 1) {
-          const float ov = __shfl_xor_sync(sub_mask, bv, off, W);
-          const int oi = __shfl_xor_sync(sub_mask, bi, off, W);
-          if (ov > bv || (ov == bv && oi < bi)) {
-            bv = ov;
-            bi = oi;
-          }
+      }
+      if (bad) atomicOr(a.status, kStatusNonfinite);
+    }
+    // merge the TPT local lists: K rounds of a TPT-lane arg-best, the owner pops its head
+    float bestv[K];
+    int besti[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      float bv = top[0];
+      int bi = id[0];
+#pragma unroll
+      for (int off = TPT >> 1; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(tmask, bv, off, TPT);
+        const int oi = __shfl_xor_sync(tmask, bi, off, TPT);
+        if (ranks_before(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
         }
-        ids[j] = bi;
-        top[j] = bv;
-        if (bi % W == sl) chosen |= 1u << (bi / W);
+      }
+      bestv[j] = bv;
+      besti[j] = bi;
+      if (id[0] == bi) {
+#pragma unroll
+        for (int q = 0; q + 1 < K; ++q) {
+          top[q] = top[q + 1];
+          id[q] = id[q + 1];
+        }
+        top[K - 1] = -INFINITY;
+        id[K - 1] = 0x7fffffff;
       }
     }
-
-    if (sl == 0) {
-      // gates: softmax over the k selected logits
-      float gw[kMaxK], gsum = 0.f;
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (j < k) {
-          gw[j] = (top[0] > -INFINITY) ? expf(top[j] - top[0]) : (j == 0 ? 1.f : 0.f);
-          gsum += gw[j];
-        }
+    for (int off = TPT >> 1; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(tmask, m, off, TPT));
+    if (m == -INFINITY) m = 0.f;  // only when every logit was non-finite (already flagged)
+    float s = 0.f;
+    if (tok)
+      for (int e = sub; e < E; e += TPT) s += expf(rowp[e] - m);
+#pragma unroll
+    for (int off = TPT >> 1; off > 0; off >>= 1) s += __shfl_xor_sync(tmask, s, off, TPT);
+
+    if (tok && sub == 0) {
+      const int t = t0 + i;
+      s_m[i] = m;
+      s_inv[i] = s > 0.f ? 1.f / s : 0.f;
+      const float lse = m + logf(s);
+      zacc = lse * lse;
+      // an id can only stay out of range when every logit was non-finite (flagged)
+#pragma unroll
+      for (int j = 0; j < K; ++j)
+        if (besti[j] < 0 || besti[j] >= E) besti[j] = j;
+      // gates: softmax over the K selected logits
+      float gw[K], gsum = 0.f;
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        gw[j] = (bestv[0] > -INFINITY) ? expf(bestv[j] - bestv[0]) : (j == 0 ? 1.f : 0.f);
+        gsum += gw[j];
       }
       unsigned cand = 0xffu;
-      if (a.rr) {
-        // keep the 2nd choice iff u < 2 * g2, g2 = 1 / (1 + exp(l1 - l2)), in fp64
-        const double thr = 2.0 / (1.0 + exp(double(top[0]) - double(top[1])));
-        if (!(double(a.u[t]) < thr)) cand &= ~2u;
-      }
+      if (K == 2 && a.rr && !rr_keep(bestv[0], bestv[1], a.u[t])) cand &= ~2u;
       s_cand[i] = uint8_t(cand);
+      const float ginv = 1.f / gsum;
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (j < k) {
-          a.expert_id[size_t(t) * k + j] = ids[j];
-          a.gate[size_t(t) * k + j] = gw[j] / gsum;
-          s_id[i * kMaxK + j] = uint8_t(ids[j]);
-          atomicAdd(&s_route[ids[j]], 1);
-        }
+      for (int j = 0; j < K; ++j) {
+        a.expert_id[size_t(t) * K + j] = besti[j];
+        a.gate[size_t(t) * K + j] = gw[j] * ginv;
+        s_id[i * kMaxK + j] = uint8_t(besti[j]);
+        atomicAdd(&s_route[besti[j]], 1);
       }
-    }
-  }
-
-  // per-chunk softmax-probability sums (fixed reduction order: deterministic)
-#pragma unroll
-  for (int v = 0; v < VPL; ++v)
-    for (int off = W; off < 32; off <<= 1) pacc[v] += __shfl_xor_sync(0xffffffffu, pacc[v], off);
-  if (sub == 0) {
-#pragma unroll
-    for (int v = 0; v < VPL; ++v) {
-      const int e = sl + v * W;
-      if (e < E) s_pacc[warp][e] = pacc[v];
     }
   }
   for (int off = 16; off > 0; off >>= 1) zacc += __shfl_xor_sync(0xffffffffu, zacc, off);
   if (lane == 0) s_z[warp] = zacc;
   __syncthreads();
-  for (int e = tid; e < E; e += kThreads) {
-    float s = 0.f;
-    for (int w = 0; w < kWarps; ++w) s += s_pacc[w][e];
-    a.ppart[size_t(c) * E + e] = s;
-    a.hroute[size_t(c) * E + e] = s_route[e];
+
+  // per-expert softmax-probability sums over the chunk: tpe threads per expert, each a
+  // strided subset of tokens, partials added in a fixed order
+  {
+    int tpe = kT / E;
+    if (tpe < 1) tpe = 1;
+    for (int base = 0; base < E * tpe; base += kT) {
+      const int x = base + tid;
+      const int e = x / tpe, sb = x % tpe;
+      float acc = 0.f;
+      if (e < E)
+        for (int t = sb; t < nt; t += tpe) acc += expf(s_log[t * ld + e] - s_m[t]) * s_inv[t];
+      s_pp[tid] = acc;
+      __syncthreads();
+      if (e < E && sb == 0) {
+        float sum = 0.f;
+        for (int q = 0; q < tpe; ++q) sum += s_pp[tid + q];
+        a.ppart[size_t(c) * E + e] = sum;
+        a.hroute[size_t(c) * E + e] = s_route[e];
+      }
+      __syncthreads();
+    }
   }
   if (tid == 0) {
-    float s = 0.f;
-    for (int w = 0; w < kWarps; ++w) s += s_z[w];
-    a.zpart[c] = s;
+    float sz = 0.f;
+    for (int w = 0; w < kT / 32; ++w) sz += s_z[w];
+    a.zpart[c] = sz;
   }
 
-  // rank of each candidate among the chunk's earlier candidates of the same (j, e)
-  const int i = tid;
-  const bool valid = i < nt;
+  // rank of each candidate among the chunk's earlier candidates of the same (j, e); the
+  // first kThreads threads hold one token each
+  const bool valid = tid < nt;
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int j = 0; j < k; ++j) {
-    for (int x = tid; x < kWarps * E; x += kThreads) s_wc[x / E][x % E] = 0;
+  for (int j = 0; j < K; ++j) {
+    for (int x = tid; x < kWarps * E; x += kT) s_wc[x / E][x % E] = 0;
     __syncthreads();
-    const bool cand = valid && ((s_cand[i] >> j) & 1u);
-    const int e = cand ? int(s_id[i * kMaxK + j]) : -1;
-    const int key = cand ? e : (1024 + lane);
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    const int rk = __popc(peers & lt_mask);
-    if (cand && rk == 0) s_wc[warp][e] = __popc(peers);
+    int e = -1, rk = 0;
+    if (tid < kThreads) {
+      const bool cnd = valid && ((s_cand[tid] >> j) & 1u);
+      e = cnd ? int(s_id[tid * kMaxK + j]) : -1;
+      const int key = cnd ? e : (1024 + lane);
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      rk = __popc(peers & lt_mask);
+      if (cnd && rk == 0) s_wc[warp][e] = __popc(peers);
+    }
     __syncthreads();
-    for (int e2 = tid; e2 < E; e2 += kThreads) {
+    for (int e2 = tid; e2 < E; e2 += kT) {
       int run = 0;
+#pragma unroll
       for (int w = 0; w < kWarps; ++w) {
         const int v = s_wc[w][e2];
         s_wc[w][e2] = run;
         run += v;
       }
-      a.hist[(size_t(c) * k + j) * E + e2] = run;
+      a.hist[(size_t(c) * K + j) * E + e2] = run;
     }
     __syncthreads();
-    if (valid) a.rank[size_t(t0 + i) * k + j] = cand ? s_wc[warp][e] + rk : -1;
+    if (valid) a.rank[size_t(t0 + tid) * K + j] = e >= 0 ? s_wc[warp][e] + rk : -1;
     __syncthreads();
   }
 }
 
-// Sums of `ncol` columns over rows [0, n) of a row-major [n][ncol] array, in a fixed order:
-// each of P segments of rows is summed in row order, then the segments in segment order.
+// Column sums over rows [0, n) of a row-major [n][ncol] array in a fixed order: P segments
+// of rows, each summed in row order with kBatch loads in flight, then the segments in order.
 template <typename T>
-__device__ void column_sums(const T* base, int ncol, int n, T* s_part, T* out) {
-  int P = 1024 / ncol;
+__device__ void column_sums(const T* __restrict__ base, int ncol, int n, T* s_part, T* out) {
+  int P = kScanThreads / ncol;
   P = P < 1 ? 1 : (P > n ? n : P);
-  if (P < 1) P = 1;
   const int L = (n + P - 1) / P;
   for (int idx = threadIdx.x; idx < ncol * P; idx += blockDim.x) {
     const int col = idx % ncol, s = idx / ncol;
     const int cb = s * L, ce = min(n, cb + L);
     T sum = T(0);
-    for (int r = cb; r < ce; ++r) sum += base[size_t(r) * ncol + col];
+    for (int r0 = cb; r0 < ce; r0 += kBatch) {
+      T v[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) v[q] = (r0 + q < ce) ? base[size_t(r0 + q) * ncol + col] : T(0);
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) sum += v[q];
+    }
     s_part[idx] = sum;
   }
   __syncthreads();
@@ -279,13 +341,30 @@ __device__ void column_sums(const T* base, int ncol, int n, T* s_part, T* out) {
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(1024) route_scan_kernel(RouteArgs a) {
-  __shared__ int s_part[2 * 1024];
+// Fixed-order block reduction of one float per thread (all threads participate).
+__device__ float block_sum(float v, float* s_red) {
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  float r = 0.f;
+  if (warp == 0) {
+    r = lane < int(blockDim.x >> 5) ? s_red[lane] : 0.f;
+    for (int off = 16; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+  }
+  __syncthreads();
+  return r;  // valid in thread 0
+}
+
+__global__ void __launch_bounds__(kScanThreads) route_scan_kernel(RouteArgs a) {
+  __shared__ int s_part[2 * kScanThreads];
   __shared__ int s_tot[kMaxK * kMaxE];
   __shared__ int s_routed[kMaxE];
-  __shared__ float s_fpart[1024];
+  __shared__ float s_fpart[kScanThreads];
   __shared__ float s_psum[kMaxE];
   __shared__ float s_zsum[1];
+  __shared__ float s_red[32];
+  __shared__ int s_off[kMaxE + 1];
   __shared__ int s_last;
 
   const int g = blockIdx.x, tid = threadIdx.x;
@@ -293,19 +372,25 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(RouteArgs a) {
   const size_t c0 = size_t(g) * n;
 
   // candidate histograms: exclusive scan over the group's chunks, per (j, e) column
-  int P = 1024 / ncol;
+  int P = kScanThreads / ncol;
   P = P < 1 ? 1 : (P > n ? n : P);
   const int L = (n + P - 1) / P;
-  int32_t* hist = a.hist + c0 * ncol;
-  for (int idx = tid; idx < ncol * P; idx += 1024) {
+  int32_t* __restrict__ hist = a.hist + c0 * ncol;
+  for (int idx = tid; idx < ncol * P; idx += kScanThreads) {
     const int col = idx % ncol, s = idx / ncol;
     const int cb = s * L, ce = min(n, cb + L);
     int sum = 0;
-    for (int r = cb; r < ce; ++r) sum += hist[size_t(r) * ncol + col];
+    for (int r0 = cb; r0 < ce; r0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) v[q] = (r0 + q < ce) ? hist[size_t(r0 + q) * ncol + col] : 0;
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) sum += v[q];
+    }
     s_part[idx] = sum;
   }
   __syncthreads();
-  for (int col = tid; col < ncol; col += 1024) {
+  for (int col = tid; col < ncol; col += kScanThreads) {
     int run = 0;
     for (int s = 0; s < P; ++s) {
       const int v = s_part[s * ncol + col];
@@ -315,20 +400,24 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(RouteArgs a) {
     s_tot[col] = run;
   }
   __syncthreads();
-  for (int idx = tid; idx < ncol * P; idx += 1024) {
+  for (int idx = tid; idx < ncol * P; idx += kScanThreads) {
     const int col = idx % ncol, s = idx / ncol;
     const int j = col / E, e = col % E;
     int run = s_part[idx];
     for (int jj = 0; jj < j; ++jj) run += s_tot[jj * E + e];  // earlier choice ranks first
     const int cb = s * L, ce = min(n, cb + L);
-    for (int r = cb; r < ce; ++r) {
-      const size_t o = size_t(r) * ncol + col;
-      const int v = hist[o];
-      hist[o] = run;
-      run += v;
+    for (int r0 = cb; r0 < ce; r0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) v[q] = (r0 + q < ce) ? hist[size_t(r0 + q) * ncol + col] : 0;
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        if (r0 + q < ce) hist[size_t(r0 + q) * ncol + col] = run;
+        run += v[q];
+      }
     }
   }
-  for (int e = tid; e < E; e += 1024) {
+  for (int e = tid; e < E; e += kScanThreads) {
     int cand = 0;
     for (int j = 0; j < k; ++j) cand += s_tot[j * E + e];
     a.counts[g * E + e] = (a.C >= 0 && cand > a.C) ? a.C : cand;
@@ -339,12 +428,12 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(RouteArgs a) {
   column_sums<int>(a.hroute + c0 * E, E, n, s_part, s_routed);
   column_sums<float>(a.ppart + c0 * E, E, n, s_fpart, s_psum);
   column_sums<float>(a.zpart + c0, 1, n, s_fpart, s_zsum);
-  for (int e = tid; e < E; e += 1024) a.counts_routed[g * E + e] = s_routed[e];
+  for (int e = tid; e < E; e += kScanThreads) a.counts_routed[g * E + e] = s_routed[e];
+  // aux term of the group: E * sum_e (routed_e / (Sg*k)) * (psum_e / Sg)
+  const float term = tid < E ? float(s_routed[tid]) * s_psum[tid] : 0.f;
+  const float tsum = block_sum(term, s_red);
   if (tid == 0) {
-    // E * sum_e (routed_e / (Sg*k)) * (psum_e / Sg)
-    double acc = 0.0;
-    for (int e = 0; e < E; ++e) acc += double(s_routed[e]) * double(s_psum[e]);
-    a.gaux[g] = float(acc * double(E) / (double(a.Sg) * a.k * double(a.Sg)));
+    a.gaux[g] = float(double(tsum) * double(E) / (double(a.Sg) * a.k * double(a.Sg)));
     a.gz[g] = s_zsum[0];
   }
 
@@ -355,36 +444,68 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(RouteArgs a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int e = tid; e < E; e += 1024) {
+  const int32_t* __restrict__ counts = a.counts;
+  for (int e = tid; e < E; e += kScanThreads) {
     int tot = 0;
-    for (int gg = 0; gg < a.G; ++gg) tot += __ldcg(a.counts + gg * E + e);
+    for (int g0 = 0; g0 < a.G; g0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) v[q] = (g0 + q < a.G) ? __ldcg(counts + (g0 + q) * E + e) : 0;
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) tot += v[q];
+    }
     s_routed[e] = tot;
   }
   __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int e = 0; e < E; ++e) {
-      const int v = s_routed[e];
-      s_routed[e] = run;
-      a.offsets[e] = run;
-      run += v;
+  if (tid < 32) {  // exclusive scan over experts: 8 per lane, then a warp scan
+    const int per = (E + 31) / 32;
+    int loc = 0;
+    for (int q = 0; q < per; ++q) {
+      const int e = tid * per + q;
+      if (e < E) loc += s_routed[e];
     }
-    a.offsets[E] = run;
-    double aux = 0.0, z = 0.0;
-    for (int gg = 0; gg < a.G; ++gg) {
-      aux += double(__ldcg(a.gaux + gg));
-      z += double(__ldcg(a.gz + gg));
+    int inc = loc;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, inc, off);
+      if (tid >= off) inc += v;
     }
-    *a.aux = float(aux / a.G);
-    *a.z = float(z / a.S);
-    *a.done = 0u;
+    int run = inc - loc;
+    for (int q = 0; q < per; ++q) {
+      const int e = tid * per + q;
+      if (e < E) {
+        s_off[e] = run;
+        a.offsets[e] = run;
+        run += s_routed[e];
+      }
+    }
+    if (tid == 31) a.offsets[E] = inc;
+  }
+  {  // loss scalars: fixed-order sums over groups
+    float ga = 0.f, gzs = 0.f;
+    for (int gg = tid; gg < a.G; gg += kScanThreads) {
+      ga += __ldcg(a.gaux + gg);
+      gzs += __ldcg(a.gz + gg);
+    }
+    ga = block_sum(ga, s_red);
+    gzs = block_sum(gzs, s_red);
+    if (tid == 0) {
+      *a.aux = ga / float(a.G);
+      *a.z = gzs / float(a.S);
+      *a.done = 0u;
+    }
   }
   __syncthreads();
-  for (int e = tid; e < E; e += 1024) {
-    int run = s_routed[e];
-    for (int gg = 0; gg < a.G; ++gg) {
-      a.gbase[gg * E + e] = run;
-      run += __ldcg(a.counts + gg * E + e);
+  for (int e = tid; e < E; e += kScanThreads) {
+    int run = s_off[e];
+    for (int g0 = 0; g0 < a.G; g0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) v[q] = (g0 + q < a.G) ? __ldcg(counts + (g0 + q) * E + e) : 0;
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        if (g0 + q < a.G) a.gbase[(g0 + q) * E + e] = run;
+        run += v[q];
+      }
     }
   }
 }
@@ -427,10 +548,30 @@ __global__ void __launch_bounds__(256) route_finalize_kernel(RouteArgs a) {
   a.gate[idx] = gt;
 }
 
+template <int K, int TPT>
+int launch_topk_t(const RouteArgs& a, int n_chunks, cudaStream_t st) {
+  const size_t smem = size_t(kThreads) * (a.E + TPT) * sizeof(float);
+  MOE_CUDA_CHECK(cudaFuncSetAttribute(route_topk_kernel<K, TPT>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+  route_topk_kernel<K, TPT><<<n_chunks, kThreads * TPT, smem, st>>>(a);
+  MOE_CUDA_CHECK(cudaGetLastError());
+  return MOE_OK;
+}
+
+// threads per token: enough lanes that each holds at most 16 experts
+template <int K>
+int launch_topk(const RouteArgs& a, int n_chunks, cudaStream_t st) {
+  if (a.E <= 16) return launch_topk_t<K, 1>(a, n_chunks, st);
+  if (a.E <= 32) return launch_topk_t<K, 2>(a, n_chunks, st);
+  if (a.E <= 64) return launch_topk_t<K, 4>(a, n_chunks, st);
+  return launch_topk_t<K, 8>(a, n_chunks, st);
+}
+
 }  // namespace
 
 int launch_route(const moe_config_t& c, int C, const float* logits, const float* u,
                  const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st) {
+  if (reinterpret_cast<uintptr_t>(logits) % 16 != 0) return MOE_ERR_INVALID_ARG;
   RouteArgs a;
   a.logits = logits;
   a.u = u;
@@ -452,13 +593,19 @@ int launch_route(const moe_config_t& c, int C, const float* logits, const float*
   a.gaux = reinterpret_cast<float*>(ws + L.gaux);
   a.gz = reinterpret_cast<float*>(ws + L.gz);
 
-  const dim3 g1(L.n_chunks);
-  if (c.E <= 32) route_topk_kernel<1><<<g1, kThreads, 0, st>>>(a);
-  else if (c.E <= 64) route_topk_kernel<2><<<g1, kThreads, 0, st>>>(a);
-  else if (c.E <= 128) route_topk_kernel<4><<<g1, kThreads, 0, st>>>(a);
-  else route_topk_kernel<8><<<g1, kThreads, 0, st>>>(a);
-  MOE_CUDA_CHECK(cudaGetLastError());
-  route_scan_kernel<<<c.G, 1024, 0, st>>>(a);
+  int rc;
+  switch (c.k) {
+    case 1: rc = launch_topk<1>(a, L.n_chunks, st); break;
+    case 2: rc = launch_topk<2>(a, L.n_chunks, st); break;
+    case 3: rc = launch_topk<3>(a, L.n_chunks, st); break;
+    case 4: rc = launch_topk<4>(a, L.n_chunks, st); break;
+    case 5: rc = launch_topk<5>(a, L.n_chunks, st); break;
+    case 6: rc = launch_topk<6>(a, L.n_chunks, st); break;
+    case 7: rc = launch_topk<7>(a, L.n_chunks, st); break;
+    default: rc = launch_topk<8>(a, L.n_chunks, st); break;
+  }
+  if (rc != MOE_OK) return rc;
+  route_scan_kernel<<<c.G, kScanThreads, 0, st>>>(a);
   MOE_CUDA_CHECK(cudaGetLastError());
   const int64_t n = int64_t(c.S) * c.k;
   route_finalize_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(a);
