@@ -206,6 +206,30 @@ int moe_router(const moe_config_t* cfg, const void* x, const void* W_g, const fl
 int moe_route(const moe_config_t* cfg, const float* logits, const float* u,
               const moe_route_out_t* out, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/*
+ * moe_route without a workspace, for callers that cannot allocate device memory. The
+ * paper has no counterpart: this is a deployment convenience of this library.
+ *
+ * Who needs it: code that may not call cudaMalloc, for example a plugin running inside a
+ * host framework whose own allocator owns all device memory, or a latency-critical loop
+ * that must not allocate once it has started. Such a caller passes only inputs and
+ * outputs; the routing scratch comes from a fixed 4 MiB array inside this library, which
+ * every GPU that loads the library holds until the process exits.
+ *
+ *   - Same inputs, outputs and results as moe_route (bit-identical).
+ *   - Configurations whose routing scratch exceeds 4 MiB (moe_workspace_bytes with
+ *     MOE_WS_STEP) are rejected with MOE_ERR_WORKSPACE before anything is launched.
+ *   - The first call on each device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (on different streams,
+ *     or from different host threads) race and corrupt each other's results. Order them.
+ *   - device_status (nullable, device int32) receives the call's device status bits:
+ *     0 = ok, 2 = non-finite logits, 4 = invalid device data.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+int moe_route_noalloc(const moe_config_t* cfg, const float* logits, const float* u,
+                      const moe_route_out_t* out, int32_t* device_status, moe_stream_t stream);
+
 /* Gather: x_perm[r, :] = x[token_of[r], :] for r < expert_offsets[E]. x_perm [R_max, M]. */
 int moe_dispatch(const moe_config_t* cfg, const void* x, const moe_route_out_t* r,
                  void* x_perm, moe_stream_t stream);

@@ -157,6 +157,14 @@ def route(cfg, logits, u, out: RouteOutputs, ws, stream=None):
                              _ptr(ws), ws.numel(), _stream(stream)), "moe_route")
 
 
+def route_noalloc(cfg, logits, u, out: RouteOutputs, device_status=None, stream=None):
+    """moe_route without a workspace (scratch in the library's fixed 4 MiB device array),
+    for callers that cannot allocate device memory; see include/moe.h."""
+    s = out.struct()
+    _check(N.lib().moe_route_noalloc(ctypes.byref(_cfg(cfg)), _ptr(logits), _ptr(u), ctypes.byref(s),
+                                     _ptr(device_status), _stream(stream)), "moe_route_noalloc")
+
+
 def dispatch(cfg, x, out: RouteOutputs, x_perm, stream=None):
     s = out.struct()
     _check(N.lib().moe_dispatch(ctypes.byref(_cfg(cfg)), _ptr(x), ctypes.byref(s), _ptr(x_perm),
