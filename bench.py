@@ -45,7 +45,22 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", type=int, default=2, help="workload preset (1..5)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--override", action="append", default=[], metavar="KEY=VALUE",
+                   help="change a field of the preset (smaller cases for profiler captures)")
     return p.parse_args()
+
+
+def preset_for(args) -> dict:
+    from top_gating_expert_gb300.inputs import CONFIGS
+    cfg = dict(CONFIGS[args.config])
+    for kv in args.override:
+        key, val = kv.split("=", 1)
+        if key not in cfg:
+            raise SystemExit(f"unknown preset field {key}")
+        cfg[key] = type(cfg[key])(float(val)) if not isinstance(cfg[key], str) else val
+    if args.override:
+        cfg["name"] += " (" + ", ".join(args.override) + ")"
+    return cfg
 
 
 def workload_desc(cfg: dict, n: int) -> dict:
@@ -165,7 +180,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     n = args.config
-    cfg = CONFIGS[n]
+    cfg = preset_for(args)
     inp = make_inputs(cfg, preset_number=n)
     layer = moe.MoeLayer(cfg, inp.host, device=dev)
     c = layer.cfg
@@ -371,7 +386,7 @@ def _oracle_step(cfg, sample_cfg, arrays):
     return y
 
 
-def cpu_baseline(cfg, n, inp, target_flops=4e11):
+def cpu_baseline(cfg, n, inp, target_flops=1.2e12):
     """The oracle on a bounded sample: about `target_flops` of fp64 expert-FFN work."""
     f1 = 3 if cfg["act"] == "swiglu" else 2
     per_token = 2.0 * f1 * cfg["M"] * cfg["H"] * cfg["k"] + \
@@ -392,7 +407,7 @@ def run_reference(args, rank, world):
         return None
     from top_gating_expert_gb300.inputs import CONFIGS, make_inputs
     n = args.config
-    cfg = CONFIGS[n]
+    cfg = preset_for(args)
     inp = make_inputs(cfg, preset_number=n)
     sc = _sample_cfg(cfg, 1024)
     for _ in range(args.warmup):
