@@ -216,7 +216,7 @@ def run_ours(args, rank, world, local_rank):
         moe.route(c, logits, u, out, ws); mark(2)
         moe.dispatch(c, x, out, x_perm); mark(3)
         moe.expert_up(c, x_perm, out.expert_offsets, layer.W_in_packed, h_perm, ws); mark(4)
-        moe.expert_down(c, h_perm, out.expert_offsets, out.w_perm, layer.W_out, y_perm, ws); mark(5)
+        moe.expert_down(c, h_perm, out.expert_offsets, out.w_perm, layer.W_out_packed, y_perm, ws); mark(5)
         i = 6
         if shared:
             moe.shared_ffn(c, x, layer.Ws_in_packed, layer.Ws_out_packed, h_sh, s_out, ws); mark(i)

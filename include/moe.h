@@ -83,7 +83,8 @@ enum { MOE_WS_STEP = 0, MOE_WS_LAYER = 1 };
  *   n_shared >= 0 always-on shared experts of hidden size H_shared, each added with
  *     weight 1 (Lec16 "共享专家 vs. 路由专家").
  *   bf16: M % 64 == 0, H % 64 == 0 (H % 128 == 0 for SwiGLU), n_shared*H_shared likewise.
- *   f32: M <= 1024, H <= 4096 (the plain-FMA path for small layers).
+ *   f32 (the plain-FMA path, meant for small layers): M % 4 == 0, H % 4 == 0 (H % 128 == 0
+ *     for SwiGLU), H_shared % 4 == 0.
  */
 typedef struct {
   int32_t S, G, E, M, H, k;
@@ -158,29 +159,36 @@ int moe_rows_max(const moe_config_t* cfg, int64_t* R_max);
  */
 int moe_workspace_bytes(const moe_config_t* cfg, int kind, size_t* bytes);
 
-/* Element counts of the packed weight buffers (see moe_pack_weights). */
+/* Element counts of the packed weight buffers (see moe_pack_weights); any may be NULL. */
 int moe_packed_sizes(const moe_config_t* cfg, int64_t* w_in_packed_elems,
-                     int64_t* ws_in_packed_elems, int64_t* ws_out_packed_elems);
+                     int64_t* w_out_packed_elems, int64_t* ws_in_packed_elems,
+                     int64_t* ws_out_packed_elems);
 
 /* ---------------------------------------------------------------- weight packing */
 
 /*
- * Packs the routed experts' first-layer weights once, before any forward.
- *   ReLU:   W_in_packed [E, H, M] = W_in (W_up unused, may be NULL).
- *   SwiGLU: W_in_packed [E, 2H, M]; rows come in blocks of 256: block b holds W_in rows
- *           128b..128b+127 then W_up rows 128b..128b+127, so one 256-wide GEMM tile sees
- *           a gate column and its up column (Lec16 "DeepSeek V3 MoE":
- *           (Swish(x W1) * (x W2)) W3 with W1 = W_in, W2 = W_up, W3 = W_out).
- * W_in_packed must not alias W_in or W_up.
+ * Packs the routed experts' weights once, before any forward, into the layout the grouped
+ * GEMMs stream.
+ *   First layer, logical [E, N1, M]: ReLU N1 = H (W_in; W_up unused, may be NULL); SwiGLU
+ *   N1 = 2H in blocks of 256 rows: block b holds W_in rows 128b..128b+127 then W_up rows
+ *   128b..128b+127, so one 256-wide GEMM tile sees a gate column and its up column
+ *   (Lec16 "DeepSeek V3 MoE": (Swish(x W1) * (x W2)) W3, W1 = W_in, W2 = W_up, W3 = W_out).
+ *   Second layer, logical [E, M, H] = W_out.
+ *   bf16: each logical [groups, N, K] matrix is stored tile-major,
+ *   [groups][N/BN][K/64][BN][64], so every 64-column x BN-row box the GEMM loads is one
+ *   contiguous block (BN = 256, 128 or 64: the GEMM's N tile). fp32: row-major.
+ * Sizes: moe_packed_sizes. Packed buffers must not alias the unpacked ones.
  */
 int moe_pack_weights(const moe_config_t* cfg, const void* W_in, const void* W_up,
-                     void* W_in_packed, moe_stream_t stream);
+                     const void* W_out, void* W_in_packed, void* W_out_packed,
+                     moe_stream_t stream);
 
 /*
  * Packs the n_shared shared experts as ONE expert whose hidden units are all of theirs
- * (a sum of FFNs is one FFN over the concatenated hidden dimension):
- *   Ws_in_packed  [n_shared*H_shared (x2 for SwiGLU, interleaved as above), M]
- *   Ws_out_packed [M, n_shared*H_shared]
+ * (a sum of FFNs is one FFN over the concatenated hidden dimension), in the layouts of
+ * moe_pack_weights:
+ *   Ws_in_packed  logical [n_shared*H_shared (x2 for SwiGLU, interleaved as above), M]
+ *   Ws_out_packed logical [M, n_shared*H_shared]
  */
 int moe_pack_shared_weights(const moe_config_t* cfg, const void* Ws_in, const void* Ws_up,
                             const void* Ws_out, void* Ws_in_packed, void* Ws_out_packed,
@@ -245,15 +253,15 @@ int moe_expert_up(const moe_config_t* cfg, const void* x_perm, const int32_t* ex
                   const void* W_in_packed, void* h_perm, void* ws, size_t ws_bytes,
                   moe_stream_t stream);
 
-/* Grouped GEMM 2 with the gate fused in its epilogue:
+/* Grouped GEMM 2 with the gate fused in its epilogue (W_out_packed from moe_pack_weights):
  *   y_perm[r, :] = w_perm[r] * (h_perm[r] . W_out[e]^T)                 y_perm [R_max, M] */
 int moe_expert_down(const moe_config_t* cfg, const void* h_perm, const int32_t* expert_offsets,
-                    const float* w_perm, const void* W_out, void* y_perm, void* ws,
+                    const float* w_perm, const void* W_out_packed, void* y_perm, void* ws,
                     size_t ws_bytes, moe_stream_t stream);
 
 /* moe_expert_up followed by moe_expert_down; h_perm is caller scratch [R_max, H]. */
 int moe_expert_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* expert_offsets,
-                   const float* w_perm, const void* W_in_packed, const void* W_out,
+                   const float* w_perm, const void* W_in_packed, const void* W_out_packed,
                    void* h_perm, void* y_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* The shared experts on every token (weight 1 each):
@@ -277,11 +285,11 @@ int moe_combine(const moe_config_t* cfg, const void* y_perm, const moe_route_out
  * The whole layer: moe_router, moe_route, moe_dispatch, moe_expert_ffn, moe_shared_ffn
  * (when n_shared > 0) and moe_combine, with the intermediates carved from ws
  * (MOE_WS_LAYER bytes). logits_out (float [S, E]) receives the router logits when
- * non-null. W_in_packed / Ws_*_packed come from the pack calls above; bias, u, residual
+ * non-null. W_*_packed / Ws_*_packed come from the pack calls above; bias, u, residual
  * and the shared weights may be NULL when unused.
  */
 int moe_layer_forward(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
-                      const void* W_in_packed, const void* W_out, const void* Ws_in_packed,
+                      const void* W_in_packed, const void* W_out_packed, const void* Ws_in_packed,
                       const void* Ws_out_packed, const float* u, const void* residual, void* y,
                       float* logits_out, const moe_route_out_t* r, void* ws, size_t ws_bytes,
                       moe_stream_t stream);

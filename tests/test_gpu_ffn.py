@@ -60,11 +60,11 @@ def run(request, native_lib):
     moe.route(cfg, logits, d["u"] if cfg["random_routing"] else None, out, ws)
     x_perm = torch.full((R_max, cfg["M"]), float("nan"), dtype=dt, device=dev)
     moe.dispatch(cfg, d["x"], out, x_perm)
-    W_in_p = moe.pack_weights(cfg, d["W_in"], d.get("W_up"))
+    W_in_p, W_out_p = moe.pack_weights(cfg, d["W_in"], d.get("W_up"), d["W_out"])
     h_perm = torch.full((R_max, cfg["H"]), float("nan"), dtype=dt, device=dev)
     y_perm = torch.full((R_max, cfg["M"]), float("nan"), dtype=dt, device=dev)
     moe.expert_up(cfg, x_perm, out.expert_offsets, W_in_p, h_perm, ws)
-    moe.expert_down(cfg, h_perm, out.expert_offsets, out.w_perm, d["W_out"], y_perm, ws)
+    moe.expert_down(cfg, h_perm, out.expert_offsets, out.w_perm, W_out_p, y_perm, ws)
     shared_out = None
     if cfg["n_shared"]:
         ps_in, ps_out = moe.pack_shared_weights(cfg, d["Ws_in"], d.get("Ws_up"), d["Ws_out"])

@@ -43,8 +43,9 @@ _PROTOTYPES = {
     "moe_capacity": [_P(MoeConfig), _P(c_int32)],
     "moe_rows_max": [_P(MoeConfig), _P(c_int64)],
     "moe_workspace_bytes": [_P(MoeConfig), ctypes.c_int, _P(c_size_t)],
-    "moe_packed_sizes": [_P(MoeConfig), _P(c_int64), _P(c_int64), _P(c_int64)],
-    "moe_pack_weights": [_P(MoeConfig), c_void_p, c_void_p, c_void_p, c_void_p],
+    "moe_packed_sizes": [_P(MoeConfig), _P(c_int64), _P(c_int64), _P(c_int64), _P(c_int64)],
+    "moe_pack_weights": [_P(MoeConfig), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                         c_void_p],
     "moe_pack_shared_weights": [_P(MoeConfig), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                 c_void_p],
     "moe_router": [_P(MoeConfig), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,

@@ -35,7 +35,7 @@ int validate(const moe_config_t* c) {
     if (c->M % 64 || c->H % (swiglu ? 128 : 64)) return MOE_ERR_UNSUPPORTED;
     if (Hs % (swiglu ? 128 : 64)) return MOE_ERR_UNSUPPORTED;
   } else {
-    if (c->M % 4) return MOE_ERR_UNSUPPORTED;  // 16-byte rows for dispatch / combine
+    if (c->M % 4 || c->H % 4) return MOE_ERR_UNSUPPORTED;  // 16-byte rows (copies, packing)
     if (swiglu && (c->H % 128 || Hs % 128)) return MOE_ERR_UNSUPPORTED;
     if (c->n_shared > 0 && c->H_shared % 4) return MOE_ERR_UNSUPPORTED;
   }
@@ -103,26 +103,26 @@ int up_proj(const moe_config_t& c, const void* A, int64_t a_rows, const int32_t*
   d.epi = swiglu ? EPI_SWIGLU : EPI_RELU;
   d.A = A; d.a_rows = a_rows; d.K = c.M;
   d.N = swiglu ? 2 * H : H;
-  d.B = W_packed; d.b_rows = int64_t(groups) * d.N;
+  d.B = W_packed; d.b_rows = int64_t(groups) * d.N; d.b_tiled = true;
   d.offsets = offsets; d.groups = groups; d.rows_dense = rows_dense;
   d.out = h; d.ldo = H;
   d.status = status;
   return launch_gemm_bf16(d, st);
 }
 
-// GEMM 2 (x row scale) over the same segments.
+// GEMM 2 (x row scale) over the same segments; W_out_packed from launch_pack_out.
 int down_proj(const moe_config_t& c, const void* h, int64_t a_rows, const int32_t* offsets,
-              int groups, int rows_dense, int H, const float* row_scale, const void* W_out, void* y,
-              unsigned* status, cudaStream_t st) {
+              int groups, int rows_dense, int H, const float* row_scale, const void* W_out_packed,
+              void* y, unsigned* status, cudaStream_t st) {
   if (c.dtype == MOE_F32)
     return launch_ffn_down_f32(c, H, static_cast<const float*>(h), offsets, groups, rows_dense,
-                               a_rows, row_scale, static_cast<const float*>(W_out),
+                               a_rows, row_scale, static_cast<const float*>(W_out_packed),
                                static_cast<float*>(y), status, st);
   GemmDesc d;
   d.epi = EPI_SCALE;
   d.A = h; d.a_rows = a_rows; d.K = H;
   d.N = c.M;
-  d.B = W_out; d.b_rows = int64_t(groups) * c.M;
+  d.B = W_out_packed; d.b_rows = int64_t(groups) * c.M; d.b_tiled = true;
   d.offsets = offsets; d.groups = groups; d.rows_dense = rows_dense;
   d.out = y; d.ldo = c.M;
   d.row_scale = row_scale;
@@ -182,30 +182,35 @@ int moe_workspace_bytes(const moe_config_t* cfg, int kind, size_t* bytes) {
   return rc;
 }
 
-int moe_packed_sizes(const moe_config_t* cfg, int64_t* w_in_packed, int64_t* ws_in_packed,
-                     int64_t* ws_out_packed) {
+int moe_packed_sizes(const moe_config_t* cfg, int64_t* w_in_packed, int64_t* w_out_packed,
+                     int64_t* ws_in_packed, int64_t* ws_out_packed) {
   Prep p;
   const int rc = prepare(cfg, &p);
   if (rc != MOE_OK) return rc;
   const int64_t f = cfg->act == MOE_ACT_SWIGLU ? 2 : 1;
   const int64_t Hs = int64_t(cfg->n_shared) * cfg->H_shared;
   if (w_in_packed) *w_in_packed = int64_t(cfg->E) * f * cfg->H * cfg->M;
+  if (w_out_packed) *w_out_packed = int64_t(cfg->E) * cfg->M * cfg->H;
   if (ws_in_packed) *ws_in_packed = f * Hs * cfg->M;
   if (ws_out_packed) *ws_out_packed = Hs * cfg->M;
   return MOE_OK;
 }
 
-int moe_pack_weights(const moe_config_t* cfg, const void* W_in, const void* W_up, void* W_in_packed,
-                     moe_stream_t stream) {
+int moe_pack_weights(const moe_config_t* cfg, const void* W_in, const void* W_up, const void* W_out,
+                     void* W_in_packed, void* W_out_packed, moe_stream_t stream) {
   Prep p;
   int rc = prepare(cfg, &p);
   if (rc != MOE_OK) return rc;
   const bool swiglu = cfg->act == MOE_ACT_SWIGLU;
-  if (!W_in || !W_in_packed || (swiglu && !W_up)) return MOE_ERR_INVALID_ARG;
-  if (W_in_packed == W_in || W_in_packed == W_up) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(W_in) || !aligned16(W_in_packed) || (swiglu && !aligned16(W_up)))
+  if (!W_in || !W_out || !W_in_packed || !W_out_packed || (swiglu && !W_up))
     return MOE_ERR_INVALID_ARG;
-  return launch_pack_in(*cfg, cfg->E, cfg->H, W_in, W_up, W_in_packed, stream);
+  if (W_in_packed == W_in || W_in_packed == W_up || W_out_packed == W_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(W_in) || !aligned16(W_out) || !aligned16(W_in_packed) || !aligned16(W_out_packed) ||
+      (swiglu && !aligned16(W_up)))
+    return MOE_ERR_INVALID_ARG;
+  rc = launch_pack_in(*cfg, cfg->E, cfg->H, W_in, W_up, W_in_packed, stream);
+  if (rc != MOE_OK) return rc;
+  return launch_pack_out(*cfg, cfg->E, cfg->H, 1, W_out, W_out_packed, stream);
 }
 
 int moe_pack_shared_weights(const moe_config_t* cfg, const void* Ws_in, const void* Ws_up,
@@ -223,7 +228,7 @@ int moe_pack_shared_weights(const moe_config_t* cfg, const void* Ws_in, const vo
     return MOE_ERR_INVALID_ARG;
   rc = launch_pack_in(*cfg, 1, cfg->n_shared * cfg->H_shared, Ws_in, Ws_up, Ws_in_packed, stream);
   if (rc != MOE_OK) return rc;
-  return launch_pack_out_cat(*cfg, Ws_out, Ws_out_packed, stream);
+  return launch_pack_out(*cfg, 1, cfg->H_shared, cfg->n_shared, Ws_out, Ws_out_packed, stream);
 }
 
 int moe_router(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
@@ -282,23 +287,24 @@ int moe_expert_up(const moe_config_t* cfg, const void* x_perm, const int32_t* ex
 }
 
 int moe_expert_down(const moe_config_t* cfg, const void* h_perm, const int32_t* expert_offsets,
-                    const float* w_perm, const void* W_out, void* y_perm, void* ws, size_t ws_bytes,
-                    moe_stream_t stream) {
+                    const float* w_perm, const void* W_out_packed, void* y_perm, void* ws,
+                    size_t ws_bytes, moe_stream_t stream) {
   Prep p;
   int rc = prepare(cfg, &p);
   if (rc != MOE_OK) return rc;
-  if (!h_perm || !expert_offsets || !w_perm || !W_out || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (!h_perm || !expert_offsets || !w_perm || !W_out_packed || !y_perm) return MOE_ERR_INVALID_ARG;
   if ((rc = check_ws(ws, ws_bytes, p.L.step_bytes)) != MOE_OK) return rc;
-  return down_proj(*cfg, h_perm, p.R_max, expert_offsets, cfg->E, 0, cfg->H, w_perm, W_out, y_perm,
-                   status_of(ws, p.L), stream);
+  return down_proj(*cfg, h_perm, p.R_max, expert_offsets, cfg->E, 0, cfg->H, w_perm, W_out_packed,
+                   y_perm, status_of(ws, p.L), stream);
 }
 
 int moe_expert_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* expert_offsets,
-                   const float* w_perm, const void* W_in_packed, const void* W_out, void* h_perm,
-                   void* y_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+                   const float* w_perm, const void* W_in_packed, const void* W_out_packed,
+                   void* h_perm, void* y_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
   int rc = moe_expert_up(cfg, x_perm, expert_offsets, W_in_packed, h_perm, ws, ws_bytes, stream);
   if (rc != MOE_OK) return rc;
-  return moe_expert_down(cfg, h_perm, expert_offsets, w_perm, W_out, y_perm, ws, ws_bytes, stream);
+  return moe_expert_down(cfg, h_perm, expert_offsets, w_perm, W_out_packed, y_perm, ws, ws_bytes,
+                         stream);
 }
 
 int moe_shared_ffn(const moe_config_t* cfg, const void* x, const void* Ws_in_packed,
@@ -331,14 +337,14 @@ int moe_combine(const moe_config_t* cfg, const void* y_perm, const moe_route_out
 }
 
 int moe_layer_forward(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
-                      const void* W_in_packed, const void* W_out, const void* Ws_in_packed,
+                      const void* W_in_packed, const void* W_out_packed, const void* Ws_in_packed,
                       const void* Ws_out_packed, const float* u, const void* residual, void* y,
                       float* logits_out, const moe_route_out_t* r, void* ws, size_t ws_bytes,
                       moe_stream_t stream) {
   Prep p;
   int rc = prepare(cfg, &p);
   if (rc != MOE_OK) return rc;
-  if (!x || !W_g || !W_in_packed || !W_out || !y) return MOE_ERR_INVALID_ARG;
+  if (!x || !W_g || !W_in_packed || !W_out_packed || !y) return MOE_ERR_INVALID_ARG;
   if (cfg->n_shared > 0 && (!Ws_in_packed || !Ws_out_packed)) return MOE_ERR_INVALID_ARG;
   if ((rc = check_route_out(*cfg, r)) != MOE_OK) return rc;
   if ((rc = check_ws(ws, ws_bytes, p.L.layer_bytes)) != MOE_OK) return rc;
@@ -351,8 +357,8 @@ int moe_layer_forward(const moe_config_t* cfg, const void* x, const void* W_g, c
   if ((rc = moe_router(cfg, x, W_g, bias, logits, ws, ws_bytes, stream)) != MOE_OK) return rc;
   if ((rc = moe_route(cfg, logits, u, r, ws, ws_bytes, stream)) != MOE_OK) return rc;
   if ((rc = moe_dispatch(cfg, x, r, x_perm, stream)) != MOE_OK) return rc;
-  if ((rc = moe_expert_ffn(cfg, x_perm, r->expert_offsets, r->w_perm, W_in_packed, W_out, h_perm,
-                           y_perm, ws, ws_bytes, stream)) != MOE_OK)
+  if ((rc = moe_expert_ffn(cfg, x_perm, r->expert_offsets, r->w_perm, W_in_packed, W_out_packed,
+                           h_perm, y_perm, ws, ws_bytes, stream)) != MOE_OK)
     return rc;
   if (cfg->n_shared > 0 &&
       (rc = moe_shared_ffn(cfg, x, Ws_in_packed, Ws_out_packed, w + p.L.h_shared, shared_out, ws,

@@ -2,8 +2,9 @@
 //
 //   D[r, n] = sum_k A[r, k] * B[g * N + n, k]   for the rows r of group g,
 //
-// A [rows, K] and B [groups * N, K] both row-major (K-major, the [out, in] layout of a
-// linear layer), fp32 accumulation in tensor memory, a fused epilogue:
+// A [rows, K] row-major and B [groups * N, K] (row-major, or packed tile-major by
+// launch_pack_in / launch_pack_out), both K-major like the [out, in] weights of a linear
+// layer, fp32 accumulation in tensor memory, a fused epilogue:
 //   EPI_F32_BIAS  fp32 out (+ per-column bias)          -- router logits
 //   EPI_RELU      bf16 out = relu(D)                    -- expert GEMM 1, ReLU expert
 //   EPI_SWIGLU    bf16 out = silu(D_gate) * D_up        -- expert GEMM 1, SwiGLU expert
@@ -15,15 +16,23 @@
 // in expert-contiguous segments of uneven length (here read from device offsets, so the
 // host never synchronises to size the grid).
 //
-// Structure (one CTA per SM, persistent over output tiles of 128 x BN):
-//   warp 0      one thread issues TMA loads of A (128 x 64) and B (BN x 64) tiles into a
+// Structure (persistent: one CTA per SM, looping over output tiles):
+//   warp 0      one lane issues TMA loads of its A rows (128 x 64) and B rows (x 64) into a
 //               ring of shared-memory stages (128-byte swizzle), signalling `full` barriers;
-//   warp 1      allocates tensor memory; one thread issues tcgen05.mma (M=128, N=BN,
-//               K=16 per instruction) into one of two TMEM accumulators and commits to the
-//               stage's `empty` barrier and, per tile, to the accumulator's `tfull` barrier;
+//   warp 1      owns tensor memory; one lane issues tcgen05.mma (K = 16 per instruction)
+//               into one of two TMEM accumulators, committing each stage to its `empty`
+//               barrier and each tile to the accumulator's `tfull` barrier;
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..),
 //               apply the fused epilogue, store, then arrive on the accumulator's `tempty`
-//               barrier so the MMA warp can reuse it while the next tile's loads stream in.
+//               barrier, so the next tile's MMAs overlap this tile's epilogue.
+// PAIR = false: one CTA computes a 128 x BN tile (cta_group::1).
+// PAIR = true:  a cluster of two CTAs computes a 256 x BN tile with cta_group::2 MMAs: each
+//               CTA stages its 128 rows of A and BN/2 rows of B (half the weight bytes per
+//               SM per output of the single-CTA tile); the even CTA issues the MMAs, which
+//               read both CTAs' shared memory and write each CTA's 128 accumulator rows into
+//               its own TMEM; both CTAs' loads complete on the even CTA's `full` barrier, its
+//               commits arrive on both CTAs' `empty` / `tfull` barriers, and both epilogues
+//               arrive on its `tempty` barrier.
 // Tiles are ordered group by group, then by N tile, then by M tile, so the CTAs that run
 // at the same time share each weight tile through L2.
 //
@@ -47,12 +56,15 @@ constexpr int kThreads = 192;
 constexpr int kMaxGroups = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-template <int BN>
+template <int BN, bool PAIR>
 struct Cfg {
-  static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr int CTAS = PAIR ? 2 : 1;
+  static constexpr int TILE_M = BM * CTAS;  // rows of one output tile
+  static constexpr int B_ROWS = BN / CTAS;  // B rows each CTA stages
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);
   static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + 16 + 2 * (kMaxGroups + 1) * 4;
@@ -60,6 +72,7 @@ struct Cfg {
 
 struct KParams {
   const int32_t* offsets;
+  int b_tiled;  // B packed tile-major: box (g, nt, kb) is block (g * n_tiles + nt) * kblocks + kb
   int groups;
   int rows_dense;
   int64_t rows_cap;
@@ -137,6 +150,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -169,9 +190,9 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D, M = 128, N = n.
-__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+// Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D, M = m, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
@@ -203,6 +224,72 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+
+// ---- cluster / cta_group::2 forms
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+// TMA into this CTA's shared memory, completing on a barrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cluster_bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 int z, uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(cluster_bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on the barrier at this shared-memory offset in every CTA of `mask` once all
+// tcgen05 operations issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar), "h"(mask)
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -214,12 +301,94 @@ __device__ __forceinline__ void store_bf16x16(void* dst, const uint32_t (&p)[8])
   d[1] = make_uint4(p[4], p[5], p[6], p[7]);
 }
 
-// ------------------------------------------------------------------ the kernel
+// ------------------------------------------------------------------ the epilogue
+// One warp drains 32 accumulator rows (TMEM lanes) x BN columns at `tbase`; the thread
+// holding tile row `grow` stores it if `valid`. nt: the tile's N index.
 template <int BN, int EPI>
+__device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, bool valid,
+                                              int64_t grow, int nt) {
+  if constexpr (EPI == EPI_F32_BIAS) {
+    float* out = static_cast<float*>(p.out) + grow * p.ldo;
+    const bool vec = (p.ldo & 3) == 0;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      uint32_t v[16];
+      tmem_ld16(tbase + c0, v);
+      tmem_ld_wait();
+      if (valid) {
+        const int nb = nt * BN + c0;
+        float f[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          f[j] = __uint_as_float(v[j]) + ((p.bias && nb + j < p.n_valid) ? p.bias[nb + j] : 0.f);
+        if (vec && nb + 16 <= p.n_valid) {
+          float4* d = reinterpret_cast<float4*>(out + nb);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) d[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (nb + j < p.n_valid) out[nb + j] = f[j];
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_SWIGLU) {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + nt * (BN / 2);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN / 2; c0 += 16) {
+      uint32_t gv[16], uv[16];
+      tmem_ld16(tbase + c0, gv);
+      tmem_ld16(tbase + BN / 2 + c0, uv);
+      tmem_ld_wait();
+      if (valid) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float g0 = __uint_as_float(gv[2 * j]), g1 = __uint_as_float(gv[2 * j + 1]);
+          const float h0 = g0 / (1.f + __expf(-g0)) * __uint_as_float(uv[2 * j]);
+          const float h1 = g1 / (1.f + __expf(-g1)) * __uint_as_float(uv[2 * j + 1]);
+          pk[j] = pack_bf16x2(h0, h1);
+        }
+        store_bf16x16(out + c0, pk);
+      }
+    }
+  } else {
+    float scale = 1.f;
+    if (EPI == EPI_SCALE && valid && p.row_scale) scale = p.row_scale[grow];
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + nt * BN;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      uint32_t v0[16], v1[16];
+      tmem_ld16(tbase + c0, v0);
+      tmem_ld16(tbase + c0 + 16, v1);
+      tmem_ld_wait();
+      if (valid) {
+        uint32_t pk0[8], pk1[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float a0 = __uint_as_float(v0[2 * j]), a1 = __uint_as_float(v0[2 * j + 1]);
+          float b0 = __uint_as_float(v1[2 * j]), b1 = __uint_as_float(v1[2 * j + 1]);
+          if (EPI == EPI_RELU) {
+            a0 = fmaxf(a0, 0.f); a1 = fmaxf(a1, 0.f); b0 = fmaxf(b0, 0.f); b1 = fmaxf(b1, 0.f);
+          } else {
+            a0 *= scale; a1 *= scale; b0 *= scale; b1 *= scale;
+          }
+          pk0[j] = pack_bf16x2(a0, a1);
+          pk1[j] = pack_bf16x2(b0, b1);
+        }
+        store_bf16x16(out + c0, pk0);
+        store_bf16x16(out + c0 + 16, pk1);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int BN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const KParams p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -239,6 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain_bar = tempty0 + 16;
   const int G = p.offsets ? p.groups : 1;
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);  // this CTA's tile stream
+  const int units = PAIR ? int(gridDim.x >> 1) : int(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -247,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 4);
+      mbar_init(tempty0 + 8 * a, 4 * C::CTAS);
     }
     mbar_init(drain_bar, 1);
     *s_abort = 0;
@@ -255,7 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
   }
-  if (warp == 1) tmem_alloc(smem_u32(s_tmem), C::TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR) tmem_alloc_pair(smem_u32(s_tmem), C::TMEM_COLS);
+    else tmem_alloc(smem_u32(s_tmem), C::TMEM_COLS);
+  }
   if (warp == 2) {
     // m-tile prefix over the groups, from the device row offsets
     bool bad = false;
@@ -267,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lo = p.offsets ? p.offsets[g] : 0;
         const int hi = p.offsets ? p.offsets[g + 1] : p.rows_dense;
         if (lo < 0 || hi < lo || int64_t(hi) > p.rows_cap) bad = true;
-        else cnt = (hi - lo + BM - 1) / BM;
+        else cnt = (hi - lo + C::TILE_M - 1) / C::TILE_M;
         s_off[g] = lo;
         if (g == G - 1) s_off[G] = hi;
       }
@@ -283,11 +459,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       s_tstart[0] = 0;
       *s_total = bad ? 0 : run * p.n_tiles;
-      if (bad) atomicOr(p.status, kStatusDeviceData);
+      if (bad && leader) atomicOr(p.status, kStatusDeviceData);
     }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // barriers initialised in both CTAs
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   const int total = *s_total;
@@ -306,8 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int mt = s_tstart[g + 1] - s_tstart[g];
     nt = local / mt;
     const int m_t = local % mt;
-    m0 = s_off[g] + m_t * BM;
-    rows = min(BM, s_off[g + 1] - m0);
+    m0 = s_off[g] + m_t * C::TILE_M;
+    rows = min(C::TILE_M, s_off[g + 1] - m0);
   };
 
   if (warp == 0) {
@@ -315,18 +492,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0, issued = 0, issued_par = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int t = unit; t < total && ok; t += units) {
       int g, m0, rows, nt;
       decode(t, g, m0, rows, nt);
-      const int brow = g * p.N + nt * BN;
+      const int arow = m0 + int(rank) * BM;
+      const int brow = g * p.N + nt * BN + int(rank) * C::B_ROWS;
+      const int bblk = (g * p.n_tiles + nt) * kblocks;
       for (int kb = 0; kb < kblocks; ++kb) {
         ok = __all_sync(0xffffffffu, wait_bounded(empty0 + 8 * stage, phase ^ 1u, s_abort, p.status));
         if (!ok) break;
         if (lane == 0) {
           const uint32_t fb = full0 + 8 * stage;
-          mbar_expect_tx(fb, C::STAGE_BYTES);
-          tma_load_2d(smem_u32(sA + stage * C::A_BYTES), &tmA, kb * BK, m0, fb);
-          tma_load_2d(smem_u32(sB + stage * C::B_BYTES), &tmB, kb * BK, brow, fb);
+          const uint32_t dA = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t dB = smem_u32(sB + stage * C::B_BYTES);
+          if (leader) mbar_expect_tx(fb, C::CTAS * C::STAGE_BYTES);
+          if constexpr (PAIR) {
+            const uint32_t lfb = cluster_addr(fb, 0);  // the even CTA's full barrier
+            tma_load_2d_pair(dA, &tmA, kb * BK, arow, lfb);
+            if (p.b_tiled) tma_load_3d_pair(dB, &tmB, 0, int(rank) * C::B_ROWS, bblk + kb, lfb);
+            else tma_load_2d_pair(dB, &tmB, kb * BK, brow, lfb);
+          } else {
+            tma_load_2d(dA, &tmA, kb * BK, arow, fb);
+            if (p.b_tiled) tma_load_3d(dB, &tmB, 0, 0, bblk + kb, fb);
+            else tma_load_2d(dB, &tmB, kb * BK, brow, fb);
+          }
         }
         __syncwarp();
         issued |= 1u << stage;
@@ -337,58 +526,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (!ok && lane == 0) {  // let every load in flight land before the CTA exits
+    // on abort, let every load in flight land before the CTA exits (the even CTA's full
+    // barriers also count the odd CTA's bytes)
+    if (!ok && leader && lane == 0) {
       for (int s = 0; s < C::STAGES; ++s)
         if ((issued >> s) & 1u) wait_drain(full0 + 8 * s, (issued_par >> s) & 1u);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------- MMA issuer: the whole warp waits, lane 0 issues
-    constexpr uint32_t kIdesc = idesc_bf16(BN);
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true, any = false;
-    int i = 0;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
-      const int acc = i & 1;
-      const uint32_t use = uint32_t(i >> 1) & 1u;
-      ok = __all_sync(0xffffffffu, wait_bounded(tempty0 + 8 * acc, use ^ 1u, s_abort, p.status));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t d = tmem_base + uint32_t(acc * BN);
-      for (int kb = 0; kb < kblocks; ++kb) {
-        ok = __all_sync(0xffffffffu, wait_bounded(full0 + 8 * stage, phase, s_abort, p.status));
+    // ---------------- MMA issuer (the even CTA of a pair): the warp waits, lane 0 issues
+    if (leader) {
+      constexpr uint32_t kIdesc = idesc_bf16(C::TILE_M, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true, any = false;
+      int i = 0;
+      for (int t = unit; t < total && ok; t += units, ++i) {
+        const int acc = i & 1;
+        const uint32_t use = uint32_t(i >> 1) & 1u;
+        ok = __all_sync(0xffffffffu, wait_bounded(tempty0 + 8 * acc, use ^ 1u, s_abort, p.status));
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
-          const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+        const uint32_t d = tmem_base + uint32_t(acc * BN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          ok = __all_sync(0xffffffffu, wait_bounded(full0 + 8 * stage, phase, s_abort, p.status));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
+            const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_bf16(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), kIdesc,
-                     (kb | kk) != 0 ? 1u : 0u);
-          mma_commit(empty0 + 8 * stage);
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              if constexpr (PAIR)
+                mma_bf16_pair(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), kIdesc,
+                              (kb | kk) != 0 ? 1u : 0u);
+              else
+                mma_bf16(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), kIdesc,
+                         (kb | kk) != 0 ? 1u : 0u);
+            }
+            if constexpr (PAIR) mma_commit_pair(empty0 + 8 * stage, uint16_t(3));
+            else mma_commit(empty0 + 8 * stage);
+          }
+          __syncwarp();
+          any = true;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok && lane == 0) {
+          if constexpr (PAIR) mma_commit_pair(tfull0 + 8 * acc, uint16_t(3));
+          else mma_commit(tfull0 + 8 * acc);
         }
         __syncwarp();
-        any = true;
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
       }
-      if (ok && lane == 0) mma_commit(tfull0 + 8 * acc);
+      if (!ok && any && lane == 0) {  // every MMA issued must finish before TMEM is freed
+        if constexpr (PAIR) mma_commit_pair(drain_bar, uint16_t(1));
+        else mma_commit(drain_bar);
+        wait_drain(drain_bar, 0u);
+      }
       __syncwarp();
     }
-    if (!ok && any && lane == 0) {  // every MMA issued must finish before TMEM is freed
-      mma_commit(drain_bar);
-      wait_drain(drain_bar, 0u);
-    }
-    __syncwarp();
   } else {
     // ---------------- epilogue warps 2..5
-    const int q = warp & 3;  // TMEM lanes 32q..32q+31 = tile rows
+    const int q = warp & 3;  // TMEM lanes 32q..32q+31 = this CTA's tile rows
+    const uint32_t tempty_leader = PAIR ? cluster_addr(tempty0, 0) : tempty0;
     int i = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
+    for (int t = unit; t < total; t += units, ++i) {
       const int acc = i & 1;
       const uint32_t use = uint32_t(i >> 1) & 1u;
       const bool ok = __all_sync(0xffffffffu, wait_bounded(tfull0 + 8 * acc, use, s_abort, p.status));
@@ -396,95 +600,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       int g, m0, rows, nt;
       decode(t, g, m0, rows, nt);
-      const int r = q * 32 + lane;
-      const bool valid = r < rows;
-      const int64_t grow = int64_t(m0) + r;
+      const int r = int(rank) * BM + q * 32 + lane;  // row within the tile
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
-      if constexpr (EPI == EPI_F32_BIAS) {
-        float* out = static_cast<float*>(p.out) + grow * p.ldo;
-        const bool vec = (p.ldo & 3) == 0;
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(tbase + c0, v);
-          tmem_ld_wait();
-          if (valid) {
-            const int nb = nt * BN + c0;
-            float f[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              f[j] = __uint_as_float(v[j]) + ((p.bias && nb + j < p.n_valid) ? p.bias[nb + j] : 0.f);
-            if (vec && nb + 16 <= p.n_valid) {
-              float4* d = reinterpret_cast<float4*>(out + nb);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) d[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (nb + j < p.n_valid) out[nb + j] = f[j];
-            }
-          }
-        }
-      } else if constexpr (EPI == EPI_SWIGLU) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + nt * (BN / 2);
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN / 2; c0 += 16) {
-          uint32_t gv[16], uv[16];
-          tmem_ld16(tbase + c0, gv);
-          tmem_ld16(tbase + BN / 2 + c0, uv);
-          tmem_ld_wait();
-          if (valid) {
-            uint32_t pk[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float g0 = __uint_as_float(gv[2 * j]), g1 = __uint_as_float(gv[2 * j + 1]);
-              const float h0 = g0 / (1.f + __expf(-g0)) * __uint_as_float(uv[2 * j]);
-              const float h1 = g1 / (1.f + __expf(-g1)) * __uint_as_float(uv[2 * j + 1]);
-              pk[j] = pack_bf16x2(h0, h1);
-            }
-            store_bf16x16(out + c0, pk);
-          }
-        }
-      } else {
-        float scale = 1.f;
-        if (EPI == EPI_SCALE && valid && p.row_scale) scale = p.row_scale[grow];
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + nt * BN;
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          uint32_t v0[16], v1[16];
-          tmem_ld16(tbase + c0, v0);
-          tmem_ld16(tbase + c0 + 16, v1);
-          tmem_ld_wait();
-          if (valid) {
-            uint32_t pk0[8], pk1[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              float a0 = __uint_as_float(v0[2 * j]), a1 = __uint_as_float(v0[2 * j + 1]);
-              float b0 = __uint_as_float(v1[2 * j]), b1 = __uint_as_float(v1[2 * j + 1]);
-              if (EPI == EPI_RELU) {
-                a0 = fmaxf(a0, 0.f); a1 = fmaxf(a1, 0.f); b0 = fmaxf(b0, 0.f); b1 = fmaxf(b1, 0.f);
-              } else {
-                a0 *= scale; a1 *= scale; b0 *= scale; b1 *= scale;
-              }
-              pk0[j] = pack_bf16x2(a0, a1);
-              pk1[j] = pack_bf16x2(b0, b1);
-            }
-            store_bf16x16(out + c0, pk0);
-            store_bf16x16(out + c0 + 16, pk1);
-          }
-        }
-      }
+      epilogue_rows<BN, EPI>(p, tbase, r < rows, int64_t(m0) + r, nt);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      if (lane == 0) {
+        if constexpr (PAIR) mbar_arrive_cluster(tempty_leader + 8 * acc);
+        else mbar_arrive(tempty0 + 8 * acc);
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // both CTAs done with TMEM and each other's smem
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
@@ -518,15 +652,38 @@ int make_map(CUtensorMap* m, const void* base, int64_t rows, int K, int box_rows
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
-template <int BN, int EPI>
+// 3-D bf16 tensor map over a tile-major packed matrix: `blocks` contiguous [block_rows][64]
+// blocks; a box is box_rows rows (all of a block, or half of it for a CTA pair).
+int make_map_tiled(CUtensorMap* m, const void* base, int64_t blocks, int block_rows, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0) return MOE_ERR_INVALID_ARG;
+  cuuint64_t dims[3] = {cuuint64_t(BK), cuuint64_t(block_rows), cuuint64_t(blocks)};
+  cuuint64_t strides[2] = {cuuint64_t(BK) * 2, cuuint64_t(BK) * 2 * block_rows};
+  cuuint32_t box[3] = {cuuint32_t(BK), cuuint32_t(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+template <int BN, int EPI, bool PAIR>
 int run_gemm(const GemmDesc& d, cudaStream_t st) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, PAIR>;
   CUtensorMap ta, tb;
   int rc = make_map(&ta, d.A, d.a_rows, d.K, BM);
   if (rc != MOE_OK) return rc;
-  rc = make_map(&tb, d.B, d.b_rows, d.K, BN);
+  if (d.b_tiled) {
+    if (d.N % BN != 0 || d.b_rows % d.N != 0) return MOE_ERR_UNSUPPORTED;
+    rc = make_map_tiled(&tb, d.B, d.b_rows / BN * (d.K / BK), BN, C::B_ROWS);
+  } else {
+    if (PAIR) return MOE_ERR_UNSUPPORTED;
+    rc = make_map(&tb, d.B, d.b_rows, d.K, BN);
+  }
   if (rc != MOE_OK) return rc;
   KParams p;
+  p.b_tiled = d.b_tiled ? 1 : 0;
   p.offsets = d.offsets;
   p.groups = d.groups;
   p.rows_dense = d.rows_dense;
@@ -540,15 +697,34 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
   p.bias = d.bias;
   p.n_valid = d.n_valid;
   p.status = d.status;
-  auto kern = grouped_gemm_kernel<BN, EPI>;
+  auto kern = grouped_gemm_kernel<BN, EPI, PAIR>;
   MOE_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
-  const int64_t m_tiles =
-      d.offsets ? (d.a_rows + BM - 1) / BM + d.groups : (int64_t(d.rows_dense) + BM - 1) / BM;
-  int64_t grid = m_tiles * p.n_tiles;
-  if (grid > num_sms()) grid = num_sms();
-  if (grid < 1) grid = 1;
-  kern<<<unsigned(grid), kThreads, C::SMEM, st>>>(ta, tb, p);
-  MOE_CUDA_CHECK(cudaGetLastError());
+  const int64_t m_tiles = d.offsets ? (d.a_rows + C::TILE_M - 1) / C::TILE_M + d.groups
+                                    : (int64_t(d.rows_dense) + C::TILE_M - 1) / C::TILE_M;
+  const int64_t tiles = m_tiles * p.n_tiles;
+  cudaLaunchConfig_t lc = {};
+  lc.blockDim = dim3(kThreads);
+  lc.dynamicSmemBytes = C::SMEM;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  int64_t units = num_sms();
+  if constexpr (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    lc.gridDim = dim3(2);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &lc) != cudaSuccess || clusters < 1)
+      clusters = num_sms() / 2;
+    units = clusters;
+  }
+  if (units > tiles) units = tiles;
+  if (units < 1) units = 1;
+  lc.gridDim = dim3(unsigned(units * C::CTAS));
+  MOE_CUDA_CHECK(cudaLaunchKernelEx(&lc, kern, ta, tb, p));
   return MOE_OK;
 }
 
@@ -558,26 +734,34 @@ int launch_gemm_bf16(const GemmDesc& d, cudaStream_t st) {
   if (d.K < BK || d.K % BK != 0 || d.N < 1) return MOE_ERR_UNSUPPORTED;
   if (d.offsets && (d.groups < 1 || d.groups > kMaxGroups)) return MOE_ERR_UNSUPPORTED;
   if (d.a_rows < 1 || d.a_rows > INT32_MAX || d.b_rows < 1) return MOE_ERR_INVALID_ARG;
+  const int bn = gemm_bn(d.N, d.epi);
+  // 256-wide tiles of packed weights run on CTA pairs (cta_group::2, 256 x 256 tiles)
+  const bool pair = d.b_tiled && bn == 256;
   switch (d.epi) {
     case EPI_F32_BIAS:
-      if (d.N <= 16) return run_gemm<16, EPI_F32_BIAS>(d, st);
-      if (d.N <= 32) return run_gemm<32, EPI_F32_BIAS>(d, st);
-      if (d.N <= 64) return run_gemm<64, EPI_F32_BIAS>(d, st);
-      if (d.N <= 128) return run_gemm<128, EPI_F32_BIAS>(d, st);
-      if (d.N <= 256) return run_gemm<256, EPI_F32_BIAS>(d, st);
+      switch (bn) {
+        case 16: return run_gemm<16, EPI_F32_BIAS, false>(d, st);
+        case 32: return run_gemm<32, EPI_F32_BIAS, false>(d, st);
+        case 64: return run_gemm<64, EPI_F32_BIAS, false>(d, st);
+        case 128: return run_gemm<128, EPI_F32_BIAS, false>(d, st);
+        case 256: return run_gemm<256, EPI_F32_BIAS, false>(d, st);
+      }
       return MOE_ERR_UNSUPPORTED;
     case EPI_SWIGLU:
-      if (d.N % 256 != 0) return MOE_ERR_UNSUPPORTED;
-      return run_gemm<256, EPI_SWIGLU>(d, st);
+      if (bn == 256) return pair ? run_gemm<256, EPI_SWIGLU, true>(d, st)
+                                 : run_gemm<256, EPI_SWIGLU, false>(d, st);
+      return MOE_ERR_UNSUPPORTED;
     case EPI_RELU:
-      if (d.N % 256 == 0) return run_gemm<256, EPI_RELU>(d, st);
-      if (d.N % 128 == 0) return run_gemm<128, EPI_RELU>(d, st);
-      if (d.N % 64 == 0) return run_gemm<64, EPI_RELU>(d, st);
+      if (bn == 256) return pair ? run_gemm<256, EPI_RELU, true>(d, st)
+                                 : run_gemm<256, EPI_RELU, false>(d, st);
+      if (bn == 128) return run_gemm<128, EPI_RELU, false>(d, st);
+      if (bn == 64) return run_gemm<64, EPI_RELU, false>(d, st);
       return MOE_ERR_UNSUPPORTED;
     case EPI_SCALE:
-      if (d.N % 256 == 0) return run_gemm<256, EPI_SCALE>(d, st);
-      if (d.N % 128 == 0) return run_gemm<128, EPI_SCALE>(d, st);
-      if (d.N % 64 == 0) return run_gemm<64, EPI_SCALE>(d, st);
+      if (bn == 256) return pair ? run_gemm<256, EPI_SCALE, true>(d, st)
+                                 : run_gemm<256, EPI_SCALE, false>(d, st);
+      if (bn == 128) return run_gemm<128, EPI_SCALE, false>(d, st);
+      if (bn == 64) return run_gemm<64, EPI_SCALE, false>(d, st);
       return MOE_ERR_UNSUPPORTED;
   }
   return MOE_ERR_INVALID_ARG;

@@ -69,6 +69,25 @@ inline WsLayout ws_layout(const moe_config_t& c, int C) {
   return L;
 }
 
+// ------------------------------------------------------------------ GEMM tiling
+// Epilogues of the bf16 tcgen05 GEMM (gemm_tcgen05.cu).
+enum GemmEpilogue { EPI_F32_BIAS = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_SCALE = 3 };
+
+// N-tile width of the bf16 GEMM for N output columns per group (0 = unsupported). The
+// packed weight layout depends on it, so packing and launching both take it from here.
+inline int gemm_bn(int N, int epi) {
+  if (epi == EPI_F32_BIAS) {
+    for (int bn = 16; bn <= 256; bn *= 2)
+      if (N <= bn) return bn;
+    return 0;
+  }
+  if (epi == EPI_SWIGLU) return N % 256 == 0 ? 256 : 0;
+  if (N % 256 == 0) return 256;
+  if (N % 128 == 0) return 128;
+  if (N % 64 == 0) return 64;
+  return 0;
+}
+
 // ------------------------------------------------------------------ launchers
 // route.cu
 int launch_route(const moe_config_t& c, int C, const float* logits, const float* u,
@@ -80,16 +99,22 @@ int launch_dispatch(const moe_config_t& c, int64_t R_max, const void* x, const i
 int launch_combine(const moe_config_t& c, const void* y_perm, const int32_t* row,
                    const void* shared_out, const void* residual, void* y, int64_t R_max,
                    cudaStream_t st);
+// Weight packing. bf16: tile-major [groups][N/BN][K/64][BN][64] (one contiguous 32 KB block
+// per TMA box of the GEMM, BN = gemm_bn); fp32: row-major [groups][N][K].
+//   first layer: N = H (ReLU) or 2H (SwiGLU: blocks of 256 rows = 128 W_in rows, then the
+//                same 128 W_up rows), K = M;
+//   second layer: N = M, K = H (W_out [groups][M][H], or n_shared experts side by side).
 int launch_pack_in(const moe_config_t& c, int groups, int H, const void* W_in, const void* W_up,
                    void* packed, cudaStream_t st);
-int launch_pack_out_cat(const moe_config_t& c, const void* Ws_out, void* packed, cudaStream_t st);
+int launch_pack_out(const moe_config_t& c, int groups, int H, int n_parts, const void* W_out,
+                    void* packed, cudaStream_t st);
 
 // gemm_tcgen05.cu : bf16 GEMM D = A . B^T over ragged row groups, tcgen05 + TMA.
-enum GemmEpilogue { EPI_F32_BIAS = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_SCALE = 3 };
 struct GemmDesc {
   int epi = EPI_RELU;
   const void* A = nullptr; int64_t a_rows = 0; int K = 0;  // A [a_rows, K] bf16, row-major
-  const void* B = nullptr; int64_t b_rows = 0;             // B [b_rows, K] bf16, row-major
+  const void* B = nullptr; int64_t b_rows = 0;             // B [b_rows, K] bf16
+  bool b_tiled = false;            // B packed tile-major (see launch_pack_in), else row-major
   int N = 0;                       // B rows per group = GEMM N of each group
   const int32_t* offsets = nullptr;  // device [groups+1] row offsets into A; null = dense
   int groups = 1;

@@ -161,42 +161,59 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
   }
 }
 
-// Packed first-layer weights. ReLU: a copy. SwiGLU: blocks of 256 rows, 128 rows of W_in
-// then the same 128 rows of W_up.
-__global__ void __launch_bounds__(kThreads) pack_in_kernel(const uint4* __restrict__ W_in,
-                                                           const uint4* __restrict__ W_up,
-                                                           int64_t dst_rows, int H, int swiglu,
-                                                           int units, uint4* __restrict__ dst) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp0 = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
-  const int NR = swiglu ? 2 * H : H;
-  for (int64_t p = warp0; p < dst_rows; p += nwarps) {
-    const int64_t e = p / NR;
-    const int pl = int(p % NR);
-    const uint4* src;
-    if (swiglu) {
-      const int b = pl / 256, i = pl % 256;
-      src = (i < 128) ? W_in + (e * H + b * 128 + i) * units
-                      : W_up + (e * H + b * 128 + (i - 128)) * units;
+// Weight packing, one pass over the destination in 16-byte units (coalesced stores).
+// mode 0, first layer: logical row n of group g is W_in[g][n] (ReLU) or, for SwiGLU, in
+//   blocks of 256 rows, W_in[g][128b + i] for i < 128 and W_up[g][128b + i - 128] after;
+//   K = M.
+// mode 1, second layer: logical row m, column k = s*H + h of group g is W[g*parts + s][m][h]
+//   (parts = 1 for routed experts; the n_shared shared experts side by side).
+// TILED (bf16): destination [g][N/BN][K/64][BN][64], one contiguous block per GEMM box;
+// otherwise row-major [g][N][K].
+template <bool TILED>
+__global__ void __launch_bounds__(kThreads) pack_kernel(const uint4* __restrict__ W,
+                                                        const uint4* __restrict__ W2, int mode,
+                                                        int swiglu, int groups, int N, int K,
+                                                        int H, int parts, int BN, int epu,
+                                                        uint4* __restrict__ dst) {
+  const int kunits = K / epu;
+  const int64_t total = int64_t(groups) * N * kunits;
+  for (int64_t u = int64_t(blockIdx.x) * kThreads + threadIdx.x; u < total;
+       u += int64_t(gridDim.x) * kThreads) {
+    int64_t g;
+    int n, kq;
+    if (TILED) {  // 8 units of 8 bf16 per 64-wide box row
+      const int cu = int(u % 8);
+      int64_t rest = u / 8;
+      const int r = int(rest % BN);
+      rest /= BN;
+      const int KB = K / 64;
+      const int kb = int(rest % KB);
+      rest /= KB;
+      const int NT = N / BN;
+      const int nt = int(rest % NT);
+      g = rest / NT;
+      n = nt * BN + r;
+      kq = kb * 8 + cu;
     } else {
-      src = W_in + (e * H + pl) * units;
+      kq = int(u % kunits);
+      const int64_t rest = u / kunits;
+      n = int(rest % N);
+      g = rest / N;
     }
-    for (int q = lane; q < units; q += 32) dst[p * units + q] = src[q];
-  }
-}
-
-// Ws_out [n_shared, M, Hs] -> [M, n_shared*Hs] (the shared experts' hidden units side by side).
-__global__ void __launch_bounds__(kThreads) pack_out_cat_kernel(const uint4* __restrict__ src,
-                                                                int n_shared, int M, int hs_units,
-                                                                uint4* __restrict__ dst) {
-  const int64_t total = int64_t(n_shared) * M * hs_units;
-  for (int64_t idx = int64_t(blockIdx.x) * kThreads + threadIdx.x; idx < total;
-       idx += int64_t(gridDim.x) * kThreads) {
-    const int q = int(idx % hs_units);
-    const int64_t sm = idx / hs_units;  // s * M + m
-    const int s = int(sm / M), m = int(sm % M);
-    dst[(int64_t(m) * n_shared + s) * hs_units + q] = src[idx];
+    if (mode == 0) {
+      const uint4* base = W;
+      int srow = n;
+      if (swiglu) {
+        const int b = n / 256, i = n % 256;
+        srow = b * 128 + (i & 127);
+        if (i >= 128) base = W2;
+      }
+      dst[u] = base[(g * H + srow) * kunits + kq];
+    } else {
+      const int k = kq * epu;
+      const int part = k / H, h = k % H;
+      dst[u] = W[((g * parts + part) * N + n) * (H / epu) + h / epu];
+    }
   }
 }
 
@@ -244,25 +261,42 @@ int launch_combine(const moe_config_t& c, const void* y_perm, const int32_t* row
   return MOE_OK;
 }
 
-int launch_pack_in(const moe_config_t& c, int groups, int H, const void* W_in, const void* W_up,
-                   void* packed, cudaStream_t st) {
-  const int swiglu = c.act == MOE_ACT_SWIGLU;
-  const int units = int(c.M * elem_bytes(c) / 16);
-  const int64_t rows = int64_t(groups) * (swiglu ? 2 * H : H);
-  pack_in_kernel<<<grid_for(rows), kThreads, 0, st>>>(static_cast<const uint4*>(W_in),
-                                                     static_cast<const uint4*>(W_up), rows, H,
-                                                     swiglu, units, static_cast<uint4*>(packed));
+namespace {
+int run_pack(const moe_config_t& c, const void* W, const void* W2, int mode, int swiglu, int groups,
+             int N, int K, int H, int parts, int BN, void* dst, cudaStream_t st) {
+  const int epu = int(16 / elem_bytes(c));
+  if (K % epu || (mode == 1 && H % epu)) return MOE_ERR_UNSUPPORTED;
+  const int64_t total = int64_t(groups) * N * (K / epu);
+  const unsigned grid = grid_for((total + 31) / 32);
+  if (c.dtype == MOE_BF16) {
+    if (BN <= 0 || N % BN || K % 64) return MOE_ERR_UNSUPPORTED;
+    pack_kernel<true><<<grid, kThreads, 0, st>>>(static_cast<const uint4*>(W),
+                                                 static_cast<const uint4*>(W2), mode, swiglu,
+                                                 groups, N, K, H, parts, BN, epu,
+                                                 static_cast<uint4*>(dst));
+  } else {
+    pack_kernel<false><<<grid, kThreads, 0, st>>>(static_cast<const uint4*>(W),
+                                                  static_cast<const uint4*>(W2), mode, swiglu,
+                                                  groups, N, K, H, parts, 0, epu,
+                                                  static_cast<uint4*>(dst));
+  }
   MOE_CUDA_CHECK(cudaGetLastError());
   return MOE_OK;
 }
+}  // namespace
 
-int launch_pack_out_cat(const moe_config_t& c, const void* Ws_out, void* packed, cudaStream_t st) {
-  const int hs_units = int(c.H_shared * elem_bytes(c) / 16);
-  const int64_t total = int64_t(c.n_shared) * c.M * hs_units;
-  pack_out_cat_kernel<<<grid_for((total + 31) / 32), kThreads, 0, st>>>(
-      static_cast<const uint4*>(Ws_out), c.n_shared, c.M, hs_units, static_cast<uint4*>(packed));
-  MOE_CUDA_CHECK(cudaGetLastError());
-  return MOE_OK;
+int launch_pack_in(const moe_config_t& c, int groups, int H, const void* W_in, const void* W_up,
+                   void* packed, cudaStream_t st) {
+  const int swiglu = c.act == MOE_ACT_SWIGLU;
+  const int N = swiglu ? 2 * H : H;
+  const int BN = gemm_bn(N, swiglu ? EPI_SWIGLU : EPI_RELU);
+  return run_pack(c, W_in, W_up, 0, swiglu, groups, N, c.M, H, 1, BN, packed, st);
+}
+
+int launch_pack_out(const moe_config_t& c, int groups, int H, int n_parts, const void* W_out,
+                    void* packed, cudaStream_t st) {
+  const int BN = gemm_bn(c.M, EPI_SCALE);
+  return run_pack(c, W_out, nullptr, 1, 0, groups, c.M, H * n_parts, H, n_parts, BN, packed, st);
 }
 
 }  // namespace moe

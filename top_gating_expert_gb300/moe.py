@@ -80,10 +80,11 @@ def workspace_bytes(cfg, kind: int = N.MOE_WS_LAYER) -> int:
 
 
 def packed_sizes(cfg):
-    a, b, c = N.c_int64(), N.c_int64(), N.c_int64()
+    """(W_in_packed, W_out_packed, Ws_in_packed, Ws_out_packed) element counts."""
+    a, b, c, d = N.c_int64(), N.c_int64(), N.c_int64(), N.c_int64()
     _check(N.lib().moe_packed_sizes(ctypes.byref(_cfg(cfg)), ctypes.byref(a), ctypes.byref(b),
-                                    ctypes.byref(c)), "moe_packed_sizes")
-    return a.value, b.value, c.value
+                                    ctypes.byref(c), ctypes.byref(d)), "moe_packed_sizes")
+    return a.value, b.value, c.value, d.value
 
 
 def workspace(cfg, kind: int = N.MOE_WS_LAYER, device="cuda") -> torch.Tensor:
@@ -125,18 +126,20 @@ class RouteOutputs:
 
 
 # ------------------------------------------------------------------ weight packing
-def pack_weights(cfg, W_in, W_up=None, stream=None) -> torch.Tensor:
+def pack_weights(cfg, W_in, W_up, W_out, stream=None):
+    """Returns (W_in_packed, W_out_packed) in the layout the expert GEMMs stream."""
     c = _cfg(cfg)
-    n_in, _, _ = packed_sizes(c)
-    packed = torch.empty(n_in, dtype=W_in.dtype, device=W_in.device)
-    _check(N.lib().moe_pack_weights(ctypes.byref(c), _ptr(W_in), _ptr(W_up), _ptr(packed),
-                                    _stream(stream)), "moe_pack_weights")
-    return packed
+    n_in, n_out, _, _ = packed_sizes(c)
+    p_in = torch.empty(n_in, dtype=W_in.dtype, device=W_in.device)
+    p_out = torch.empty(n_out, dtype=W_in.dtype, device=W_in.device)
+    _check(N.lib().moe_pack_weights(ctypes.byref(c), _ptr(W_in), _ptr(W_up), _ptr(W_out),
+                                    _ptr(p_in), _ptr(p_out), _stream(stream)), "moe_pack_weights")
+    return p_in, p_out
 
 
 def pack_shared_weights(cfg, Ws_in, Ws_up, Ws_out, stream=None):
     c = _cfg(cfg)
-    _, n_in, n_out = packed_sizes(c)
+    _, _, n_in, n_out = packed_sizes(c)
     p_in = torch.empty(n_in, dtype=Ws_in.dtype, device=Ws_in.device)
     p_out = torch.empty(n_out, dtype=Ws_in.dtype, device=Ws_in.device)
     _check(N.lib().moe_pack_shared_weights(ctypes.byref(c), _ptr(Ws_in), _ptr(Ws_up), _ptr(Ws_out),
@@ -177,16 +180,16 @@ def expert_up(cfg, x_perm, expert_offsets, W_in_packed, h_perm, ws, stream=None)
                                  _stream(stream)), "moe_expert_up")
 
 
-def expert_down(cfg, h_perm, expert_offsets, w_perm, W_out, y_perm, ws, stream=None):
+def expert_down(cfg, h_perm, expert_offsets, w_perm, W_out_packed, y_perm, ws, stream=None):
     _check(N.lib().moe_expert_down(ctypes.byref(_cfg(cfg)), _ptr(h_perm), _ptr(expert_offsets),
-                                   _ptr(w_perm), _ptr(W_out), _ptr(y_perm), _ptr(ws), ws.numel(),
-                                   _stream(stream)), "moe_expert_down")
+                                   _ptr(w_perm), _ptr(W_out_packed), _ptr(y_perm), _ptr(ws),
+                                   ws.numel(), _stream(stream)), "moe_expert_down")
 
 
-def expert_ffn(cfg, x_perm, expert_offsets, w_perm, W_in_packed, W_out, h_perm, y_perm, ws,
+def expert_ffn(cfg, x_perm, expert_offsets, w_perm, W_in_packed, W_out_packed, h_perm, y_perm, ws,
                stream=None):
     _check(N.lib().moe_expert_ffn(ctypes.byref(_cfg(cfg)), _ptr(x_perm), _ptr(expert_offsets),
-                                  _ptr(w_perm), _ptr(W_in_packed), _ptr(W_out), _ptr(h_perm),
+                                  _ptr(w_perm), _ptr(W_in_packed), _ptr(W_out_packed), _ptr(h_perm),
                                   _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_expert_ffn")
 
@@ -204,11 +207,11 @@ def combine(cfg, y_perm, out: RouteOutputs, shared_out, residual, y, stream=None
            "moe_combine")
 
 
-def layer_forward(cfg, x, W_g, bias, W_in_packed, W_out, Ws_in_packed, Ws_out_packed, u, residual,
-                  y, logits_out, out: RouteOutputs, ws, stream=None):
+def layer_forward(cfg, x, W_g, bias, W_in_packed, W_out_packed, Ws_in_packed, Ws_out_packed, u,
+                  residual, y, logits_out, out: RouteOutputs, ws, stream=None):
     s = out.struct()
     _check(N.lib().moe_layer_forward(
-        ctypes.byref(_cfg(cfg)), _ptr(x), _ptr(W_g), _ptr(bias), _ptr(W_in_packed), _ptr(W_out),
+        ctypes.byref(_cfg(cfg)), _ptr(x), _ptr(W_g), _ptr(bias), _ptr(W_in_packed), _ptr(W_out_packed),
         _ptr(Ws_in_packed), _ptr(Ws_out_packed), _ptr(u), _ptr(residual), _ptr(y), _ptr(logits_out),
         ctypes.byref(s), _ptr(ws), ws.numel(), _stream(stream)), "moe_layer_forward")
 
@@ -234,10 +237,9 @@ class MoeLayer:
         dev = torch.device(device)
         to = lambda t: None if t is None else t.to(device=dev, dtype=dt).contiguous()
         self.W_g = to(weights["W_g"])
-        W_in, W_up = to(weights["W_in"]), to(weights.get("W_up"))
-        self.W_out = to(weights["W_out"])
-        self.W_in_packed = pack_weights(self.cfg, W_in, W_up)
-        del W_in, W_up
+        W_in, W_up, W_out = to(weights["W_in"]), to(weights.get("W_up")), to(weights["W_out"])
+        self.W_in_packed, self.W_out_packed = pack_weights(self.cfg, W_in, W_up, W_out)
+        del W_in, W_up, W_out
         self.bias = None if weights.get("bias") is None else weights["bias"].to(dev, torch.float32)
         self.Ws_in_packed = self.Ws_out_packed = None
         if self.cfg.n_shared > 0:
@@ -250,7 +252,7 @@ class MoeLayer:
         self.device = dev
 
     def forward(self, x, u=None, residual=None, stream=None):
-        layer_forward(self.cfg, x, self.W_g, self.bias, self.W_in_packed, self.W_out,
+        layer_forward(self.cfg, x, self.W_g, self.bias, self.W_in_packed, self.W_out_packed,
                       self.Ws_in_packed, self.Ws_out_packed, u, residual, self.y, self.logits,
                       self.route_out, self.ws, stream)
         return self.y
