@@ -192,3 +192,40 @@ def test_layer_forward_equals_step_calls(run):
     assert np.array_equal(to_np(layer.logits), run["logits"])
     y2 = layer.forward(d["x"], d["u"] if cfg["random_routing"] else None, residual=d["x"])
     assert np.array_equal(to_np(y2), run["y_res"])
+
+
+def test_graph_replay_equals_eager(run):
+    """The whole forward captured as a CUDA graph gives the eager call's bits."""
+    cfg, d = run["cfg"], run["dev"]
+    layer = moe.MoeLayer(cfg, {k: run["inp"].host[k] for k in run["inp"].host})
+    u = d["u"] if cfg["random_routing"] else None
+    layer.capture(d["x"], u)
+    layer.y.zero_()
+    y = layer.replay()
+    torch.cuda.synchronize()
+    assert moe.device_status(layer.ws) == 0
+    assert np.array_equal(to_np(y), run["y"])
+
+
+def test_host_pipeline_matches_eager(run):
+    """HostPipeline (pinned host in/out, two steps in flight) returns, step by step, the bits
+    of the eager forward on the same inputs."""
+    cfg = run["cfg"]
+    layer = moe.MoeLayer(cfg, {k: run["inp"].host[k] for k in run["inp"].host})
+    rr = bool(cfg["random_routing"])
+    pipe = moe.HostPipeline(layer, has_u=rr)
+    x0 = run["inp"].host["x"]
+    xs = [(x0 * (1.0 + 0.25 * i)).to(x0.dtype).pin_memory() for i in range(3)]
+    u_host = run["inp"].host["u"].pin_memory() if rr else None
+    ys = [torch.empty_like(x0).pin_memory() for _ in range(3)]
+    losses = [torch.empty(2, dtype=torch.float32).pin_memory() for _ in range(3)]
+    for i in range(3):
+        pipe.submit(i, xs[i], u_host, ys[i], losses[i])
+    torch.cuda.synchronize()
+    assert moe.device_status(layer.ws) == 0
+    for i in range(3):
+        y = layer.forward(xs[i].cuda(), u_host.cuda() if rr else None)
+        torch.cuda.synchronize()
+        assert torch.equal(ys[i], y.cpu()), i
+        assert losses[i][0].item() == layer.route_out.aux_loss.item()
+        assert losses[i][1].item() == layer.route_out.z_loss.item()

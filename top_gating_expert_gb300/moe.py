@@ -251,10 +251,31 @@ class MoeLayer:
         self.y = torch.empty((self.cfg.S, self.cfg.M), dtype=dt, device=dev)
         self.device = dev
 
-    def forward(self, x, u=None, residual=None, stream=None):
+    def forward(self, x, u=None, residual=None, stream=None, out=None):
+        y = self.y if out is None else out
         layer_forward(self.cfg, x, self.W_g, self.bias, self.W_in_packed, self.W_out_packed,
-                      self.Ws_in_packed, self.Ws_out_packed, u, residual, self.y, self.logits,
+                      self.Ws_in_packed, self.Ws_out_packed, u, residual, y, self.logits,
                       self.route_out, self.ws, stream)
+        return y
+
+    def capture(self, x, u=None, residual=None, warmup: int = 1) -> torch.cuda.CUDAGraph:
+        """Capture forward(x, u, residual) into a CUDA graph (one launch per replay). x, u,
+        residual and the layer's outputs stay the graph's fixed buffers: write new inputs
+        into them and call replay()."""
+        side = torch.cuda.Stream(device=self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                self.forward(x, u, residual)
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.forward(x, u, residual)
+        self._graph = graph
+        return graph
+
+    def replay(self):
+        self._graph.replay()
         return self.y
 
     def forward_from_host(self, x_host, u_host=None, y_host=None, losses_host=None, stream=None):
@@ -274,3 +295,66 @@ class MoeLayer:
             self._loss_dev[1:2].copy_(self.route_out.z_loss)
             losses_host.copy_(self._loss_dev, non_blocking=True)
         return y_host
+
+
+class HostPipeline:
+    """Pinned-host in, pinned-host out, `depth` steps in flight.
+
+    Step i copies its inputs host->device on a copy stream, runs the layer (a CUDA graph per
+    buffer set) on the compute stream, and copies y and the two losses device->host on a
+    second copy stream, so step i's input copy and step i-1's output copy overlap the
+    compute of the steps around them. Buffer set i % depth is reused only after step
+    i - depth's output copy has finished."""
+
+    def __init__(self, layer: MoeLayer, has_u: bool, depth: int = 2):
+        dev = layer.device
+        c = layer.cfg
+        dt = torch_dtype(c)
+        self.layer, self.depth = layer, depth
+        self.x = [torch.empty((c.S, c.M), dtype=dt, device=dev) for _ in range(depth)]
+        self.u = [torch.empty(c.S, dtype=torch.float32, device=dev) if has_u else None
+                  for _ in range(depth)]
+        self.y = [torch.empty((c.S, c.M), dtype=dt, device=dev) for _ in range(depth)]
+        self.loss = [torch.empty(2, dtype=torch.float32, device=dev) for _ in range(depth)]
+        self.compute = torch.cuda.current_stream(dev)
+        self.h2d = torch.cuda.Stream(device=dev)
+        self.d2h = torch.cuda.Stream(device=dev)
+        self.ev_in = [torch.cuda.Event() for _ in range(depth)]
+        self.ev_done = [torch.cuda.Event() for _ in range(depth)]
+        self.ev_free = [torch.cuda.Event() for _ in range(depth)]
+        self.graphs = []
+        for b in range(depth):
+            self.x[b].zero_()
+            if has_u:
+                self.u[b].fill_(0.5)
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(self.compute)
+            with torch.cuda.stream(side):
+                layer.forward(self.x[b], self.u[b], out=self.y[b])
+            self.compute.wait_stream(side)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                layer.forward(self.x[b], self.u[b], out=self.y[b])
+                self.loss[b][0:1].copy_(layer.route_out.aux_loss)
+                self.loss[b][1:2].copy_(layer.route_out.z_loss)
+            self.graphs.append(g)
+        torch.cuda.synchronize(dev)
+
+    def submit(self, i: int, x_host, u_host=None, y_host=None, loss_host=None):
+        b = i % self.depth
+        self.h2d.wait_event(self.ev_free[b])
+        with torch.cuda.stream(self.h2d):
+            self.x[b].copy_(x_host, non_blocking=True)
+            if u_host is not None:
+                self.u[b].copy_(u_host, non_blocking=True)
+            self.ev_in[b].record(self.h2d)
+        self.compute.wait_event(self.ev_in[b])
+        self.graphs[b].replay()
+        self.ev_done[b].record(self.compute)
+        self.d2h.wait_event(self.ev_done[b])
+        with torch.cuda.stream(self.d2h):
+            if y_host is not None:
+                y_host.copy_(self.y[b], non_blocking=True)
+            if loss_host is not None:
+                loss_host.copy_(self.loss[b], non_blocking=True)
+            self.ev_free[b].record(self.d2h)
