@@ -182,7 +182,8 @@ def run_ours(args, rank, world, local_rank):
     n = args.config
     cfg = preset_for(args)
     inp = make_inputs(cfg, preset_number=n)
-    layer = moe.MoeLayer(cfg, inp.host, device=dev)
+    # the layer's step output is y and the losses: the bf16 path never writes the logits
+    layer = moe.MoeLayer(cfg, inp.host, device=dev, keep_logits=False)
     c = layer.cfg
     x = inp.host["x"].to(dev)
     u = inp.host["u"].to(dev) if cfg["random_routing"] else None
@@ -190,7 +191,9 @@ def run_ours(args, rank, world, local_rank):
     residual = x if n == 5 else None
     R_max = moe.rows_max(c)
     dt = moe.torch_dtype(c)
-    ws, out, logits = layer.ws, layer.route_out, layer.logits
+    ws, out = layer.ws, layer.route_out
+    fused = cfg["dtype"] == "bf16"
+    logits = None if fused else torch.empty((c.S, c.E), dtype=torch.float32, device=dev)
     x_perm = torch.empty((R_max, c.M), dtype=dt, device=dev)
     h_perm = torch.empty((R_max, c.H), dtype=dt, device=dev)
     y_perm = torch.empty((R_max, c.M), dtype=dt, device=dev)
@@ -214,22 +217,29 @@ def run_ours(args, rank, world, local_rank):
 
     flush = _Flush()
 
-    names = ["router", "route", "dispatch", "expert_up", "expert_down"] + \
-            (["shared_ffn"] if shared else []) + ["combine"]
-    launches = {"router": 1, "route": 3, "dispatch": 1, "expert_up": 1, "expert_down": 1,
-                "shared_ffn": 2, "combine": 1}
+    names = (["router_route"] if fused else ["router", "route"]) + \
+            ["dispatch", "expert_up", "expert_down"] + (["shared_ffn"] if shared else []) + ["combine"]
+    launches = {"router_route": 3, "router": 1, "route": 3, "dispatch": 1, "expert_up": 1,
+                "expert_down": 1, "shared_ffn": 2, "combine": 1}
 
     def step(evs=None):
         def mark(i):
             if evs is not None:
                 evs[i].record()
         mark(0)
-        moe.router(c, x, layer.W_g, bias, logits, ws); mark(1)
-        moe.route(c, logits, u, out, ws); mark(2)
-        moe.dispatch(c, x, out, x_perm); mark(3)
-        moe.expert_up(c, x_perm, out.expert_offsets, layer.W_in_packed, h_perm, ws); mark(4)
-        moe.expert_down(c, h_perm, out.expert_offsets, out.w_perm, layer.W_out_packed, y_perm, ws); mark(5)
-        i = 6
+        i = 1
+        if fused:
+            moe.router_route(c, x, layer.W_g, bias, u, None, out, ws); mark(i)
+            i += 1
+        else:
+            moe.router(c, x, layer.W_g, bias, logits, ws); mark(i)
+            moe.route(c, logits, u, out, ws); mark(i + 1)
+            i += 2
+        moe.dispatch(c, x, out, x_perm); mark(i)
+        moe.expert_up(c, x_perm, out.expert_offsets, layer.W_in_packed, h_perm, ws); mark(i + 1)
+        moe.expert_down(c, h_perm, out.expert_offsets, out.w_perm, layer.W_out_packed, y_perm, ws)
+        mark(i + 2)
+        i += 3
         if shared:
             moe.shared_ffn(c, x, layer.Ws_in_packed, layer.Ws_out_packed, h_sh, s_out, ws); mark(i)
             i += 1
@@ -344,6 +354,10 @@ def run_ours(args, rank, world, local_rank):
         "router": (S * M * eb + E * M * eb + S * E * 4 + (E * 4 if bias is not None else 0),
                    2.0 * S * M * E),
         "route": (S * E * 4 + S * 4 + S * k * (4 + 4 + 4 + 1 + 4) + R * 8, 0.0),
+        # x and W_g in; u in; per assignment id, gate, pos, row (int32/fp32) and drop (u8); the
+        # inverse map and gate per kept row (the logits never leave the chip)
+        "router_route": (S * M * eb + E * M * eb + (E * 4 if bias is not None else 0) + S * 4
+                         + S * k * (4 + 4 + 4 + 1 + 4) + R * 8, 2.0 * S * M * E),
         "dispatch": (2 * R * M * eb + R * 4, 0.0),
         "expert_up": (used * f1 * H * M * eb + R * M * eb + R * H * eb, 2.0 * f1 * R * M * H),
         "expert_down": (used * M * H * eb + R * H * eb + R * M * eb + R * 4, 2.0 * R * M * H),

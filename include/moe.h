@@ -215,6 +215,25 @@ int moe_route(const moe_config_t* cfg, const float* logits, const float* u,
               const moe_route_out_t* out, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_router followed by moe_route in one pass over x: the same outputs in *out, and the
+ * logits in logits_out when it is non-null (Lec16 Systems for MoE Models, "MoE Kernel
+ * 优化": the gating function -- projection, softmax, top-k and the token-to-expert table --
+ * fused instead of one kernel per step).
+ *   bf16: one kernel per 128-token chunk computes the chunk's logits on the tensor cores
+ *         and routes from them without writing them to memory (unless logits_out is
+ *         given), then moe_route's scan and finalize kernels run. logits_out may be NULL.
+ *   fp32: moe_router into logits_out, then moe_route; logits_out must be non-null.
+ * The routing outputs are what moe_route computes from the logits this call forms (and
+ * stores in logits_out when non-null), bit for bit. Those logits are moe_router's up to
+ * fp32 summation order: each 128-token chunk adds its 64-wide blocks of the model
+ * dimension starting at a chunk-dependent block. Passing logits_out or not changes no
+ * other output. ws: MOE_WS_STEP bytes. Errors: as moe_router and moe_route.
+ */
+int moe_router_route(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
+                     const float* u, float* logits_out, const moe_route_out_t* out, void* ws,
+                     size_t ws_bytes, moe_stream_t stream);
+
+/*
  * moe_route without a workspace, for callers that cannot allocate device memory. The
  * paper has no counterpart: this is a deployment convenience of this library.
  *
@@ -282,7 +301,7 @@ int moe_combine(const moe_config_t* cfg, const void* y_perm, const moe_route_out
                 const void* shared_out, const void* residual, void* y, moe_stream_t stream);
 
 /*
- * The whole layer: moe_router, moe_route, moe_dispatch, moe_expert_ffn, moe_shared_ffn
+ * The whole layer: moe_router_route, moe_dispatch, moe_expert_ffn, moe_shared_ffn
  * (when n_shared > 0) and moe_combine, with the intermediates carved from ws
  * (MOE_WS_LAYER bytes). logits_out (float [S, E]) receives the router logits when
  * non-null. W_*_packed / Ws_*_packed come from the pack calls above; bias, u, residual

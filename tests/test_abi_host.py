@@ -96,6 +96,15 @@ def test_compute_entry_points_check_arguments_on_host(native_lib):
                             None) == -1
     assert L.moe_layer_forward(ctypes.byref(c), fake, fake, None, fake, fake, None, None, fake, None,
                                fake, None, ctypes.byref(out2), fake, 16, None) == -3
+    assert L.moe_router_route(ctypes.byref(c), None, fake, None, fake, None, ctypes.byref(out2), fake,
+                              need, None) == -1
+    assert L.moe_router_route(ctypes.byref(c), fake, fake, None, None, None, ctypes.byref(out2), fake,
+                              need, None) == -1  # random routing needs u
+    assert L.moe_router_route(ctypes.byref(c), fake, fake, None, fake, None, ctypes.byref(out2), fake,
+                              16, None) == -3
+    c32 = moe.make_config(CONFIGS[1])
+    assert L.moe_router_route(ctypes.byref(c32), fake, fake, None, fake, None, ctypes.byref(out2),
+                              fake, moe.workspace_bytes(c32, N.MOE_WS_STEP), None) == -1  # fp32 needs logits_out
     assert L.moe_get_device_status(None, None) == -1
     # shared-expert calls need shared experts
     assert L.moe_shared_ffn(ctypes.byref(c), fake, fake, fake, fake, fake, fake, need, None) == -1

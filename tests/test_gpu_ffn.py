@@ -9,7 +9,8 @@ import pytest
 import torch
 
 from oracle import moe_oracle as O
-from gpu_util import (RTOL, LOGIT_RTOL, assert_close, compare_route, oracle_cfg, route_np, to_np)
+from gpu_util import (LOSS_RTOL, RTOL, LOGIT_RTOL, assert_close, compare_route, oracle_cfg, route_np,
+                      to_np)
 from top_gating_expert_gb300 import _native as N
 from top_gating_expert_gb300 import moe
 from top_gating_expert_gb300.inputs import make_inputs, preset
@@ -56,8 +57,9 @@ def run(request, native_lib):
     ws = moe.workspace(cfg, N.MOE_WS_STEP, dev)
     out = moe.RouteOutputs.allocate(cfg, dev)
     logits = torch.empty((cfg["S"], cfg["E"]), dtype=torch.float32, device=dev)
-    moe.router(cfg, d["x"], d["W_g"], d.get("bias"), logits, ws)
-    moe.route(cfg, logits, d["u"] if cfg["random_routing"] else None, out, ws)
+    # the router and routing as the layer runs them (bf16: one fused kernel + scan + finalize)
+    moe.router_route(cfg, d["x"], d["W_g"], d.get("bias"), d["u"] if cfg["random_routing"] else None,
+                     logits, out, ws)
     x_perm = torch.full((R_max, cfg["M"]), float("nan"), dtype=dt, device=dev)
     moe.dispatch(cfg, d["x"], out, x_perm)
     W_in_p, W_out_p = moe.pack_weights(cfg, d["W_in"], d.get("W_up"), d["W_out"])
@@ -96,6 +98,63 @@ def test_route_bit_exact(run):
     cfg = run["cfg"]
     o = O.route(run["logits"], oracle_cfg(cfg), run["inp"].np["u"])
     compare_route(run["route"], o, run["name"])
+
+
+def _same_route(g, want, what):
+    R = int(want["expert_offsets"][-1])
+    for key in ("expert_id", "gate", "pos", "drop_reason", "row", "counts", "counts_routed",
+                "expert_offsets"):
+        assert np.array_equal(g[key], want[key]), f"{what}: {key}"
+    assert np.array_equal(g["token_of"][:R], want["token_of"][:R]), f"{what}: token_of"
+    assert np.array_equal(g["w_perm"][:R], want["w_perm"][:R]), f"{what}: w_perm"
+    for key in ("aux_loss", "z_loss"):
+        a, b = float(g[key][0]), float(want[key][0])
+        assert abs(a - b) <= LOSS_RTOL * abs(b) + 1e-7, (what, key, a, b)
+
+
+def test_router_route_without_logits_out(run):
+    """moe_router_route that keeps its logits on chip gives the same bits as the run that
+    also stored them (the fixture's)."""
+    cfg, d = run["cfg"], run["dev"]
+    if cfg["dtype"] != "bf16":
+        pytest.skip("the fp32 path needs logits_out")
+    ws = moe.workspace(cfg, N.MOE_WS_STEP, "cuda")
+    out = moe.RouteOutputs.allocate(cfg, "cuda")
+    moe.router_route(cfg, d["x"], d["W_g"], d.get("bias"), d["u"] if cfg["random_routing"] else None,
+                     None, out, ws)
+    assert moe.device_status(ws) == 0
+    _same_route(route_np(out), run["route"], run["name"])
+
+
+def test_unfused_router_then_route(run):
+    """The two separate steps (moe_router, then moe_route from the stored logits): logits
+    within tolerance of the oracle's and of the fused kernel's, routing bit-exact against the
+    oracle routed from them."""
+    cfg, d, a = run["cfg"], run["dev"], run["inp"].np
+    ws = moe.workspace(cfg, N.MOE_WS_STEP, "cuda")
+    out = moe.RouteOutputs.allocate(cfg, "cuda")
+    logits = torch.empty((cfg["S"], cfg["E"]), dtype=torch.float32, device="cuda")
+    moe.router(cfg, d["x"], d["W_g"], d.get("bias"), logits, ws)
+    moe.route(cfg, logits, d["u"] if cfg["random_routing"] else None, out, ws)
+    assert moe.device_status(ws) == 0
+    lg = to_np(logits)
+    assert_close(lg, O.router_logits(a["x"], a["W_g"], a.get("bias")), LOGIT_RTOL[cfg["dtype"]],
+                 "logits")
+    assert_close(lg, run["logits"], LOGIT_RTOL[cfg["dtype"]], "logits vs fused")
+    compare_route(route_np(out), O.route(lg, oracle_cfg(cfg), a["u"]), run["name"])
+
+
+def test_layer_without_logits_equals_with(run):
+    """A layer that does not keep its logits (the benchmark's) computes the same step."""
+    cfg, d = run["cfg"], run["dev"]
+    if cfg["dtype"] != "bf16":
+        pytest.skip("the fp32 path always materialises logits")
+    layer = moe.MoeLayer(cfg, {k: run["inp"].host[k] for k in run["inp"].host}, keep_logits=False)
+    y = layer.forward(d["x"], d["u"] if cfg["random_routing"] else None)
+    assert moe.device_status(layer.ws) == 0
+    assert layer.logits is None
+    assert np.array_equal(to_np(y), run["y"])
+    _same_route(route_np(layer.route_out), run["route"], run["name"])
 
 
 def test_dispatch_exact(run):
@@ -183,7 +242,7 @@ def test_layer_output_vs_oracle(run):
 
 
 def test_layer_forward_equals_step_calls(run):
-    """moe_layer_forward launches the same kernels: identical bits."""
+    """moe_layer_forward launches the step calls' kernels: identical bits."""
     cfg, d = run["cfg"], run["dev"]
     layer = moe.MoeLayer(cfg, {k: run["inp"].host[k] for k in run["inp"].host})
     y = layer.forward(d["x"], d["u"] if cfg["random_routing"] else None)

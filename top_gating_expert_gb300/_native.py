@@ -51,6 +51,8 @@ _PROTOTYPES = {
     "moe_router": [_P(MoeConfig), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
                    c_void_p],
     "moe_route": [_P(MoeConfig), c_void_p, c_void_p, _P(MoeRouteOut), c_void_p, c_size_t, c_void_p],
+    "moe_router_route": [_P(MoeConfig), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                         _P(MoeRouteOut), c_void_p, c_size_t, c_void_p],
     "moe_route_noalloc": [_P(MoeConfig), c_void_p, c_void_p, _P(MoeRouteOut), c_void_p, c_void_p],
     "moe_dispatch": [_P(MoeConfig), c_void_p, _P(MoeRouteOut), c_void_p, c_void_p],
     "moe_expert_up": [_P(MoeConfig), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,

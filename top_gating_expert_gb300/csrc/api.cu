@@ -264,6 +264,25 @@ int moe_route(const moe_config_t* cfg, const float* logits, const float* u,
                       static_cast<char*>(ws), p.L, stream);
 }
 
+int moe_router_route(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
+                     const float* u, float* logits_out, const moe_route_out_t* out, void* ws,
+                     size_t ws_bytes, moe_stream_t stream) {
+  Prep p;
+  int rc = prepare(cfg, &p);
+  if (rc != MOE_OK) return rc;
+  if (!x || !W_g || (cfg->random_routing && !u)) return MOE_ERR_INVALID_ARG;
+  if (cfg->dtype == MOE_F32 && !logits_out) return MOE_ERR_INVALID_ARG;
+  if ((rc = check_route_out(*cfg, out)) != MOE_OK) return rc;
+  if ((rc = check_ws(ws, ws_bytes, p.L.step_bytes)) != MOE_OK) return rc;
+  if (cfg->dtype == MOE_F32) {
+    if ((rc = moe_router(cfg, x, W_g, bias, logits_out, ws, ws_bytes, stream)) != MOE_OK) return rc;
+    return moe_route(cfg, logits_out, u, out, ws, ws_bytes, stream);
+  }
+  if (logits_out && !aligned16(logits_out)) return MOE_ERR_INVALID_ARG;
+  return launch_router_route(*cfg, p.C, x, W_g, bias, cfg->random_routing ? u : nullptr,
+                             logits_out, *out, static_cast<char*>(ws), p.L, stream);
+}
+
 int moe_dispatch(const moe_config_t* cfg, const void* x, const moe_route_out_t* r, void* x_perm,
                  moe_stream_t stream) {
   Prep p;
@@ -349,13 +368,14 @@ int moe_layer_forward(const moe_config_t* cfg, const void* x, const void* W_g, c
   if ((rc = check_route_out(*cfg, r)) != MOE_OK) return rc;
   if ((rc = check_ws(ws, ws_bytes, p.L.layer_bytes)) != MOE_OK) return rc;
   char* w = static_cast<char*>(ws);
-  float* logits = logits_out ? logits_out : reinterpret_cast<float*>(w + p.L.logits);
+  float* logits = logits_out;
   void* x_perm = w + p.L.x_perm;
   void* h_perm = w + p.L.h_perm;
   void* y_perm = w + p.L.y_perm;
   void* shared_out = cfg->n_shared > 0 ? static_cast<void*>(w + p.L.s_out) : nullptr;
-  if ((rc = moe_router(cfg, x, W_g, bias, logits, ws, ws_bytes, stream)) != MOE_OK) return rc;
-  if ((rc = moe_route(cfg, logits, u, r, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  if (cfg->dtype == MOE_F32 && !logits) logits = reinterpret_cast<float*>(w + p.L.logits);
+  if ((rc = moe_router_route(cfg, x, W_g, bias, u, logits, r, ws, ws_bytes, stream)) != MOE_OK)
+    return rc;
   if ((rc = moe_dispatch(cfg, x, r, x_perm, stream)) != MOE_OK) return rc;
   if ((rc = moe_expert_ffn(cfg, x_perm, r->expert_offsets, r->w_perm, W_in_packed, W_out_packed,
                            h_perm, y_perm, ws, ws_bytes, stream)) != MOE_OK)

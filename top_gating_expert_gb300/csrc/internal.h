@@ -2,6 +2,7 @@
 // Not part of the public ABI (that is include/moe.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -92,6 +93,11 @@ inline int gemm_bn(int N, int epi) {
 // route.cu
 int launch_route(const moe_config_t& c, int C, const float* logits, const float* u,
                  const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st);
+// bf16 router projection fused with the first routing kernel (logits_out nullable), then the
+// same scan and finalize kernels as launch_route.
+int launch_router_route(const moe_config_t& c, int C, const void* x, const void* W_g,
+                        const float* bias, const float* u, float* logits_out,
+                        const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st);
 
 // permute.cu
 int launch_dispatch(const moe_config_t& c, int64_t R_max, const void* x, const int32_t* token_of,
@@ -126,6 +132,9 @@ struct GemmDesc {
   unsigned* status = nullptr;
 };
 int launch_gemm_bf16(const GemmDesc& d, cudaStream_t st);
+// 2-D tensor map over a row-major bf16 [rows, K] matrix, boxes of 64 columns x box_rows rows,
+// 128-byte swizzle (the operand layout of the tcgen05 kernels).
+int make_tma_map_rows(CUtensorMap* m, const void* base, int64_t rows, int K, int box_rows);
 
 // simt_f32.cu : plain-FMA fp32 path for small layers.
 int launch_router_f32(const moe_config_t& c, const float* x, const float* W_g, const float* bias,

@@ -30,6 +30,7 @@
 #include <math.h>
 
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace moe {
 namespace {
@@ -92,11 +93,13 @@ __device__ __forceinline__ bool ranks_before(float v, int i, float w, int j) {
   return v > w || (v == w && i < j);
 }
 
-// TPT threads per token (consecutive lanes), each owning experts sub, sub+TPT, ...
+// The per-chunk routing work on a chunk's logits staged in shared memory (s_log: nt rows of
+// E logits, row stride ld = E + TPT). TPT threads per token (consecutive lanes), each owning
+// experts sub, sub + TPT, ...; the CTA has kThreads * TPT threads, all of which call this.
+// Non-finite logits are replaced by -inf in s_log (and flagged).
 template <int K, int TPT>
-__global__ void __launch_bounds__(kThreads * TPT) route_topk_kernel(RouteArgs a) {
+__device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int c, int t0, int nt) {
   constexpr int kT = kThreads * TPT;
-  extern __shared__ float s_log[];  // [kThreads][E + TPT] (padded: conflict-free lanes)
   __shared__ float s_m[kThreads], s_inv[kThreads], s_pp[kT];
   __shared__ uint8_t s_id[kThreads * kMaxK];
   __shared__ uint8_t s_cand[kThreads];
@@ -104,33 +107,10 @@ __global__ void __launch_bounds__(kThreads * TPT) route_topk_kernel(RouteArgs a)
   __shared__ int s_route[kMaxE];
   __shared__ float s_z[kT / 32];
 
-  const int c = blockIdx.x;
-  const int g = c / a.n_cpg, cc = c % a.n_cpg;
-  const int t0 = g * a.Sg + cc * kThreads;
-  const int nt = min(kThreads, a.Sg - cc * kThreads);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, ld = E + TPT;
-
   if (c == 0 && tid == 0) *a.done = 0u;  // ticket counter of route_scan_kernel
   for (int e = tid; e < E; e += kT) s_route[e] = 0;
-
-  // stage the chunk's logits (contiguous rows t0..t0+nt-1) into padded shared memory
-  const float* __restrict__ src = a.logits + size_t(t0) * E;
-  const int n = nt * E;
-  if ((E & 3) == 0 && (ld & 3) == 0) {
-    const float4* __restrict__ src4 = reinterpret_cast<const float4*>(src);
-#pragma unroll 4
-    for (int q = tid; q < n / 4; q += kT) {
-      const int idx = q * 4, r = idx / E, col = idx - r * E;
-      *reinterpret_cast<float4*>(s_log + r * ld + col) = __ldg(src4 + q);
-    }
-  } else {
-#pragma unroll 4
-    for (int q = tid; q < n; q += kT) {
-      const int r = q / E;
-      s_log[r * ld + (q - r * E)] = __ldg(src + q);
-    }
-  }
   __syncthreads();
 
   // token i = tid / TPT; this thread's experts: sub, sub + TPT, ...
@@ -310,6 +290,210 @@ __global__ void __launch_bounds__(kThreads * TPT) route_topk_kernel(RouteArgs a)
     if (valid) a.rank[size_t(t0 + tid) * K + j] = e >= 0 ? s_wc[warp][e] + rk : -1;
     __syncthreads();
   }
+}
+
+// One CTA per chunk: stage the chunk's logits (contiguous rows t0..t0+nt-1, coalesced) into
+// padded shared memory, then topk_chunk.
+template <int K, int TPT>
+__global__ void __launch_bounds__(kThreads * TPT) route_topk_kernel(RouteArgs a) {
+  constexpr int kT = kThreads * TPT;
+  extern __shared__ float s_log[];  // [kThreads][E + TPT] (padded: conflict-free lanes)
+  const int c = blockIdx.x;
+  const int g = c / a.n_cpg, cc = c % a.n_cpg;
+  const int t0 = g * a.Sg + cc * kThreads;
+  const int nt = min(kThreads, a.Sg - cc * kThreads);
+  const int tid = threadIdx.x;
+  const int E = a.E, ld = E + TPT;
+  const float* __restrict__ src = a.logits + size_t(t0) * E;
+  const int n = nt * E;
+  if ((E & 3) == 0 && (ld & 3) == 0) {
+    const float4* __restrict__ src4 = reinterpret_cast<const float4*>(src);
+#pragma unroll 4
+    for (int q = tid; q < n / 4; q += kT) {
+      const int idx = q * 4, r = idx / E, col = idx - r * E;
+      *reinterpret_cast<float4*>(s_log + r * ld + col) = __ldg(src4 + q);
+    }
+  } else {
+#pragma unroll 4
+    for (int q = tid; q < n; q += kT) {
+      const int r = q / E;
+      s_log[r * ld + (q - r * E)] = __ldg(src + q);
+    }
+  }
+  topk_chunk<K, TPT>(a, s_log, c, t0, nt);  // its first barrier orders the staging
+}
+
+// ------------------------------------------------------------------ fused router + top-k
+// The router projection and route_topk_kernel's work in one kernel (bf16 inputs). A CTA of
+// kThreads * TPT threads takes one chunk: warp 0 streams the chunk's 128 rows of x and all
+// of W_g through a ring of shared-memory stages with TMA, warp 1 accumulates the 128 x E
+// logits tile with tcgen05.mma in tensor memory (fp32), warps 4..7 read it back (warp w
+// reads TMEM lanes 32 (w % 4) ..) and add the bias into padded shared memory laid out as
+// route_topk_kernel stages it (over the drained stage ring), optionally storing the logits
+// to memory too; then the whole CTA runs topk_chunk. The logits never round-trip through
+// HBM. Each chunk starts its K loop at its own k-block (rotated by the chunk index) so that
+// the CTAs do not all read the same W_g lines from L2 at the same time; the fp32 logits
+// are then summed in a chunk-dependent order of 64-wide blocks (within fp32 rounding of
+// any other order). Lec16 Systems for MoE Models, "MoE Kernel 优化": the gating function
+// as one fused kernel instead of one per step.
+struct FusedRouterArgs {
+  const float* bias;   // per-expert logit offset, nullable
+  float* logits_out;   // [S, E] fp32, nullable
+  int Mdim;            // contraction length (the model dimension)
+  int BN;              // MMA N = smallest of 16, 32, .., 256 that is >= E
+  int stages;
+};
+
+template <int K, int TPT>
+__global__ void __launch_bounds__(kThreads * TPT, 1)
+    router_topk_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                       RouteArgs a, FusedRouterArgs f) {
+  using namespace sm100;
+  static_assert(kThreads * TPT >= 256, "roles need warps 0, 1 and 4..7");
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bars[2 * 8 + 1];
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int BN = f.BN, NS = f.stages;
+  const int A_BYTES = 128 * 64 * 2, B_BYTES = BN * 64 * 2;
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + NS * A_BYTES;
+  float* s_log = reinterpret_cast<float*>(smem);  // reuses the ring once the MMAs are done
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * 8, done_bar = empty0 + 8 * 8;
+  const int tcols = BN < 32 ? 32 : BN;
+
+  const int c = blockIdx.x;
+  const int g = c / a.n_cpg, cc = c % a.n_cpg;
+  const int t0 = g * a.Sg + cc * kThreads;
+  const int nt = min(kThreads, a.Sg - cc * kThreads);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = a.E, ld = E + TPT;
+  const int kblocks = f.Mdim / 64;
+  const int rot = c % kblocks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(done_bar, 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_map(&tmX);
+    tma_prefetch_map(&tmW);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&s_tmem), tcols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, issued_par = 0;
+    bool ok = true;
+    for (int j = 0; j < kblocks; ++j) {
+      ok = __all_sync(0xffffffffu, wait_bounded(empty0 + 8 * stage, phase ^ 1u, &s_abort, a.status));
+      if (!ok) break;
+      if (lane == 0) {
+        int kb = j + rot;
+        if (kb >= kblocks) kb -= kblocks;
+        const uint32_t fb = full0 + 8 * stage;
+        mbar_expect_tx(fb, A_BYTES + B_BYTES);
+        tma_load_2d(smem_u32(sA + stage * A_BYTES), &tmX, kb * 64, t0, fb);
+        tma_load_2d(smem_u32(sB + stage * B_BYTES), &tmW, kb * 64, 0, fb);
+      }
+      __syncwarp();
+      issued |= 1u << stage;
+      issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+      if (++stage == NS) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0)
+      for (int s = 0; s < NS; ++s)
+        if ((issued >> s) & 1u) wait_drain(full0 + 8 * s, (issued_par >> s) & 1u);
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: one 128 x BN tile
+    const uint32_t idesc = idesc_bf16(128, BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true, any = false;
+    for (int j = 0; j < kblocks; ++j) {
+      ok = __all_sync(0xffffffffu, wait_bounded(full0 + 8 * stage, phase, &s_abort, a.status));
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t a0 = smem_u32(sA + stage * A_BYTES), b0 = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                   (j | kk) != 0 ? 1u : 0u);
+        mma_commit(empty0 + 8 * stage);
+      }
+      __syncwarp();
+      any = true;
+      if (++stage == NS) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    // done_bar completes once every MMA issued has finished (also after an abort, so that
+    // shared and tensor memory are reused or freed only once nothing writes them)
+    if (lane == 0 && any) mma_commit(done_bar);
+    if (!ok && any && lane == 0) wait_drain(done_bar, 0u);
+    __syncwarp();
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------- drain: token i = 32 q + lane owns TMEM lane i
+    const int q = warp & 3, i = q * 32 + lane;
+    const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
+    const bool ok = __all_sync(0xffffffffu, wait_bounded(done_bar, 0u, &s_abort, a.status));
+    if (ok) {
+      tc_fence_after();
+      const bool store = f.logits_out != nullptr && i < nt;
+      float* dst = store ? f.logits_out + size_t(t0 + i) * E : nullptr;
+      float* row = s_log + i * ld;
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(trow + c0, v);
+        tmem_ld_wait();
+        float l[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj)
+          l[jj] = __uint_as_float(v[jj]) + ((f.bias && c0 + jj < E) ? f.bias[c0 + jj] : 0.f);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj)
+          if (c0 + jj < E) row[c0 + jj] = l[jj];
+        if (store) {
+          if ((E & 3) == 0 && c0 + 16 <= E) {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+              reinterpret_cast<float4*>(dst + c0)[jj] =
+                  make_float4(l[4 * jj], l[4 * jj + 1], l[4 * jj + 2], l[4 * jj + 3]);
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              if (c0 + jj < E) dst[c0 + jj] = l[jj];
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tcols);
+  }
+  // after a timeout (flagged in the status word) the routing below runs, in bounds, on
+  // whatever the buffer holds rather than leaving its outputs unset
+  topk_chunk<K, TPT>(a, s_log, c, t0, nt);
 }
 
 // Column sums over rows [0, n) of a row-major [n][ncol] array in a fixed order: P segments
@@ -567,11 +751,30 @@ int launch_topk(const RouteArgs& a, int n_chunks, cudaStream_t st) {
   return launch_topk_t<K, 8>(a, n_chunks, st);
 }
 
-}  // namespace
+template <int K, int TPT>
+int launch_router_topk_t(const CUtensorMap& tx, const CUtensorMap& tw, const RouteArgs& a,
+                         const FusedRouterArgs& f, int n_chunks, cudaStream_t st) {
+  const size_t ring = size_t(f.stages) * (128 * 64 * 2 + size_t(f.BN) * 64 * 2);
+  const size_t stage_log = size_t(kThreads) * (a.E + TPT) * sizeof(float);
+  const size_t smem = (ring > stage_log ? ring : stage_log) + 1024;
+  MOE_CUDA_CHECK(cudaFuncSetAttribute(router_topk_kernel<K, TPT>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+  router_topk_kernel<K, TPT><<<n_chunks, kThreads * TPT, smem, st>>>(tx, tw, a, f);
+  MOE_CUDA_CHECK(cudaGetLastError());
+  return MOE_OK;
+}
 
-int launch_route(const moe_config_t& c, int C, const float* logits, const float* u,
-                 const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st) {
-  if (reinterpret_cast<uintptr_t>(logits) % 16 != 0) return MOE_ERR_INVALID_ARG;
+// as launch_topk, with at least two threads per token (the roles need eight warps)
+template <int K>
+int launch_router_topk(const CUtensorMap& tx, const CUtensorMap& tw, const RouteArgs& a,
+                       const FusedRouterArgs& f, int n_chunks, cudaStream_t st) {
+  if (a.E <= 32) return launch_router_topk_t<K, 2>(tx, tw, a, f, n_chunks, st);
+  if (a.E <= 64) return launch_router_topk_t<K, 4>(tx, tw, a, f, n_chunks, st);
+  return launch_router_topk_t<K, 8>(tx, tw, a, f, n_chunks, st);
+}
+
+RouteArgs route_args(const moe_config_t& c, int C, const float* logits, const float* u,
+                     const moe_route_out_t& out, char* ws, const WsLayout& L) {
   RouteArgs a;
   a.logits = logits;
   a.u = u;
@@ -592,7 +795,25 @@ int launch_route(const moe_config_t& c, int C, const float* logits, const float*
   a.gbase = reinterpret_cast<int32_t*>(ws + L.gbase);
   a.gaux = reinterpret_cast<float*>(ws + L.gaux);
   a.gz = reinterpret_cast<float*>(ws + L.gz);
+  return a;
+}
 
+// the two launches after the per-chunk kernel
+int launch_scan_finalize(const moe_config_t& c, const RouteArgs& a, cudaStream_t st) {
+  route_scan_kernel<<<c.G, kScanThreads, 0, st>>>(a);
+  MOE_CUDA_CHECK(cudaGetLastError());
+  const int64_t n = int64_t(c.S) * c.k;
+  route_finalize_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(a);
+  MOE_CUDA_CHECK(cudaGetLastError());
+  return MOE_OK;
+}
+
+}  // namespace
+
+int launch_route(const moe_config_t& c, int C, const float* logits, const float* u,
+                 const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st) {
+  if (reinterpret_cast<uintptr_t>(logits) % 16 != 0) return MOE_ERR_INVALID_ARG;
+  const RouteArgs a = route_args(c, C, logits, u, out, ws, L);
   int rc;
   switch (c.k) {
     case 1: rc = launch_topk<1>(a, L.n_chunks, st); break;
@@ -605,12 +826,42 @@ int launch_route(const moe_config_t& c, int C, const float* logits, const float*
     default: rc = launch_topk<8>(a, L.n_chunks, st); break;
   }
   if (rc != MOE_OK) return rc;
-  route_scan_kernel<<<c.G, kScanThreads, 0, st>>>(a);
-  MOE_CUDA_CHECK(cudaGetLastError());
-  const int64_t n = int64_t(c.S) * c.k;
-  route_finalize_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(a);
-  MOE_CUDA_CHECK(cudaGetLastError());
-  return MOE_OK;
+  return launch_scan_finalize(c, a, st);
+}
+
+int launch_router_route(const moe_config_t& c, int C, const void* x, const void* W_g,
+                        const float* bias, const float* u, float* logits_out,
+                        const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st) {
+  FusedRouterArgs f;
+  f.bias = bias;
+  f.logits_out = logits_out;
+  f.Mdim = c.M;
+  f.BN = gemm_bn(c.E, EPI_F32_BIAS);
+  if (f.BN == 0 || c.M % 64 != 0 || c.M <= 0) return MOE_ERR_UNSUPPORTED;
+  // one CTA per SM (up to 1024 threads at <= 64 registers): the ring takes ~192 KB
+  const int stage_bytes = 128 * 64 * 2 + f.BN * 64 * 2;
+  int stages = (192 * 1024) / stage_bytes;
+  stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+  const int kblocks = c.M / 64;
+  if (stages > kblocks) stages = kblocks;
+  f.stages = stages;
+  CUtensorMap tx, tw;
+  int rc = make_tma_map_rows(&tx, x, c.S, c.M, 128);
+  if (rc != MOE_OK) return rc;
+  if ((rc = make_tma_map_rows(&tw, W_g, c.E, c.M, f.BN)) != MOE_OK) return rc;
+  const RouteArgs a = route_args(c, C, nullptr, u, out, ws, L);
+  switch (c.k) {
+    case 1: rc = launch_router_topk<1>(tx, tw, a, f, L.n_chunks, st); break;
+    case 2: rc = launch_router_topk<2>(tx, tw, a, f, L.n_chunks, st); break;
+    case 3: rc = launch_router_topk<3>(tx, tw, a, f, L.n_chunks, st); break;
+    case 4: rc = launch_router_topk<4>(tx, tw, a, f, L.n_chunks, st); break;
+    case 5: rc = launch_router_topk<5>(tx, tw, a, f, L.n_chunks, st); break;
+    case 6: rc = launch_router_topk<6>(tx, tw, a, f, L.n_chunks, st); break;
+    case 7: rc = launch_router_topk<7>(tx, tw, a, f, L.n_chunks, st); break;
+    default: rc = launch_router_topk<8>(tx, tw, a, f, L.n_chunks, st); break;
+  }
+  if (rc != MOE_OK) return rc;
+  return launch_scan_finalize(c, a, st);
 }
 
 }  // namespace moe

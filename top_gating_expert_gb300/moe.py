@@ -160,6 +160,15 @@ def route(cfg, logits, u, out: RouteOutputs, ws, stream=None):
                              _ptr(ws), ws.numel(), _stream(stream)), "moe_route")
 
 
+def router_route(cfg, x, W_g, bias, u, logits_out, out: RouteOutputs, ws, stream=None):
+    """moe_router + moe_route in one pass (bf16: the logits stay on chip unless logits_out
+    is given; fp32 needs logits_out)."""
+    s = out.struct()
+    _check(N.lib().moe_router_route(ctypes.byref(_cfg(cfg)), _ptr(x), _ptr(W_g), _ptr(bias), _ptr(u),
+                                    _ptr(logits_out), ctypes.byref(s), _ptr(ws), ws.numel(),
+                                    _stream(stream)), "moe_router_route")
+
+
 def route_noalloc(cfg, logits, u, out: RouteOutputs, device_status=None, stream=None):
     """moe_route without a workspace (scratch in the library's fixed 4 MiB device array),
     for callers that cannot allocate device memory; see include/moe.h."""
@@ -229,7 +238,9 @@ class MoeLayer:
     the step's inputs from (pinned) host tensors, runs the layer and copies y and the two
     losses back."""
 
-    def __init__(self, cfg: dict, weights: dict, device="cuda"):
+    def __init__(self, cfg: dict, weights: dict, device="cuda", keep_logits: bool = True):
+        """keep_logits: also store the router logits in ``self.logits`` on every forward
+        (for inspection and tests); without it the bf16 path never writes them."""
         self.cfg_dict = cfg
         self.cfg = make_config(cfg)
         _check(validate(self.cfg), "moe_validate_config")
@@ -247,7 +258,8 @@ class MoeLayer:
                 self.cfg, to(weights["Ws_in"]), to(weights.get("Ws_up")), to(weights["Ws_out"]))
         self.ws = workspace(self.cfg, N.MOE_WS_LAYER, dev)
         self.route_out = RouteOutputs.allocate(self.cfg, dev)
-        self.logits = torch.zeros((self.cfg.S, self.cfg.E), dtype=torch.float32, device=dev)
+        self.logits = (torch.zeros((self.cfg.S, self.cfg.E), dtype=torch.float32, device=dev)
+                       if keep_logits else None)
         self.y = torch.empty((self.cfg.S, self.cfg.M), dtype=dt, device=dev)
         self.device = dev
 
