@@ -1,11 +1,20 @@
 // The C ABI of include/moe.h: argument checks, workspace carving and the order of launches.
 // Every check that can fail does so on the host, before anything is launched.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "internal.h"
 
 namespace moe {
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("MOE_PDL");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
 
 int num_sms() {
   int dev = 0, n = 0;

@@ -218,6 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (PAIR) tmem_alloc_pair(smem_u32(s_tmem), C::TMEM_COLS);
     else tmem_alloc(smem_u32(s_tmem), C::TMEM_COLS);
   }
+  pdl_wait();  // everything above is local setup; below, the first reads of the inputs
+  pdl_trigger();
   if (warp == 2) {
     // m-tile prefix over the groups, from the device row offsets
     bool bad = false;
@@ -492,7 +494,7 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
   lc.blockDim = dim3(kThreads);
   lc.dynamicSmemBytes = C::SMEM;
   lc.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   int64_t units = num_sms();
   if constexpr (PAIR) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -510,6 +512,12 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
   if (units > tiles) units = tiles;
   if (units < 1) units = 1;
   lc.gridDim = dim3(unsigned(units * C::CTAS));
+  if (pdl_enabled()) {  // see launch_kernel
+    attr[lc.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[lc.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs += 1;
+  }
   MOE_CUDA_CHECK(cudaLaunchKernelEx(&lc, kern, ta, tb, p));
   return MOE_OK;
 }

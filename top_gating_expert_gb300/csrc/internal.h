@@ -148,6 +148,38 @@ int launch_ffn_down_f32(const moe_config_t& c, int H, const float* h, const int3
 
 int num_sms();
 
+// Programmatic dependent launch: every kernel of the library is launched with programmatic
+// stream serialisation (unless the environment sets MOE_PDL=0), so that it may start while
+// its predecessor in the stream drains. Each kernel therefore calls pdl_wait() before its
+// first global-memory access (it returns once the preceding kernel has completed and its
+// writes are visible; without the attribute it returns at once), then pdl_trigger() to let
+// its own successor be scheduled.
+bool pdl_enabled();
+
+template <typename... Params, typename... Args>
+int launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                  Args&&... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (pdl_enabled()) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+  }
+  if (cudaLaunchKernelEx(&lc, kernel, static_cast<Args&&>(args)...) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#endif
+
 }  // namespace moe
 
 #define MOE_CUDA_CHECK(call)                       \

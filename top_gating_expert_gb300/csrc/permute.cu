@@ -38,6 +38,8 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(const uint4* __restr
                                                             const int32_t* __restrict__ offsets,
                                                             int E, int S, int units, int64_t R_max,
                                                             uint4* __restrict__ x_perm) {
+  pdl_wait();
+  pdl_trigger();
   int64_t R = offsets[E];
   R = R < 0 ? 0 : (R > R_max ? R_max : R);
   const int lane = threadIdx.x & 31;
@@ -109,6 +111,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
     const uint4* __restrict__ y_perm, const int32_t* __restrict__ row, int k, int S, int units,
     int64_t R_max, const uint4* __restrict__ shared, const uint4* __restrict__ residual,
     uint4* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
@@ -230,20 +234,17 @@ unsigned grid_for(int64_t warps_needed) {
 int launch_dispatch(const moe_config_t& c, int64_t R_max, const void* x, const int32_t* token_of,
                     const int32_t* offsets, void* x_perm, cudaStream_t st) {
   const int units = int(c.M * elem_bytes(c) / 16);
-  dispatch_kernel<<<grid_for(R_max), kThreads, 0, st>>>(
-      static_cast<const uint4*>(x), token_of, offsets, c.E, c.S, units, R_max,
-      static_cast<uint4*>(x_perm));
-  MOE_CUDA_CHECK(cudaGetLastError());
-  return MOE_OK;
+  return launch_kernel(dispatch_kernel, dim3(grid_for(R_max)), dim3(kThreads), 0, st,
+                       static_cast<const uint4*>(x), token_of, offsets, c.E, c.S, units, R_max,
+                       static_cast<uint4*>(x_perm));
 }
 
 template <bool kBF16>
-void combine_dispatch_k(int k, unsigned grid, cudaStream_t st, const uint4* yp, const int32_t* row,
-                        int S, int units, int64_t R_max, const uint4* sh, const uint4* res,
-                        uint4* y) {
-  if (k <= 2) combine_kernel<kBF16, 2><<<grid, kThreads, 0, st>>>(yp, row, k, S, units, R_max, sh, res, y);
-  else if (k <= 4) combine_kernel<kBF16, 4><<<grid, kThreads, 0, st>>>(yp, row, k, S, units, R_max, sh, res, y);
-  else combine_kernel<kBF16, 8><<<grid, kThreads, 0, st>>>(yp, row, k, S, units, R_max, sh, res, y);
+int combine_dispatch_k(int k, unsigned grid, cudaStream_t st, const uint4* yp, const int32_t* row,
+                       int S, int units, int64_t R_max, const uint4* sh, const uint4* res,
+                       uint4* y) {
+  auto kern = k <= 2 ? combine_kernel<kBF16, 2> : (k <= 4 ? combine_kernel<kBF16, 4> : combine_kernel<kBF16, 8>);
+  return launch_kernel(kern, dim3(grid), dim3(kThreads), 0, st, yp, row, k, S, units, R_max, sh, res, y);
 }
 
 int launch_combine(const moe_config_t& c, const void* y_perm, const int32_t* row,
@@ -255,10 +256,8 @@ int launch_combine(const moe_config_t& c, const void* y_perm, const int32_t* row
   auto sh = static_cast<const uint4*>(shared_out);
   auto res = static_cast<const uint4*>(residual);
   auto yo = static_cast<uint4*>(y);
-  if (c.dtype == MOE_BF16) combine_dispatch_k<true>(c.k, grid, st, yp, row, c.S, units, R_max, sh, res, yo);
-  else combine_dispatch_k<false>(c.k, grid, st, yp, row, c.S, units, R_max, sh, res, yo);
-  MOE_CUDA_CHECK(cudaGetLastError());
-  return MOE_OK;
+  if (c.dtype == MOE_BF16) return combine_dispatch_k<true>(c.k, grid, st, yp, row, c.S, units, R_max, sh, res, yo);
+  return combine_dispatch_k<false>(c.k, grid, st, yp, row, c.S, units, R_max, sh, res, yo);
 }
 
 namespace {

@@ -304,6 +304,8 @@ __global__ void __launch_bounds__(kThreads * TPT) route_topk_kernel(RouteArgs a)
   const int nt = min(kThreads, a.Sg - cc * kThreads);
   const int tid = threadIdx.x;
   const int E = a.E, ld = E + TPT;
+  pdl_wait();
+  pdl_trigger();
   const float* __restrict__ src = a.logits + size_t(t0) * E;
   const int n = nt * E;
   if ((E & 3) == 0 && (ld & 3) == 0) {
@@ -390,6 +392,8 @@ __global__ void __launch_bounds__(kThreads * TPT, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     // ---------------- TMA producer
@@ -554,6 +558,8 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(RouteArgs a) {
   const int g = blockIdx.x, tid = threadIdx.x;
   const int E = a.E, k = a.k, ncol = k * E, n = a.n_cpg;
   const size_t c0 = size_t(g) * n;
+  pdl_wait();
+  pdl_trigger();
 
   // candidate histograms: exclusive scan over the group's chunks, per (j, e) column
   int P = kScanThreads / ncol;
@@ -695,6 +701,8 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(RouteArgs a) {
 }
 
 __global__ void __launch_bounds__(256) route_finalize_kernel(RouteArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= int64_t(a.S) * a.k) return;
   const int t = int(idx / a.k), j = int(idx % a.k);
@@ -737,9 +745,7 @@ int launch_topk_t(const RouteArgs& a, int n_chunks, cudaStream_t st) {
   const size_t smem = size_t(kThreads) * (a.E + TPT) * sizeof(float);
   MOE_CUDA_CHECK(cudaFuncSetAttribute(route_topk_kernel<K, TPT>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-  route_topk_kernel<K, TPT><<<n_chunks, kThreads * TPT, smem, st>>>(a);
-  MOE_CUDA_CHECK(cudaGetLastError());
-  return MOE_OK;
+  return launch_kernel(route_topk_kernel<K, TPT>, dim3(n_chunks), dim3(kThreads * TPT), smem, st, a);
 }
 
 // threads per token: enough lanes that each holds at most 16 experts
@@ -759,9 +765,8 @@ int launch_router_topk_t(const CUtensorMap& tx, const CUtensorMap& tw, const Rou
   const size_t smem = (ring > stage_log ? ring : stage_log) + 1024;
   MOE_CUDA_CHECK(cudaFuncSetAttribute(router_topk_kernel<K, TPT>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-  router_topk_kernel<K, TPT><<<n_chunks, kThreads * TPT, smem, st>>>(tx, tw, a, f);
-  MOE_CUDA_CHECK(cudaGetLastError());
-  return MOE_OK;
+  return launch_kernel(router_topk_kernel<K, TPT>, dim3(n_chunks), dim3(kThreads * TPT), smem, st,
+                       tx, tw, a, f);
 }
 
 // as launch_topk, with at least two threads per token (the roles need eight warps)
@@ -800,12 +805,10 @@ RouteArgs route_args(const moe_config_t& c, int C, const float* logits, const fl
 
 // the two launches after the per-chunk kernel
 int launch_scan_finalize(const moe_config_t& c, const RouteArgs& a, cudaStream_t st) {
-  route_scan_kernel<<<c.G, kScanThreads, 0, st>>>(a);
-  MOE_CUDA_CHECK(cudaGetLastError());
+  int rc = launch_kernel(route_scan_kernel, dim3(c.G), dim3(kScanThreads), 0, st, a);
+  if (rc != MOE_OK) return rc;
   const int64_t n = int64_t(c.S) * c.k;
-  route_finalize_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(a);
-  MOE_CUDA_CHECK(cudaGetLastError());
-  return MOE_OK;
+  return launch_kernel(route_finalize_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, st, a);
 }
 
 }  // namespace

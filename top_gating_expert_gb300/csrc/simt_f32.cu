@@ -14,6 +14,8 @@ namespace {
 __global__ void router_f32_kernel(const float* __restrict__ x, const float* __restrict__ W_g,
                                   const float* __restrict__ bias, int S, int E, int M,
                                   float* __restrict__ logits) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= int64_t(S) * E) return;
   const int64_t t = idx / E;
@@ -42,6 +44,8 @@ __device__ __forceinline__ int group_of(const int32_t* offsets, int groups, int6
 __global__ void ffn_up_f32_kernel(const float* __restrict__ A, const int32_t* __restrict__ offsets,
                                   int groups, int rows_dense, int64_t rows_cap, int M, int H,
                                   int swiglu, const float* __restrict__ W, float* __restrict__ h) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t r = idx / H;
   const int j = int(idx % H);
@@ -76,6 +80,8 @@ __global__ void ffn_down_f32_kernel(const float* __restrict__ h, const int32_t* 
                                     int groups, int rows_dense, int64_t rows_cap, int M, int H,
                                     const float* __restrict__ scale, const float* __restrict__ W,
                                     float* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t r = idx / M;
   const int m = int(idx % M);
@@ -99,29 +105,25 @@ __global__ void ffn_down_f32_kernel(const float* __restrict__ h, const int32_t* 
 int launch_router_f32(const moe_config_t& c, const float* x, const float* W_g, const float* bias,
                       float* logits, cudaStream_t st) {
   const int64_t n = int64_t(c.S) * c.E;
-  router_f32_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(x, W_g, bias, c.S, c.E, c.M, logits);
-  MOE_CUDA_CHECK(cudaGetLastError());
-  return MOE_OK;
+  return launch_kernel(router_f32_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, st, x, W_g,
+                       bias, c.S, c.E, c.M, logits);
 }
 
 int launch_ffn_up_f32(const moe_config_t& c, int H, const float* A, const int32_t* offsets,
                       int groups, int rows_dense, int64_t rows_cap, const float* W_packed,
                       float* h, unsigned* /*status*/, cudaStream_t st) {
   const int64_t n = rows_cap * H;
-  ffn_up_f32_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(
-      A, offsets, groups, rows_dense, rows_cap, c.M, H, c.act == MOE_ACT_SWIGLU, W_packed, h);
-  MOE_CUDA_CHECK(cudaGetLastError());
-  return MOE_OK;
+  return launch_kernel(ffn_up_f32_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, st, A,
+                       offsets, groups, rows_dense, rows_cap, c.M, H, int(c.act == MOE_ACT_SWIGLU),
+                       W_packed, h);
 }
 
 int launch_ffn_down_f32(const moe_config_t& c, int H, const float* h, const int32_t* offsets,
                         int groups, int rows_dense, int64_t rows_cap, const float* row_scale,
                         const float* W_out, float* y, unsigned* /*status*/, cudaStream_t st) {
   const int64_t n = rows_cap * c.M;
-  ffn_down_f32_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(
-      h, offsets, groups, rows_dense, rows_cap, c.M, H, row_scale, W_out, y);
-  MOE_CUDA_CHECK(cudaGetLastError());
-  return MOE_OK;
+  return launch_kernel(ffn_down_f32_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, st, h,
+                       offsets, groups, rows_dense, rows_cap, c.M, H, row_scale, W_out, y);
 }
 
 }  // namespace moe
