@@ -54,7 +54,7 @@ inline WsLayout ws_layout(const moe_config_t& c, int C) {
   L.zpart = o;  o = align256(o + size_t(L.n_chunks) * 4);
   L.rank = o;   o = align256(o + size_t(c.S) * c.k * 4);
   L.gbase = o;  o = align256(o + size_t(c.G) * c.E * 4);
-  L.gaux = o;   o = align256(o + size_t(c.G) * 4);
+  L.gaux = o;   o = align256(o + size_t(c.G) * c.E * 4);  // [G][<= E slices]
   L.gz = o;     o = align256(o + size_t(c.G) * 4);
   L.step_bytes = o;
   const int64_t R = rows_max(c, C);

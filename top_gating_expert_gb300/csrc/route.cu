@@ -18,12 +18,13 @@
 //      max, sum-exp, gates and the random-routing decision. The CTA ranks its candidates per
 //      (choice rank j, expert) with warp match + a scan over warps, and writes per-chunk
 //      histograms, routed counts, per-expert softmax-probability sums and the
-//      logsumexp^2 sum (fixed summation orders: deterministic).
-//   2. route_scan_kernel   one CTA per group: exclusive scan of the chunk histograms in
-//      (choice rank, chunk) order -- the GShard queue order -- giving each chunk's first slot
-//      per (j, expert); kept counts per (group, expert); the group's aux-loss term. The last
-//      CTA to finish (atomic ticket, no waiting) forms expert_offsets, the per-(group,
-//      expert) first rows and the two loss scalars.
+//      logsumexp^2 sum (fixed summation orders: deterministic). router_topk_kernel does the
+//      same after computing the chunk's logits itself on the tensor cores.
+//   2. route_scan_kernel   X CTAs per group, each a slice of the experts: exclusive scans of
+//      the chunk histograms in (choice rank, chunk) order -- the GShard queue order -- giving
+//      each chunk's first slot per (j, expert); kept counts per (group, expert); the slice's
+//      aux-loss term. The last CTA to finish (atomic ticket, no waiting) forms
+//      expert_offsets, the per-(group, expert) first rows and the two loss scalars.
 //   3. route_finalize_kernel  one thread per assignment: slot, keep/drop, row, inverse map.
 // Every integer output is a pure function of the logits and u: no atomic decides an order.
 #include <float.h>
@@ -39,8 +40,8 @@ constexpr int kThreads = kRouteChunk;  // one token per thread
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 8;
-constexpr int kScanThreads = 1024;
-constexpr int kBatch = 16;  // loads kept in flight per thread in the column scans
+constexpr int kScanThreads = 256;
+constexpr int kBatch = 16;  // loads kept in flight per thread in the scans
 
 struct RouteArgs {
   const float* logits;
@@ -67,7 +68,7 @@ struct RouteArgs {
   float* zpart;     // [n_chunks]: sum of logsumexp^2 per chunk
   int32_t* rank;    // [S][k]: rank among the chunk's candidates of the same (j, e); -1 if none
   int32_t* gbase;   // [G][E]: first row of (group, expert)
-  float* gaux;      // [G]
+  float* gaux;      // [G][X]: aux-loss term of each expert slice of each group
   float* gz;        // [G]
 };
 
@@ -93,12 +94,21 @@ __device__ __forceinline__ bool ranks_before(float v, int i, float w, int j) {
   return v > w || (v == w && i < j);
 }
 
+// The random-routing draw of this thread's token when it is the token's first lane (read
+// early, so that its latency hides behind the staging of the logits).
+template <int K, int TPT>
+__device__ __forceinline__ float token_u(const RouteArgs& a, int t0, int nt) {
+  const int i = int(threadIdx.x) / TPT;
+  return (K == 2 && a.rr && int(threadIdx.x) % TPT == 0 && i < nt) ? __ldg(a.u + t0 + i) : 0.f;
+}
+
 // The per-chunk routing work on a chunk's logits staged in shared memory (s_log: nt rows of
 // E logits, row stride ld = E + TPT). TPT threads per token (consecutive lanes), each owning
 // experts sub, sub + TPT, ...; the CTA has kThreads * TPT threads, all of which call this.
 // Non-finite logits are replaced by -inf in s_log (and flagged).
 template <int K, int TPT>
-__device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int c, int t0, int nt) {
+__device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int c, int t0, int nt,
+                                           float u_tok) {
   constexpr int kT = kThreads * TPT;
   __shared__ float s_m[kThreads], s_inv[kThreads], s_pp[kT];
   __shared__ uint8_t s_id[kThreads * kMaxK];
@@ -215,7 +225,7 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
         gsum += gw[j];
       }
       unsigned cand = 0xffu;
-      if (K == 2 && a.rr && !rr_keep(bestv[0], bestv[1], a.u[t])) cand &= ~2u;
+      if (K == 2 && a.rr && !rr_keep(bestv[0], bestv[1], u_tok)) cand &= ~2u;
       s_cand[i] = uint8_t(cand);
       const float ginv = 1.f / gsum;
 #pragma unroll
@@ -306,6 +316,7 @@ __global__ void __launch_bounds__(kThreads * TPT) route_topk_kernel(RouteArgs a)
   const int E = a.E, ld = E + TPT;
   pdl_wait();
   pdl_trigger();
+  const float u_tok = token_u<K, TPT>(a, t0, nt);
   const float* __restrict__ src = a.logits + size_t(t0) * E;
   const int n = nt * E;
   if ((E & 3) == 0 && (ld & 3) == 0) {
@@ -322,7 +333,7 @@ __global__ void __launch_bounds__(kThreads * TPT) route_topk_kernel(RouteArgs a)
       s_log[r * ld + (q - r * E)] = __ldg(src + q);
     }
   }
-  topk_chunk<K, TPT>(a, s_log, c, t0, nt);  // its first barrier orders the staging
+  topk_chunk<K, TPT>(a, s_log, c, t0, nt, u_tok);  // its first barrier orders the staging
 }
 
 // ------------------------------------------------------------------ fused router + top-k
@@ -394,6 +405,7 @@ __global__ void __launch_bounds__(kThreads * TPT, 1)
   const uint32_t tmem = s_tmem;
   pdl_wait();
   pdl_trigger();
+  const float u_tok = token_u<K, TPT>(a, t0, nt);
 
   if (warp == 0) {
     // ---------------- TMA producer
@@ -497,36 +509,7 @@ __global__ void __launch_bounds__(kThreads * TPT, 1)
   }
   // after a timeout (flagged in the status word) the routing below runs, in bounds, on
   // whatever the buffer holds rather than leaving its outputs unset
-  topk_chunk<K, TPT>(a, s_log, c, t0, nt);
-}
-
-// Column sums over rows [0, n) of a row-major [n][ncol] array in a fixed order: P segments
-// of rows, each summed in row order with kBatch loads in flight, then the segments in order.
-template <typename T>
-__device__ void column_sums(const T* __restrict__ base, int ncol, int n, T* s_part, T* out) {
-  int P = kScanThreads / ncol;
-  P = P < 1 ? 1 : (P > n ? n : P);
-  const int L = (n + P - 1) / P;
-  for (int idx = threadIdx.x; idx < ncol * P; idx += blockDim.x) {
-    const int col = idx % ncol, s = idx / ncol;
-    const int cb = s * L, ce = min(n, cb + L);
-    T sum = T(0);
-    for (int r0 = cb; r0 < ce; r0 += kBatch) {
-      T v[kBatch];
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) v[q] = (r0 + q < ce) ? base[size_t(r0 + q) * ncol + col] : T(0);
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) sum += v[q];
-    }
-    s_part[idx] = sum;
-  }
-  __syncthreads();
-  for (int col = threadIdx.x; col < ncol; col += blockDim.x) {
-    T sum = T(0);
-    for (int s = 0; s < P; ++s) sum += s_part[s * ncol + col];
-    out[col] = sum;
-  }
-  __syncthreads();
+  topk_chunk<K, TPT>(a, s_log, c, t0, nt, u_tok);
 }
 
 // Fixed-order block reduction of one float per thread (all threads participate).
@@ -544,159 +527,269 @@ __device__ float block_sum(float v, float* s_red) {
   return r;  // valid in thread 0
 }
 
-__global__ void __launch_bounds__(kScanThreads) route_scan_kernel(RouteArgs a) {
-  __shared__ int s_part[2 * kScanThreads];
-  __shared__ int s_tot[kMaxK * kMaxE];
-  __shared__ int s_routed[kMaxE];
-  __shared__ float s_fpart[kScanThreads];
-  __shared__ float s_psum[kMaxE];
-  __shared__ float s_zsum[1];
-  __shared__ float s_red[32];
-  __shared__ int s_off[kMaxE + 1];
+// CTA (g, x) of a G x X grid takes group g's experts e0 .. e0 + nw - 1 (e0 = x * ew): the
+// columns (j, e) of the chunk histograms, each an exclusive scan down the group's chunks
+// offset by the group's candidates of choice ranks j' < j for e (the GShard queue order:
+// all first choices, then all second choices, each in token order), and the sums over
+// chunks of the routed counts and probability sums of its experts (the group's
+// logsumexp^2 sum in the x = 0 CTA). A thread owns one (segment of chunks, column) and
+// issues all its loads before using any. The last CTA to finish (atomic ticket, no
+// waiting) forms expert_offsets, the first row of every (group, expert) and the two loss
+// scalars. Every sum has a fixed order.
+__global__ void __launch_bounds__(kScanThreads) route_scan_kernel(RouteArgs a, int X, int ew) {
+  __shared__ int s_ph[kScanThreads];      // hist segment sums, then exclusive prefixes
+  __shared__ int s_pr[kScanThreads];      // routed-count segment sums (j = 0 columns)
+  __shared__ float s_pp[kScanThreads];    // probability segment sums (j = 0 columns)
+  __shared__ float s_pz[kScanThreads];    // logsumexp^2 segment sums (column 0, x = 0)
+  __shared__ int s_tot[kScanThreads];     // column totals
+  __shared__ int s_routed[kScanThreads];
+  __shared__ float s_psum[kScanThreads];
+  __shared__ float s_red[kScanThreads / 32];
+  __shared__ int s_wsum[kScanThreads / 32];
   __shared__ int s_last;
 
-  const int g = blockIdx.x, tid = threadIdx.x;
-  const int E = a.E, k = a.k, ncol = k * E, n = a.n_cpg;
-  const size_t c0 = size_t(g) * n;
-  pdl_wait();
-  pdl_trigger();
-
-  // candidate histograms: exclusive scan over the group's chunks, per (j, e) column
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = blockIdx.x / X, x = blockIdx.x % X;
+  const int E = a.E, k = a.k, n = a.n_cpg, KE = k * E;
+  const int e0 = x * ew, nw = min(ew, E - e0);
+  const int ncol = k * nw;  // <= kScanThreads (host)
   int P = kScanThreads / ncol;
   P = P < 1 ? 1 : (P > n ? n : P);
   const int L = (n + P - 1) / P;
-  int32_t* __restrict__ hist = a.hist + c0 * ncol;
-  for (int idx = tid; idx < ncol * P; idx += kScanThreads) {
-    const int col = idx % ncol, s = idx / ncol;
-    const int cb = s * L, ce = min(n, cb + L);
-    int sum = 0;
+  pdl_wait();
+  pdl_trigger();
+
+  const int col = tid % ncol, seg = tid / ncol;
+  const bool active = seg < P;
+  const int j = col / nw, el = col % nw, e = e0 + el;
+  const bool lead = j == 0;
+  const bool zl = x == 0 && col == 0;
+  const int cb = min(n, seg * L), ce = min(n, cb + L);
+  const size_t c0 = size_t(g) * n;
+  int32_t* __restrict__ hist = a.hist + c0 * KE + size_t(j) * E + e;  // rows KE apart
+  const int32_t* __restrict__ hr = a.hroute + c0 * E + e;
+  const float* __restrict__ pp = a.ppart + c0 * E + e;
+  const float* __restrict__ zp = a.zpart + c0;
+
+  int keep[kBatch];
+  int hs = 0, rs = 0;
+  float ps = 0.f, zs = 0.f;
+  if (active) {
     for (int r0 = cb; r0 < ce; r0 += kBatch) {
-      int v[kBatch];
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) v[q] = (r0 + q < ce) ? hist[size_t(r0 + q) * ncol + col] : 0;
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) sum += v[q];
-    }
-    s_part[idx] = sum;
-  }
-  __syncthreads();
-  for (int col = tid; col < ncol; col += kScanThreads) {
-    int run = 0;
-    for (int s = 0; s < P; ++s) {
-      const int v = s_part[s * ncol + col];
-      s_part[s * ncol + col] = run;
-      run += v;
-    }
-    s_tot[col] = run;
-  }
-  __syncthreads();
-  for (int idx = tid; idx < ncol * P; idx += kScanThreads) {
-    const int col = idx % ncol, s = idx / ncol;
-    const int j = col / E, e = col % E;
-    int run = s_part[idx];
-    for (int jj = 0; jj < j; ++jj) run += s_tot[jj * E + e];  // earlier choice ranks first
-    const int cb = s * L, ce = min(n, cb + L);
-    for (int r0 = cb; r0 < ce; r0 += kBatch) {
-      int v[kBatch];
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) v[q] = (r0 + q < ce) ? hist[size_t(r0 + q) * ncol + col] : 0;
+      int v[kBatch], w[kBatch];
+      float p[kBatch], z[kBatch];
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
-        if (r0 + q < ce) hist[size_t(r0 + q) * ncol + col] = run;
-        run += v[q];
+        const bool in = r0 + q < ce;
+        v[q] = in ? hist[size_t(r0 + q) * KE] : 0;
+        w[q] = (in && lead) ? hr[size_t(r0 + q) * E] : 0;
+        p[q] = (in && lead) ? pp[size_t(r0 + q) * E] : 0.f;
+        z[q] = (in && zl) ? zp[r0 + q] : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        hs += v[q];
+        rs += w[q];
+        ps += p[q];
+        zs += z[q];
+        if (r0 == cb) keep[q] = v[q];
       }
     }
   }
-  for (int e = tid; e < E; e += kScanThreads) {
-    int cand = 0;
-    for (int j = 0; j < k; ++j) cand += s_tot[j * E + e];
-    a.counts[g * E + e] = (a.C >= 0 && cand > a.C) ? a.C : cand;
+  s_ph[tid] = hs;
+  s_pr[tid] = rs;
+  s_pp[tid] = ps;
+  s_pz[tid] = zs;
+  __syncthreads();
+
+  // per column, over its P segments in order: exclusive prefix (in place) and totals
+  if (P <= 8) {
+    if (tid < ncol) {
+      int run = 0, rr = 0;
+      float pr = 0.f, zr = 0.f;
+      for (int s = 0; s < P; ++s) {
+        const int i = s * ncol + tid;
+        const int v = s_ph[i];
+        s_ph[i] = run;
+        run += v;
+        rr += s_pr[i];
+        pr += s_pp[i];
+        zr += s_pz[i];
+      }
+      s_tot[tid] = run;
+      if (tid < nw) {
+        s_routed[tid] = rr;
+        s_psum[tid] = pr;
+      }
+      if (tid == 0 && x == 0) a.gz[g] = zr;
+    }
+  } else {  // one warp per column: lane l takes segments l*per .. l*per + per - 1
+    const int per = (P + 31) / 32;
+    for (int cl = warp; cl < ncol; cl += kScanThreads / 32) {
+      const int s0 = lane * per, s1 = min(P, s0 + per);
+      int loc = 0, rr = 0;
+      float pr = 0.f, zr = 0.f;
+      for (int s = s0; s < s1; ++s) {
+        const int i = s * ncol + cl;
+        loc += s_ph[i];
+        rr += s_pr[i];
+        pr += s_pp[i];
+        zr += s_pz[i];
+      }
+      int inc = loc;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += v;
+      }
+      int run = inc - loc;
+      for (int s = s0; s < s1; ++s) {
+        const int i = s * ncol + cl;
+        const int v = s_ph[i];
+        s_ph[i] = run;
+        run += v;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        rr += __shfl_xor_sync(0xffffffffu, rr, off);
+        pr += __shfl_xor_sync(0xffffffffu, pr, off);
+        zr += __shfl_xor_sync(0xffffffffu, zr, off);
+      }
+      if (lane == 31) s_tot[cl] = inc;
+      if (lane == 0) {
+        if (cl < nw) {
+          s_routed[cl] = rr;
+          s_psum[cl] = pr;
+        }
+        if (cl == 0 && x == 0) a.gz[g] = zr;
+      }
+    }
   }
   __syncthreads();
 
-  // routed counts, probability sums and logsumexp^2 sum of the group
-  column_sums<int>(a.hroute + c0 * E, E, n, s_part, s_routed);
-  column_sums<float>(a.ppart + c0 * E, E, n, s_fpart, s_psum);
-  column_sums<float>(a.zpart + c0, 1, n, s_fpart, s_zsum);
-  for (int e = tid; e < E; e += kScanThreads) a.counts_routed[g * E + e] = s_routed[e];
-  // aux term of the group: E * sum_e (routed_e / (Sg*k)) * (psum_e / Sg)
-  const float term = tid < E ? float(s_routed[tid]) * s_psum[tid] : 0.f;
-  const float tsum = block_sum(term, s_red);
-  if (tid == 0) {
-    a.gaux[g] = float(double(tsum) * double(E) / (double(a.Sg) * a.k * double(a.Sg)));
-    a.gz[g] = s_zsum[0];
+  // first slot of every (chunk, j, e) of the segment
+  if (active && cb < ce) {
+    int run = s_ph[seg * ncol + col];
+    for (int jj = 0; jj < j; ++jj) run += s_tot[jj * nw + el];
+    if (L <= kBatch) {
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        if (cb + q < ce) {
+          hist[size_t(cb + q) * KE] = run;
+          run += keep[q];
+        }
+      }
+    } else {
+      for (int r0 = cb; r0 < ce; r0 += kBatch) {
+        int v[kBatch];
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) v[q] = (r0 + q < ce) ? hist[size_t(r0 + q) * KE] : 0;
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+          if (r0 + q < ce) hist[size_t(r0 + q) * KE] = run;
+          run += v[q];
+        }
+      }
+    }
+  }
+  if (tid < nw) {
+    int cand = 0;
+    for (int jj = 0; jj < k; ++jj) cand += s_tot[jj * nw + tid];
+    a.counts[g * E + e0 + tid] = (a.C >= 0 && cand > a.C) ? a.C : cand;
+    a.counts_routed[g * E + e0 + tid] = s_routed[tid];
+  }
+  // this slice's share of the group's load-balancing term: sum over its experts of
+  // routed_e * psum_e (lanes over experts, then a fixed tree)
+  if (warp == 0) {
+    float t = 0.f;
+    for (int i = lane; i < nw; i += 32) t += float(s_routed[i]) * s_psum[i];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    if (lane == 0) a.gaux[size_t(g) * X + x] = t;
   }
 
-  // the last group to finish forms the offsets and the loss scalars
+  // the last CTA to finish forms the offsets and the loss scalars
   __threadfence();
   __syncthreads();
   if (tid == 0) s_last = (atomicAdd(a.done, 1u) == gridDim.x - 1);
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  const int G = a.G;
   const int32_t* __restrict__ counts = a.counts;
-  for (int e = tid; e < E; e += kScanThreads) {
-    int tot = 0;
-    for (int g0 = 0; g0 < a.G; g0 += kBatch) {
+  int tot = 0;  // rows of expert tid over all groups
+  if (tid < E) {
+    for (int g0 = 0; g0 < G; g0 += kBatch) {
       int v[kBatch];
 #pragma unroll
-      for (int q = 0; q < kBatch; ++q) v[q] = (g0 + q < a.G) ? __ldcg(counts + (g0 + q) * E + e) : 0;
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) tot += v[q];
-    }
-    s_routed[e] = tot;
-  }
-  __syncthreads();
-  if (tid < 32) {  // exclusive scan over experts: 8 per lane, then a warp scan
-    const int per = (E + 31) / 32;
-    int loc = 0;
-    for (int q = 0; q < per; ++q) {
-      const int e = tid * per + q;
-      if (e < E) loc += s_routed[e];
-    }
-    int inc = loc;
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, inc, off);
-      if (tid >= off) inc += v;
-    }
-    int run = inc - loc;
-    for (int q = 0; q < per; ++q) {
-      const int e = tid * per + q;
-      if (e < E) {
-        s_off[e] = run;
-        a.offsets[e] = run;
-        run += s_routed[e];
-      }
-    }
-    if (tid == 31) a.offsets[E] = inc;
-  }
-  {  // loss scalars: fixed-order sums over groups
-    float ga = 0.f, gzs = 0.f;
-    for (int gg = tid; gg < a.G; gg += kScanThreads) {
-      ga += __ldcg(a.gaux + gg);
-      gzs += __ldcg(a.gz + gg);
-    }
-    ga = block_sum(ga, s_red);
-    gzs = block_sum(gzs, s_red);
-    if (tid == 0) {
-      *a.aux = ga / float(a.G);
-      *a.z = gzs / float(a.S);
-      *a.done = 0u;
-    }
-  }
-  __syncthreads();
-  for (int e = tid; e < E; e += kScanThreads) {
-    int run = s_off[e];
-    for (int g0 = 0; g0 < a.G; g0 += kBatch) {
-      int v[kBatch];
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) v[q] = (g0 + q < a.G) ? __ldcg(counts + (g0 + q) * E + e) : 0;
+      for (int q = 0; q < kBatch; ++q) v[q] = (g0 + q < G) ? __ldcg(counts + (g0 + q) * E + tid) : 0;
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
-        if (g0 + q < a.G) a.gbase[(g0 + q) * E + e] = run;
-        run += v[q];
+        tot += v[q];
+        if (g0 == 0) keep[q] = v[q];
       }
     }
+  }
+  // exclusive scan of tot over the experts (thread order)
+  int inc = tot;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += v;
+  }
+  if (lane == 31) s_wsum[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int v = lane < kScanThreads / 32 ? s_wsum[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v += u;
+    }
+    if (lane < kScanThreads / 32) s_wsum[lane] = v;  // inclusive over warps
+  }
+  __syncthreads();
+  const int off_e = inc - tot + (warp > 0 ? s_wsum[warp - 1] : 0);
+  if (tid < E) {
+    a.offsets[tid] = off_e;
+    if (tid == E - 1) a.offsets[E] = off_e + tot;
+    int run = off_e;
+    if (G <= kBatch) {
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        if (q < G) {
+          a.gbase[q * E + tid] = run;
+          run += keep[q];
+        }
+      }
+    } else {
+      for (int g0 = 0; g0 < G; g0 += kBatch) {
+        int v[kBatch];
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) v[q] = (g0 + q < G) ? __ldcg(counts + (g0 + q) * E + tid) : 0;
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+          if (g0 + q < G) a.gbase[(g0 + q) * E + tid] = run;
+          run += v[q];
+        }
+      }
+    }
+  }
+  // losses: aux = mean over groups of E * sum_e f_e P_e (f_e = routed_e / (Sg k),
+  // P_e = psum_e / Sg); z = mean over tokens of logsumexp^2. Fixed-order sums.
+  float ga = 0.f, gzs = 0.f;
+  for (int gg = tid; gg < G; gg += kScanThreads) {
+    float tsum = 0.f;
+    for (int xx = 0; xx < X; ++xx) tsum += __ldcg(a.gaux + size_t(gg) * X + xx);
+    ga += float(double(tsum) * double(E) / (double(a.Sg) * a.k * double(a.Sg)));
+    gzs += __ldcg(a.gz + gg);
+  }
+  ga = block_sum(ga, s_red);
+  gzs = block_sum(gzs, s_red);
+  if (tid == 0) {
+    *a.aux = ga / float(G);
+    *a.z = gzs / float(a.S);
+    *a.done = 0u;
   }
 }
 
@@ -759,8 +852,16 @@ int launch_topk(const RouteArgs& a, int n_chunks, cudaStream_t st) {
 
 template <int K, int TPT>
 int launch_router_topk_t(const CUtensorMap& tx, const CUtensorMap& tw, const RouteArgs& a,
-                         const FusedRouterArgs& f, int n_chunks, cudaStream_t st) {
-  const size_t ring = size_t(f.stages) * (128 * 64 * 2 + size_t(f.BN) * 64 * 2);
+                         FusedRouterArgs f, int n_chunks, cudaStream_t st) {
+  // ring of (x, W_g) stages: with more chunks than SMs and <= 512 threads a CTA, two CTAs
+  // share an SM (about 96 KB each), else one CTA takes about 192 KB
+  const int stage_bytes = 128 * 64 * 2 + f.BN * 64 * 2;
+  const bool two = n_chunks > num_sms() && kThreads * TPT <= 512;
+  int stages = (two ? 96 * 1024 : 192 * 1024) / stage_bytes;
+  stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+  if (stages > f.Mdim / 64) stages = f.Mdim / 64;
+  f.stages = stages;
+  const size_t ring = size_t(f.stages) * stage_bytes;
   const size_t stage_log = size_t(kThreads) * (a.E + TPT) * sizeof(float);
   const size_t smem = (ring > stage_log ? ring : stage_log) + 1024;
   MOE_CUDA_CHECK(cudaFuncSetAttribute(router_topk_kernel<K, TPT>,
@@ -805,7 +906,16 @@ RouteArgs route_args(const moe_config_t& c, int C, const float* logits, const fl
 
 // the two launches after the per-chunk kernel
 int launch_scan_finalize(const moe_config_t& c, const RouteArgs& a, cudaStream_t st) {
-  int rc = launch_kernel(route_scan_kernel, dim3(c.G), dim3(kScanThreads), 0, st, a);
+  // experts per scan CTA: about 2048 values of a group per CTA, at most kScanThreads columns
+  const int64_t vals = int64_t(a.n_cpg) * (int64_t(c.k) * c.E + 2 * c.E + 1);
+  int X = int((vals + 2047) / 2048);
+  if (X > c.E) X = c.E;
+  if (X < 1) X = 1;
+  int ew = (c.E + X - 1) / X;
+  if (ew > kScanThreads / c.k) ew = kScanThreads / c.k;
+  X = (c.E + ew - 1) / ew;
+  int rc = launch_kernel(route_scan_kernel, dim3(unsigned(c.G * X)), dim3(kScanThreads), 0, st, a, X,
+                         ew);
   if (rc != MOE_OK) return rc;
   const int64_t n = int64_t(c.S) * c.k;
   return launch_kernel(route_finalize_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, st, a);
@@ -841,13 +951,7 @@ int launch_router_route(const moe_config_t& c, int C, const void* x, const void*
   f.Mdim = c.M;
   f.BN = gemm_bn(c.E, EPI_F32_BIAS);
   if (f.BN == 0 || c.M % 64 != 0 || c.M <= 0) return MOE_ERR_UNSUPPORTED;
-  // one CTA per SM (up to 1024 threads at <= 64 registers): the ring takes ~192 KB
-  const int stage_bytes = 128 * 64 * 2 + f.BN * 64 * 2;
-  int stages = (192 * 1024) / stage_bytes;
-  stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
-  const int kblocks = c.M / 64;
-  if (stages > kblocks) stages = kblocks;
-  f.stages = stages;
+  f.stages = 0;  // set per launch shape
   CUtensorMap tx, tw;
   int rc = make_tma_map_rows(&tx, x, c.S, c.M, 128);
   if (rc != MOE_OK) return rc;
