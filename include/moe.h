@@ -223,11 +223,10 @@ int moe_route(const moe_config_t* cfg, const float* logits, const float* u,
  *         and routes from them without writing them to memory (unless logits_out is
  *         given), then moe_route's scan and finalize kernels run. logits_out may be NULL.
  *   fp32: moe_router into logits_out, then moe_route; logits_out must be non-null.
- * The routing outputs are what moe_route computes from the logits this call forms (and
- * stores in logits_out when non-null), bit for bit. Those logits are moe_router's up to
- * fp32 summation order: each 128-token chunk adds its 64-wide blocks of the model
- * dimension starting at a chunk-dependent block. Passing logits_out or not changes no
- * other output. ws: MOE_WS_STEP bytes. Errors: as moe_router and moe_route.
+ * The logits equal moe_router's bit for bit, and every output equals what moe_route
+ * computes from them, bit for bit, except that with E <= 16 aux_loss and z_loss may differ
+ * in the last bits (the softmax sums are split over more threads). Passing logits_out or
+ * not changes no other output. ws: MOE_WS_STEP bytes. Errors: as moe_router and moe_route.
  */
 int moe_router_route(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
                      const float* u, float* logits_out, const moe_route_out_t* out, void* ws,

@@ -128,8 +128,8 @@ def test_router_route_without_logits_out(run):
 
 def test_unfused_router_then_route(run):
     """The two separate steps (moe_router, then moe_route from the stored logits): logits
-    within tolerance of the oracle's and of the fused kernel's, routing bit-exact against the
-    oracle routed from them."""
+    within tolerance of the oracle's and bit-identical to the fused kernel's, routing
+    bit-exact against the oracle routed from them and equal to the fused call's."""
     cfg, d, a = run["cfg"], run["dev"], run["inp"].np
     ws = moe.workspace(cfg, N.MOE_WS_STEP, "cuda")
     out = moe.RouteOutputs.allocate(cfg, "cuda")
@@ -140,8 +140,9 @@ def test_unfused_router_then_route(run):
     lg = to_np(logits)
     assert_close(lg, O.router_logits(a["x"], a["W_g"], a.get("bias")), LOGIT_RTOL[cfg["dtype"]],
                  "logits")
-    assert_close(lg, run["logits"], LOGIT_RTOL[cfg["dtype"]], "logits vs fused")
+    assert np.array_equal(lg, run["logits"]), "logits differ from the fused kernel's"
     compare_route(route_np(out), O.route(lg, oracle_cfg(cfg), a["u"]), run["name"])
+    _same_route(route_np(out), run["route"], run["name"])
 
 
 def test_layer_without_logits_equals_with(run):

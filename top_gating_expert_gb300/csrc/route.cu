@@ -105,12 +105,13 @@ __device__ __forceinline__ float token_u(const RouteArgs& a, int t0, int nt) {
 // The per-chunk routing work on a chunk's logits staged in shared memory (s_log: nt rows of
 // E logits, row stride ld = E + TPT). TPT threads per token (consecutive lanes), each owning
 // experts sub, sub + TPT, ...; the CTA has kThreads * TPT threads, all of which call this.
-// Non-finite logits are replaced by -inf in s_log (and flagged).
+// Non-finite logits count as -inf (and are flagged); each staged logit is overwritten by
+// exp(logit - max of its token).
 template <int K, int TPT>
 __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int c, int t0, int nt,
                                            float u_tok) {
   constexpr int kT = kThreads * TPT;
-  __shared__ float s_m[kThreads], s_inv[kThreads], s_pp[kT];
+  __shared__ float s_inv[kThreads], s_pp[kT];
   __shared__ uint8_t s_id[kThreads * kMaxK];
   __shared__ uint8_t s_cand[kThreads];
   __shared__ int s_wc[kWarps][kMaxE];
@@ -201,15 +202,20 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
 #pragma unroll
     for (int off = TPT >> 1; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(tmask, m, off, TPT));
     if (m == -INFINITY) m = 0.f;  // only when every logit was non-finite (already flagged)
+    // sum of exp(l - m); each exp(l - m) replaces its logit in the row (the probability
+    // sums below reuse it; the top-k logits are held in registers)
     float s = 0.f;
     if (tok)
-      for (int e = sub; e < E; e += TPT) s += expf(rowp[e] - m);
+      for (int e = sub; e < E; e += TPT) {
+        const float v = expf(rowp[e] - m);
+        rowp[e] = v;
+        s += v;
+      }
 #pragma unroll
     for (int off = TPT >> 1; off > 0; off >>= 1) s += __shfl_xor_sync(tmask, s, off, TPT);
 
     if (tok && sub == 0) {
       const int t = t0 + i;
-      s_m[i] = m;
       s_inv[i] = s > 0.f ? 1.f / s : 0.f;
       const float lse = m + logf(s);
       zacc = lse * lse;
@@ -251,7 +257,7 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
       const int e = x / tpe, sb = x % tpe;
       float acc = 0.f;
       if (e < E)
-        for (int t = sb; t < nt; t += tpe) acc += expf(s_log[t * ld + e] - s_m[t]) * s_inv[t];
+        for (int t = sb; t < nt; t += tpe) acc += s_log[t * ld + e] * s_inv[t];
       s_pp[tid] = acc;
       __syncthreads();
       if (e < E && sb == 0) {
@@ -344,11 +350,10 @@ __global__ void __launch_bounds__(kThreads * TPT) route_topk_kernel(RouteArgs a)
 // reads TMEM lanes 32 (w % 4) ..) and add the bias into padded shared memory laid out as
 // route_topk_kernel stages it (over the drained stage ring), optionally storing the logits
 // to memory too; then the whole CTA runs topk_chunk. The logits never round-trip through
-// HBM. Each chunk starts its K loop at its own k-block (rotated by the chunk index) so that
-// the CTAs do not all read the same W_g lines from L2 at the same time; the fp32 logits
-// are then summed in a chunk-dependent order of 64-wide blocks (within fp32 rounding of
-// any other order). Lec16 Systems for MoE Models, "MoE Kernel 优化": the gating function
-// as one fused kernel instead of one per step.
+// HBM. The MMA sequence (64-wide k-blocks in order, four K = 16 steps each) and the bias
+// addition are those of the router GEMM, so the logits equal moe_router's bit for bit.
+// Lec16 Systems for MoE Models, "MoE Kernel 优化": the gating function as one fused kernel
+// instead of one per step.
 struct FusedRouterArgs {
   const float* bias;   // per-expert logit offset, nullable
   float* logits_out;   // [S, E] fp32, nullable
@@ -385,7 +390,6 @@ __global__ void __launch_bounds__(kThreads * TPT, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E, ld = E + TPT;
   const int kblocks = f.Mdim / 64;
-  const int rot = c % kblocks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -416,8 +420,7 @@ __global__ void __launch_bounds__(kThreads * TPT, 1)
       ok = __all_sync(0xffffffffu, wait_bounded(empty0 + 8 * stage, phase ^ 1u, &s_abort, a.status));
       if (!ok) break;
       if (lane == 0) {
-        int kb = j + rot;
-        if (kb >= kblocks) kb -= kblocks;
+        const int kb = j;
         const uint32_t fb = full0 + 8 * stage;
         mbar_expect_tx(fb, A_BYTES + B_BYTES);
         tma_load_2d(smem_u32(sA + stage * A_BYTES), &tmX, kb * 64, t0, fb);
@@ -483,9 +486,16 @@ __global__ void __launch_bounds__(kThreads * TPT, 1)
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj)
           l[jj] = __uint_as_float(v[jj]) + ((f.bias && c0 + jj < E) ? f.bias[c0 + jj] : 0.f);
+        if ((ld & 3) == 0 && c0 + 16 <= E) {  // 16-byte stores (rows are 16-byte aligned)
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj)
-          if (c0 + jj < E) row[c0 + jj] = l[jj];
+          for (int jj = 0; jj < 4; ++jj)
+            reinterpret_cast<float4*>(row + c0)[jj] =
+                make_float4(l[4 * jj], l[4 * jj + 1], l[4 * jj + 2], l[4 * jj + 3]);
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            if (c0 + jj < E) row[c0 + jj] = l[jj];
+        }
         if (store) {
           if ((E & 3) == 0 && c0 + 16 <= E) {
 #pragma unroll
