@@ -44,6 +44,20 @@ Readings where the pages are silent or garbled (each is repeated in the design n
   R10 SwiGLU uses Swish = SiLU (beta = 1): (silu(x W_in^T) * (x W_up^T)) W_out^T.
   R11 the layer returns the expert output; with a residual given, y = residual + that.
   R12 the garbled GShard output formula is read as y = sum_i G(x)_i E_i(x) (Lec16).
+  R16 group-limited top-k (Lec16 "DeepSeek V3 MoE": 256 experts in 8 groups, 4 groups
+      kept): the experts form n_groups contiguous groups of E/n_groups; a group's score
+      is its largest logit (the page does not say; the max is monotone in the softmax
+      score); each token keeps the topk_groups best groups (ties to the lower group)
+      and takes its top-k among their experts. Softmax, logsumexp and the losses still
+      run over all E experts.
+  R17 gate normalisation (MegaBlocks §2 "权重归一化": optional p-norm of the top-k
+      weights; Lec16 "DeepSeek V3 MoE": TopK(Softmax(h W), 8)): "softmax_topk" (the
+      default) renormalises the k selected probabilities to sum 1 (the p = 1 norm);
+      "none" keeps the k full-softmax probabilities as they are; "pnorm" divides them
+      by their p-norm.
+  R18 uniform assignment (MegaBlocks §2 benchmark switch): the k expert ids of token t
+      become (t*k + j) mod E; the gates stay those of the router's own top-k; random
+      routing is not combined with it. Counts and the aux loss follow the new ids.
 
 Parity status: every function below is pinned by tests that do not re-type it
 (brute force on tiny inputs, closed forms, invariants, library routines, hand-worked
@@ -122,6 +136,45 @@ def top_k_gates(logits, ids) -> np.ndarray:
     sel = np.take_along_axis(_f64(logits), ids, axis=1)
     z = np.exp(sel - sel[:, :1])
     return z / z.sum(axis=1, keepdims=True)
+
+
+def group_limited_top_k(logits, k: int, n_groups: int, topk_groups: int) -> np.ndarray:
+    """[Lec16] "DeepSeek V3 MoE" group-limited routing (reading R16): keep each token's
+    topk_groups groups of largest best logit (stable: lower group first on ties), then
+    the k largest logits among the experts of those groups (reading R6 order)."""
+    l = _f64(logits)
+    if not np.all(np.isfinite(l)):
+        raise ValueError("non-finite router logits")
+    S, E = l.shape
+    if E % n_groups or k > topk_groups * (E // n_groups):
+        raise ValueError("groups must divide E and hold at least k experts")
+    size = E // n_groups
+    best = l.reshape(S, n_groups, size).max(axis=2)
+    kept_groups = np.argsort(-best, axis=1, kind="stable")[:, :topk_groups]
+    allowed = np.zeros((S, n_groups), dtype=bool)
+    np.put_along_axis(allowed, kept_groups, True, axis=1)
+    masked = np.where(np.repeat(allowed, size, axis=1), l, -np.inf)
+    return np.argsort(-masked, axis=1, kind="stable")[:, :k].astype(np.int64)
+
+
+def normalised_gates(logits, ids, norm: str = "softmax_topk", p: float = 1.0) -> np.ndarray:
+    """Gates of the selected experts under the three normalisations of reading R17."""
+    if norm == "softmax_topk":
+        return top_k_gates(logits, ids)
+    probs, _ = log_softmax_parts(logits)
+    sel = np.take_along_axis(probs, ids, axis=1)
+    if norm == "none":
+        return sel
+    if norm == "pnorm":
+        if not p > 0:
+            raise ValueError("p must be positive")
+        return sel / np.power(np.sum(np.power(sel, p), axis=1, keepdims=True), 1.0 / p)
+    raise ValueError(f"unknown gate normalisation {norm!r}")
+
+
+def uniform_ids(S: int, E: int, k: int) -> np.ndarray:
+    """Reading R18: token t's j-th expert is (t*k + j) mod E."""
+    return (np.arange(S, dtype=np.int64)[:, None] * k + np.arange(k, dtype=np.int64)[None, :]) % E
 
 
 # ---------------------------------------------------------------------------------------
@@ -248,13 +301,21 @@ def route(logits, cfg: dict, u=None) -> dict:
     logits = _f64(logits)
     assert logits.shape == (S, E)
     C = capacity(S, G, E, k, cfg["capacity_factor"])
-    ids = top_k(logits, k)
-    gates = top_k_gates(logits, ids)
+    ng = int(cfg.get("n_expert_groups", 0) or 0)
+    if ng > 1:
+        ids = group_limited_top_k(logits, k, ng, int(cfg["topk_groups"]))
+    else:
+        ids = top_k(logits, k)
+    gates = normalised_gates(logits, ids, cfg.get("gate_norm", "softmax_topk"),
+                             float(cfg.get("gate_p", 1.0)))
     candidate = np.ones((S, k), dtype=bool)
     if cfg.get("random_routing", 0):
-        if k != 2 or u is None:
-            raise ValueError("random routing needs k == 2 and a uniform draw per token")
+        if k != 2 or u is None or cfg.get("uniform_assignment", 0):
+            raise ValueError("random routing needs k == 2, a uniform draw per token and "
+                             "no uniform assignment")
         candidate[:, 1] = random_routing_keep(logits, ids, u)
+    if cfg.get("uniform_assignment", 0):
+        ids = uniform_ids(S, E, k)
     pos, reason, counts = assign_slots(ids, candidate, G, E, C)
     Sg = S // G
     counts_routed = np.zeros((G, E), dtype=np.int64)

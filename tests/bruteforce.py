@@ -21,25 +21,61 @@ def bf_capacity(S, G, E, k, cf):
     return c
 
 
+def bf_group_limited(row, k, n_groups, topk_groups):
+    """Exhaustive search: the groups are ranked by their best logit (lower group first on
+    ties) and the best topk_groups kept; among every k-subset of their experts the one
+    whose members, listed by (logit desc, index asc), compare largest wins."""
+    import itertools
+    E = len(row)
+    size = E // n_groups
+    best = [max(row[g * size:(g + 1) * size]) for g in range(n_groups)]
+    groups = sorted(range(n_groups), key=lambda g: (-best[g], g))[:topk_groups]
+    allowed = [e for e in range(E) if e // size in groups]
+    winner, win_key = None, None
+    for sub in itertools.combinations(allowed, k):
+        listed = sorted(sub, key=lambda e: (-row[e], e))
+        key = [(-row[e], e) for e in listed]
+        if win_key is None or key < win_key:
+            winner, win_key = listed, key
+    return winner
+
+
 def bf_route(logits, cfg, u=None):
     """logits: list of S lists of E floats. Returns a dict of plain lists."""
     S, G, E, k = cfg["S"], cfg["G"], cfg["E"], cfg["k"]
     Sg = S // G
     C = bf_capacity(S, G, E, k, cfg["capacity_factor"])
     ids, gates, cand = [], [], []
+    ng = int(cfg.get("n_expert_groups", 0) or 0)
+    norm = cfg.get("gate_norm", "softmax_topk")
     for t in range(S):
-        order = sorted(range(E), key=lambda e: (-logits[t][e], e))[:k]
+        if ng > 1:
+            order = bf_group_limited(logits[t], k, ng, int(cfg["topk_groups"]))
+        else:
+            order = sorted(range(E), key=lambda e: (-logits[t][e], e))[:k]
         ids.append(order)
         top = logits[t][order[0]]
-        w = [math.exp(logits[t][e] - top) for e in order]
-        tot = sum(w)
-        gates.append([wi / tot for wi in w])
+        if norm == "softmax_topk":
+            w = [math.exp(logits[t][e] - top) for e in order]
+            tot = sum(w)
+            gates.append([wi / tot for wi in w])
+        else:
+            mx = max(logits[t])
+            den = sum(math.exp(v - mx) for v in logits[t])
+            pr = [math.exp(logits[t][e] - mx) / den for e in order]
+            if norm == "pnorm":
+                p = float(cfg["gate_p"])
+                nrm = sum(v ** p for v in pr) ** (1.0 / p)
+                pr = [v / nrm for v in pr]
+            gates.append(pr)
         c = [True] * k
         if cfg.get("random_routing", 0):
             l1, l2 = logits[t][order[0]], logits[t][order[1]]
             g2 = math.exp(l2) / (math.exp(l1) + math.exp(l2))
             c[1] = float(u[t]) < min(1.0, 2.0 * g2)
         cand.append(c)
+    if cfg.get("uniform_assignment", 0):
+        ids = [[(t * k + j) % E for j in range(k)] for t in range(S)]
     pos = [[-1] * k for _ in range(S)]
     reason = [[0] * k for _ in range(S)]
     counts = [[0] * E for _ in range(G)]
