@@ -65,6 +65,9 @@ enum {
   MOE_ERR_DEVICE_DATA = -7  /* device: an index or offset read on the device was invalid */
 };
 
+/* gate normalisations (moe_config_t.gate_norm) */
+enum { MOE_GATE_SOFTMAX_TOPK = 0, MOE_GATE_NONE = 1, MOE_GATE_PNORM = 2 };
+
 /* drop_reason values */
 enum { MOE_KEPT = 0, MOE_DROP_CAPACITY = 1, MOE_DROP_RANDOM = 2 };
 
@@ -85,6 +88,20 @@ enum { MOE_WS_STEP = 0, MOE_WS_LAYER = 1 };
  *   bf16: M % 64 == 0, H % 64 == 0 (H % 128 == 0 for SwiGLU), n_shared*H_shared likewise.
  *   f32 (the plain-FMA path, meant for small layers): M % 4 == 0, H % 4 == 0 (H % 128 == 0
  *     for SwiGLU), H_shared % 4 == 0.
+ * Routing variants (a zero-filled tail gives the default routing above):
+ *   gate_norm: MOE_GATE_SOFTMAX_TOPK (softmax over the k selected logits), MOE_GATE_NONE
+ *     (the k full-softmax probabilities as they are: Lec16 "DeepSeek V3 MoE",
+ *     TopK(Softmax(h W), 8)) or MOE_GATE_PNORM (those probabilities divided by their
+ *     gate_p-norm; gate_p > 0, finite: MegaBlocks router §2). The random-routing
+ *     decision always uses the softmax over the two selected logits.
+ *   n_expert_groups: 0 or 1 = off; else 2..16 dividing E: the experts form that many
+ *     contiguous groups, each token keeps the topk_groups (1..n_expert_groups) groups
+ *     of largest best logit (ties to the lower group) and takes its top-k among their
+ *     experts; k <= topk_groups * E / n_expert_groups (Lec16 "DeepSeek V3 MoE": 8
+ *     groups, 4 kept).
+ *   uniform_assignment: 0/1; 1 replaces token t's expert ids by (t*k + j) mod E and keeps
+ *     the router's gates (MegaBlocks router §2 benchmark switch); not with
+ *     random_routing.
  */
 typedef struct {
   int32_t S, G, E, M, H, k;
@@ -93,6 +110,10 @@ typedef struct {
   int32_t n_shared, H_shared;
   int32_t act;   /* MOE_ACT_* */
   int32_t dtype; /* MOE_F32 / MOE_BF16 */
+  int32_t gate_norm;  /* MOE_GATE_* */
+  float gate_p;
+  int32_t n_expert_groups, topk_groups;
+  int32_t uniform_assignment;
 } moe_config_t;
 
 /*
@@ -100,7 +121,8 @@ typedef struct {
  *   expert_id   int32 [S, k]  chosen experts, largest logit first; equal logits rank
  *                             the lower expert index first.
  *   gate        float [S, k]  Softmax over the k selected logits (= the full softmax's
- *                             top-k probabilities renormalised); 0 where not kept.
+ *                             top-k probabilities renormalised), or as gate_norm says;
+ *                             0 where not kept.
  *   pos         int32 [S, k]  slot in the (group, expert) queue, -1 when not kept.
  *                             Queue order: all 1st choices of the group in token order,
  *                             then all 2nd choices, ...; random-skipped choices take no slot.
@@ -138,7 +160,8 @@ typedef struct {
 /* Human-readable name of a status code (static storage). */
 const char* moe_status_string(int status);
 
-/* ABI version of this library (major * 100 + minor). */
+/* ABI version of this library (major * 100 + minor): 101 (moe_config_t with the routing
+ * variant fields). */
 int moe_abi_version(void);
 
 /* MOE_OK if the configuration is valid and built, else the reason. Host only. */

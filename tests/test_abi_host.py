@@ -22,7 +22,7 @@ def test_exports_every_declared_symbol(native_lib):
 def test_status_strings(native_lib):
     for code, name in N.STATUS_NAMES.items():
         assert native_lib.moe_status_string(code).decode().startswith(name)
-    assert native_lib.moe_abi_version() == 100
+    assert native_lib.moe_abi_version() == 101
 
 
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
@@ -58,6 +58,13 @@ BAD = [
     dict(k=3, random_routing=1),  # random routing needs k == 2
     dict(random_routing=2),
     dict(n_shared=1, H_shared=0),
+    dict(gate_norm="pnorm", gate_p=0.0), dict(gate_norm="pnorm", gate_p=float("inf")),
+    dict(n_expert_groups=3),                        # does not divide E = 128
+    dict(n_expert_groups=32, topk_groups=4),        # more than 16 groups
+    dict(n_expert_groups=8, topk_groups=0), dict(n_expert_groups=8, topk_groups=9),
+    dict(E=16, n_expert_groups=8, topk_groups=1, k=3, random_routing=0),  # 1 group of 2 < k
+    dict(uniform_assignment=1),                     # preset 2 has random routing
+    dict(uniform_assignment=2, random_routing=0),
 ]
 
 
@@ -66,6 +73,14 @@ def test_invalid_configs_rejected(native_lib, over):
     from top_gating_expert_gb300 import moe
     cfg = preset(2, **over)
     assert moe.validate(cfg) == -1
+
+
+def test_valid_variant_configs(native_lib):
+    from top_gating_expert_gb300 import moe
+    for over in (dict(gate_norm="none"), dict(gate_norm="pnorm", gate_p=2.0),
+                 dict(n_expert_groups=8, topk_groups=4), dict(n_expert_groups=16, topk_groups=1),
+                 dict(uniform_assignment=1, random_routing=0)):
+        assert moe.validate(preset(2, **over)) == 0, over
 
 
 @pytest.mark.parametrize("over", [dict(M=1000), dict(H=4000), dict(act="swiglu", H=4160)])

@@ -13,6 +13,7 @@ c_int32, c_int64, c_float, c_size_t, c_void_p = (ctypes.c_int32, ctypes.c_int64,
 
 MOE_F32, MOE_BF16 = 0, 1
 MOE_ACT_RELU, MOE_ACT_SWIGLU = 0, 1
+GATE_NORMS = {"softmax_topk": 0, "none": 1, "pnorm": 2}
 MOE_WS_STEP, MOE_WS_LAYER = 0, 1
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
@@ -23,7 +24,9 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED
 class MoeConfig(ctypes.Structure):
     _fields_ = [("S", c_int32), ("G", c_int32), ("E", c_int32), ("M", c_int32), ("H", c_int32),
                 ("k", c_int32), ("capacity_factor", c_float), ("random_routing", c_int32),
-                ("n_shared", c_int32), ("H_shared", c_int32), ("act", c_int32), ("dtype", c_int32)]
+                ("n_shared", c_int32), ("H_shared", c_int32), ("act", c_int32), ("dtype", c_int32),
+                ("gate_norm", c_int32), ("gate_p", c_float), ("n_expert_groups", c_int32),
+                ("topk_groups", c_int32), ("uniform_assignment", c_int32)]
 
 
 ROUTE_FIELDS = ("expert_id", "gate", "pos", "drop_reason", "row", "counts", "counts_routed",

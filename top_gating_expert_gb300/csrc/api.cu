@@ -37,6 +37,17 @@ int validate(const moe_config_t* c) {
   if (c->random_routing && c->k != 2) return MOE_ERR_INVALID_ARG;
   if (!isfinite(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
   if (c->n_shared < 0 || (c->n_shared > 0 && c->H_shared < 1)) return MOE_ERR_INVALID_ARG;
+  if (c->gate_norm < MOE_GATE_SOFTMAX_TOPK || c->gate_norm > MOE_GATE_PNORM) return MOE_ERR_INVALID_ARG;
+  if (c->gate_norm == MOE_GATE_PNORM && !(isfinite(c->gate_p) && c->gate_p > 0.f))
+    return MOE_ERR_INVALID_ARG;
+  if (c->n_expert_groups < 0 || c->n_expert_groups > 16) return MOE_ERR_INVALID_ARG;
+  if (c->n_expert_groups > 1) {
+    if (c->E % c->n_expert_groups) return MOE_ERR_INVALID_ARG;
+    if (c->topk_groups < 1 || c->topk_groups > c->n_expert_groups) return MOE_ERR_INVALID_ARG;
+    if (c->k > c->topk_groups * (c->E / c->n_expert_groups)) return MOE_ERR_INVALID_ARG;
+  }
+  if (c->uniform_assignment != 0 && c->uniform_assignment != 1) return MOE_ERR_INVALID_ARG;
+  if (c->uniform_assignment && c->random_routing) return MOE_ERR_INVALID_ARG;
   if (int64_t(c->S) * c->k > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
   const int64_t Hs = int64_t(c->n_shared) * c->H_shared;
   const bool swiglu = c->act == MOE_ACT_SWIGLU;
@@ -160,7 +171,7 @@ const char* moe_status_string(int status) {
   return "unknown status";
 }
 
-int moe_abi_version(void) { return 100; }
+int moe_abi_version(void) { return 101; }
 
 int moe_validate_config(const moe_config_t* cfg) {
   Prep p;

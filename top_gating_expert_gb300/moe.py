@@ -35,7 +35,12 @@ def make_config(cfg: dict) -> N.MoeConfig:
         random_routing=int(cfg.get("random_routing", 0)),
         n_shared=int(cfg.get("n_shared", 0)), H_shared=int(cfg.get("H_shared", 0)),
         act=N.MOE_ACT_SWIGLU if cfg["act"] == "swiglu" else N.MOE_ACT_RELU,
-        dtype=N.MOE_BF16 if cfg["dtype"] == "bf16" else N.MOE_F32)
+        dtype=N.MOE_BF16 if cfg["dtype"] == "bf16" else N.MOE_F32,
+        gate_norm=N.GATE_NORMS[cfg.get("gate_norm", "softmax_topk")],
+        gate_p=float(cfg.get("gate_p", 1.0)),
+        n_expert_groups=int(cfg.get("n_expert_groups", 0) or 0),
+        topk_groups=int(cfg.get("topk_groups", 0) or 0),
+        uniform_assignment=int(cfg.get("uniform_assignment", 0)))
 
 
 def _cfg(c) -> N.MoeConfig:
