@@ -159,10 +159,12 @@ def traffic_for(kernel: str, config: int):
             # | kernel | config | dram bytes per launch | source sha1 |
             try:
                 sha = cells[3]
-                src = os.path.join(ROOT, "top_gating_expert_gb300", "csrc", cells[4])
-                with open(src, "rb") as f:
-                    if hashlib.sha1(f.read()).hexdigest()[:12] != sha:
-                        return None
+                h = hashlib.sha1()
+                for name in cells[4].split("+"):  # the kernel's source files, in order
+                    with open(os.path.join(ROOT, "top_gating_expert_gb300", "csrc", name.strip()), "rb") as f:
+                        h.update(f.read())
+                if h.hexdigest()[:12] != sha:
+                    return None
                 return float(cells[2])
             except Exception:
                 return None
