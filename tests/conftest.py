@@ -17,9 +17,8 @@ def pytest_configure(config):
 
 @pytest.fixture(scope="session")
 def native_lib():
-    """The C-ABI library, built in-tree first if it is missing."""
+    """The C-ABI library, (re)built in-tree first if it is missing or older than a source."""
     from top_gating_expert_gb300 import build as b
-    if not os.path.exists(b.library_path()):
-        b.build_library()
+    b.build_library()
     from top_gating_expert_gb300 import _native
     return _native.lib()
