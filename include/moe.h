@@ -72,7 +72,7 @@ enum { MOE_GATE_SOFTMAX_TOPK = 0, MOE_GATE_NONE = 1, MOE_GATE_PNORM = 2 };
 enum { MOE_KEPT = 0, MOE_DROP_CAPACITY = 1, MOE_DROP_RANDOM = 2 };
 
 /* workspace kinds for moe_workspace_bytes */
-enum { MOE_WS_STEP = 0, MOE_WS_LAYER = 1 };
+enum { MOE_WS_STEP = 0, MOE_WS_LAYER = 1, MOE_WS_BACKWARD = 2 };
 
 /*
  * Layer configuration. Parameter names follow the pages' problem statement: S tokens,
@@ -175,7 +175,8 @@ int moe_rows_max(const moe_config_t* cfg, int64_t* R_max);
 
 /*
  * Workspace bytes. MOE_WS_STEP: what moe_router, moe_route, moe_expert_* and
- * moe_shared_ffn need (status word + routing scratch). MOE_WS_LAYER: what
+ * moe_shared_ffn need (status word + routing scratch). MOE_WS_BACKWARD: what
+ * moe_layer_backward needs. MOE_WS_LAYER: what
  * moe_layer_forward needs (the step workspace plus logits, x_perm, h, y_perm and the
  * shared-expert buffers). Workspaces must be 256-byte aligned and zero-filled once
  * before first use (the status word lives in their first bytes).
@@ -334,6 +335,67 @@ int moe_layer_forward(const moe_config_t* cfg, const void* x, const void* W_g, c
                       const void* Ws_out_packed, const float* u, const void* residual, void* y,
                       float* logits_out, const moe_route_out_t* r, void* ws, size_t ws_bytes,
                       moe_stream_t stream);
+
+/* ---------------------------------------------------------------- the backward pass */
+
+/*
+ * Transposed weights for the backward's data-gradient GEMMs, packed tile-major like the
+ * forward's (element counts as moe_packed_sizes' w_in / w_out):
+ *   Wt_out_packed  logical [E, H, M]: W_out[e] transposed (gradient through GEMM 2);
+ *   Wt_in_packed   logical [E, M, H] (ReLU) or [E, M, 2H] (SwiGLU, the K order of the forward's
+ *                  interleaved pack): W_in[e] (and W_up[e]) transposed.
+ * bf16 only.
+ */
+int moe_pack_weights_backward(const moe_config_t* cfg, const void* W_in, const void* W_up,
+                              const void* W_out, void* Wt_in_packed, void* Wt_out_packed,
+                              moe_stream_t stream);
+
+/* The same for the shared experts, with their hidden units side by side (counts as
+ * moe_packed_sizes' ws_in / ws_out). */
+int moe_pack_shared_weights_backward(const moe_config_t* cfg, const void* Ws_in, const void* Ws_up,
+                                     const void* Ws_out, void* Wst_in_packed, void* Wst_out_packed,
+                                     moe_stream_t stream);
+
+/* Gradients written by moe_layer_backward (device pointers; fp32 weights' gradients). */
+typedef struct {
+  void* dx;       /* [S, M] in the layer's element type                                   */
+  float* dW_g;    /* [E, M]                                                                */
+  float* dbias;   /* [E], nullable (the gradient of a per-expert logit offset)            */
+  float* dW_in;   /* [E, H, M]                                                             */
+  float* dW_up;   /* [E, H, M] (SwiGLU), else NULL                                         */
+  float* dW_out;  /* [E, M, H]                                                             */
+  float* dWs_in;  /* [n_shared * H_shared, M] (shared experts side by side), or NULL       */
+  float* dWs_up;  /* [n_shared * H_shared, M] (SwiGLU), or NULL                            */
+  float* dWs_out; /* [M, n_shared * H_shared], or NULL                                     */
+} moe_grads_t;
+
+/*
+ * The backward pass of moe_layer_forward: the gradients of
+ *     L = sum(dy * y) + aux_coef * aux_loss + z_coef * z_loss
+ * (dy [S, M] the upstream gradient of y; MegaBlocks router §3: the load-balancing loss
+ * reaches the router only through the expert scores, its counts being constants; §2:
+ * z-loss) with the routing decisions held fixed. A dropped assignment gives its gate no
+ * gradient. Gates: MOE_GATE_SOFTMAX_TOPK or MOE_GATE_NONE (others: MOE_ERR_UNSUPPORTED), no
+ * uniform assignment; bf16 only.
+ * Inputs from the forward: logits (the forward's logits_out, [S, E]), r (its routing
+ * outputs) and fwd_ws (the MOE_WS_LAYER workspace of that moe_layer_forward call,
+ * unchanged since: it holds x_perm, h and the shared experts' h). residual: 1 if the
+ * forward had a residual (dx then includes dy). Packs: W_in_packed / Ws_in_packed from
+ * the forward pack calls (the SwiGLU pre-activations are recomputed), the transposed packs
+ * from moe_pack_weights_backward / moe_pack_shared_weights_backward (shared ones NULL
+ * without shared experts). ws: MOE_WS_BACKWARD bytes (its own status word).
+ * Every step runs on the GPU: gather of dy, GEMM 2's data gradient with the gate's
+ * gradient, the SwiGLU derivative, GEMM 1's data gradient (tcgen05); the weights'
+ * gradients as K-ragged tcgen05 GEMMs over per-expert 64-padded transposed rows; the
+ * router's gradient (dlogits, then dx, dW_g, dbias); dx summed in fp32 and rounded once.
+ */
+int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, const void* W_g,
+                       const void* W_in_packed, const void* Wt_in_packed, const void* Wt_out_packed,
+                       const void* Ws_in_packed, const void* Wst_in_packed,
+                       const void* Wst_out_packed, const float* logits, const moe_route_out_t* r,
+                       const void* fwd_ws, size_t fwd_ws_bytes, int residual, float aux_coef,
+                       float z_coef, const moe_grads_t* grads, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
 
 /*
  * Synchronises `stream`, reads the status word in ws, clears it, and returns MOE_OK or

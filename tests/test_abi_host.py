@@ -123,3 +123,34 @@ def test_compute_entry_points_check_arguments_on_host(native_lib):
     assert L.moe_get_device_status(None, None) == -1
     # shared-expert calls need shared experts
     assert L.moe_shared_ffn(ctypes.byref(c), fake, fake, fake, fake, fake, fake, need, None) == -1
+
+
+def test_backward_host_checks(native_lib):
+    """The backward's workspace kind and its argument checks, before any launch."""
+    from top_gating_expert_gb300 import moe
+    L = native_lib
+    c = moe.make_config(CONFIGS[2])
+    step = moe.workspace_bytes(c, N.MOE_WS_STEP)
+    bwd = moe.workspace_bytes(c, N.MOE_WS_BACKWARD)
+    assert bwd > step
+    fake = ctypes.c_void_p(1 << 20)
+    out = N.MoeRouteOut(**{f: (1 << 20) for f in N.ROUTE_FIELDS})
+    g = N.MoeGrads(**{f: (1 << 20) for f in N.GRAD_FIELDS})
+    lay = moe.workspace_bytes(c, N.MOE_WS_LAYER)
+    args = lambda **kw: [kw.get(n, v) for n, v in (
+        ("x", fake), ("dy", fake), ("W_g", fake), ("W_in_p", fake), ("Wt_in", fake), ("Wt_out", fake),
+        ("Ws_in", None), ("Wst_in", None), ("Wst_out", None), ("logits", fake))]
+    tail = lambda fwd=fake, fwd_bytes=lay, ws=fake, ws_bytes=bwd, grads=g: (
+        ctypes.byref(out), fwd, fwd_bytes, 0, ctypes.c_float(0.0), ctypes.c_float(0.0),
+        ctypes.byref(grads), ws, ws_bytes, None)
+    assert L.moe_layer_backward(ctypes.byref(c), *args(dy=None), *tail()) == -1
+    assert L.moe_layer_backward(ctypes.byref(c), *args(logits=None), *tail()) == -1
+    assert L.moe_layer_backward(ctypes.byref(c), *args(), *tail(ws_bytes=16)) == -3
+    assert L.moe_layer_backward(ctypes.byref(c), *args(), *tail(fwd_bytes=16)) == -3
+    g0 = N.MoeGrads(**{f: (1 << 20) for f in N.GRAD_FIELDS}); g0.dW_in = None
+    assert L.moe_layer_backward(ctypes.byref(c), *args(), *tail(grads=g0)) == -1
+    c32 = moe.make_config(CONFIGS[1])
+    assert L.moe_layer_backward(ctypes.byref(c32), *args(), *tail()) == -2   # bf16 only
+    cp = moe.make_config(preset(2, gate_norm="pnorm", gate_p=2.0))
+    assert L.moe_layer_backward(ctypes.byref(cp), *args(), *tail()) == -2    # forward-only gates
+    assert L.moe_pack_weights_backward(ctypes.byref(c32), fake, fake, fake, fake, fake, None) == -2

@@ -14,7 +14,7 @@ c_int32, c_int64, c_float, c_size_t, c_void_p = (ctypes.c_int32, ctypes.c_int64,
 MOE_F32, MOE_BF16 = 0, 1
 MOE_ACT_RELU, MOE_ACT_SWIGLU = 0, 1
 GATE_NORMS = {"softmax_topk": 0, "none": 1, "pnorm": 2}
-MOE_WS_STEP, MOE_WS_LAYER = 0, 1
+MOE_WS_STEP, MOE_WS_LAYER, MOE_WS_BACKWARD = 0, 1, 2
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
                 -3: "MOE_ERR_WORKSPACE", -4: "MOE_ERR_CUDA", -5: "MOE_ERR_TIMEOUT",
@@ -35,6 +35,13 @@ ROUTE_FIELDS = ("expert_id", "gate", "pos", "drop_reason", "row", "counts", "cou
 
 class MoeRouteOut(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ROUTE_FIELDS]
+
+
+GRAD_FIELDS = ("dx", "dW_g", "dbias", "dW_in", "dW_up", "dW_out", "dWs_in", "dWs_up", "dWs_out")
+
+
+class MoeGrads(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in GRAD_FIELDS]
 
 
 _P = ctypes.POINTER
@@ -71,6 +78,14 @@ _PROTOTYPES = {
     "moe_layer_forward": [_P(MoeConfig), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                           c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, _P(MoeRouteOut),
                           c_void_p, c_size_t, c_void_p],
+    "moe_pack_weights_backward": [_P(MoeConfig), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                  c_void_p],
+    "moe_pack_shared_weights_backward": [_P(MoeConfig), c_void_p, c_void_p, c_void_p, c_void_p,
+                                         c_void_p, c_void_p],
+    "moe_layer_backward": [_P(MoeConfig), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                           c_void_p, c_void_p, c_void_p, c_void_p, _P(MoeRouteOut), c_void_p,
+                           c_size_t, ctypes.c_int, c_float, c_float, _P(MoeGrads), c_void_p,
+                           c_size_t, c_void_p],
     "moe_get_device_status": [c_void_p, c_void_p],
 }
 _RESTYPES = {"moe_status_string": ctypes.c_char_p}

@@ -195,10 +195,14 @@ int moe_rows_max(const moe_config_t* cfg, int64_t* R_max) {
 }
 
 int moe_workspace_bytes(const moe_config_t* cfg, int kind, size_t* bytes) {
-  if (!bytes || (kind != MOE_WS_STEP && kind != MOE_WS_LAYER)) return MOE_ERR_INVALID_ARG;
+  if (!bytes || (kind != MOE_WS_STEP && kind != MOE_WS_LAYER && kind != MOE_WS_BACKWARD))
+    return MOE_ERR_INVALID_ARG;
   Prep p;
   const int rc = prepare(cfg, &p);
-  if (rc == MOE_OK) *bytes = kind == MOE_WS_STEP ? p.L.step_bytes : p.L.layer_bytes;
+  if (rc == MOE_OK)
+    *bytes = kind == MOE_WS_STEP ? p.L.step_bytes
+             : kind == MOE_WS_LAYER ? p.L.layer_bytes
+                                    : ws_layout_bwd(*cfg, p.C).bytes;
   return rc;
 }
 
@@ -405,6 +409,213 @@ int moe_layer_forward(const moe_config_t* cfg, const void* x, const void* W_g, c
                            ws_bytes, stream)) != MOE_OK)
     return rc;
   return moe_combine(cfg, y_perm, r, shared_out, residual, y, stream);
+}
+
+int moe_pack_weights_backward(const moe_config_t* cfg, const void* W_in, const void* W_up,
+                              const void* W_out, void* Wt_in_packed, void* Wt_out_packed,
+                              moe_stream_t stream) {
+  Prep p;
+  int rc = prepare(cfg, &p);
+  if (rc != MOE_OK) return rc;
+  if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const bool sw = cfg->act == MOE_ACT_SWIGLU;
+  if (!W_in || !W_out || !Wt_in_packed || !Wt_out_packed || (sw && !W_up)) return MOE_ERR_INVALID_ARG;
+  rc = launch_pack_transposed(0, 0, cfg->E, cfg->H, cfg->M, cfg->M, cfg->H, 1, W_out, nullptr,
+                              Wt_out_packed, stream);
+  if (rc != MOE_OK) return rc;
+  return launch_pack_transposed(1, sw, cfg->E, cfg->M, sw ? 2 * cfg->H : cfg->H, cfg->M, cfg->H, 1,
+                                W_in, W_up, Wt_in_packed, stream);
+}
+
+int moe_pack_shared_weights_backward(const moe_config_t* cfg, const void* Ws_in, const void* Ws_up,
+                                     const void* Ws_out, void* Wst_in_packed, void* Wst_out_packed,
+                                     moe_stream_t stream) {
+  Prep p;
+  int rc = prepare(cfg, &p);
+  if (rc != MOE_OK) return rc;
+  if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (cfg->n_shared < 1) return MOE_ERR_INVALID_ARG;
+  const bool sw = cfg->act == MOE_ACT_SWIGLU;
+  if (!Ws_in || !Ws_out || !Wst_in_packed || !Wst_out_packed || (sw && !Ws_up))
+    return MOE_ERR_INVALID_ARG;
+  const int Hc = cfg->n_shared * cfg->H_shared;
+  rc = launch_pack_transposed(0, 0, 1, Hc, cfg->M, cfg->M, cfg->H_shared, cfg->n_shared, Ws_out,
+                              nullptr, Wst_out_packed, stream);
+  if (rc != MOE_OK) return rc;
+  return launch_pack_transposed(1, sw, 1, cfg->M, sw ? 2 * Hc : Hc, cfg->M, Hc, 1, Ws_in, Ws_up,
+                                Wst_in_packed, stream);
+}
+
+// One expert FFN's backward on (ragged or dense) row segments, the steps moe_layer_backward
+// runs for the routed experts and again for the shared ones.
+struct FfnBwd {
+  const void* x_rows;   // forward A rows (x_perm, or x for the dense shared segment)
+  int64_t rows_cap;     // rows of x_rows / the segment buffers
+  const int32_t* offsets;  // ragged segments (null: one dense segment of dense_rows)
+  int groups, dense_rows;
+  int Hn;               // hidden units of one group
+  const void* W_in_packed;  // forward pack (SwiGLU recompute)
+  const void* Wt_in_packed;
+  const void* Wt_out_packed;
+  const void* dy_rows;  // [rows_cap, M] upstream gradient rows
+  const float* w;       // per-row gate (null: 1)
+  const void* h;        // forward hidden [rows_cap, Hn]
+  void* dh;             // SwiGLU scratch [rows_cap, Hn]
+  void* dab;            // [rows_cap, F]
+  float* gpart;         // nullable
+  void* dx_rows;        // [rows_cap, M]
+};
+
+int ffn_backward_data(const moe_config_t& c, const FfnBwd& f, unsigned* status, cudaStream_t st) {
+  const bool sw = c.act == MOE_ACT_SWIGLU;
+  const int64_t F = sw ? 2 * int64_t(f.Hn) : f.Hn;
+  GemmDesc d;  // gradient through GEMM 2 (and the ReLU mask, the gate's gradient)
+  d.epi = EPI_DGRAD2;
+  d.A = f.dy_rows; d.a_rows = f.rows_cap; d.K = c.M;
+  d.B = f.Wt_out_packed; d.N = f.Hn; d.b_rows = int64_t(f.groups) * f.Hn; d.b_tiled = true;
+  d.offsets = f.offsets; d.groups = f.groups; d.rows_dense = f.dense_rows;
+  d.out = sw ? f.dh : f.dab; d.ldo = f.Hn;
+  d.row_scale = f.w; d.aux = f.h; d.ld_aux = f.Hn; d.gpart = f.gpart; d.relu = sw ? 0 : 1;
+  d.status = status;
+  int rc = launch_gemm_bf16(d, st);
+  if (rc != MOE_OK) return rc;
+  if (sw) {  // recompute the pre-activations, apply the SwiGLU derivative
+    GemmDesc e;
+    e.epi = EPI_SWIGLU_BWD;
+    e.A = f.x_rows; e.a_rows = f.rows_cap; e.K = c.M;
+    e.B = f.W_in_packed; e.N = 2 * f.Hn; e.b_rows = int64_t(f.groups) * 2 * f.Hn; e.b_tiled = true;
+    e.offsets = f.offsets; e.groups = f.groups; e.rows_dense = f.dense_rows;
+    e.out = f.dab; e.ldo = F; e.aux = f.dh; e.ld_aux = f.Hn;
+    e.status = status;
+    if ((rc = launch_gemm_bf16(e, st)) != MOE_OK) return rc;
+  }
+  GemmDesc g;  // gradient through GEMM 1
+  g.epi = EPI_SCALE;
+  g.A = f.dab; g.a_rows = f.rows_cap; g.K = int(F);
+  g.B = f.Wt_in_packed; g.N = c.M; g.b_rows = int64_t(f.groups) * c.M; g.b_tiled = true;
+  g.offsets = f.offsets; g.groups = f.groups; g.rows_dense = f.dense_rows;
+  g.out = f.dx_rows; g.ldo = c.M;
+  g.status = status;
+  return launch_gemm_bf16(g, st);
+}
+
+// dW[g] (fp32 [c1][N]) = A_g . B_g^T over group g's padded K segment (A [c1][Kp], B [N][Kp]).
+int weight_grad(const void* A, int c1, const void* B, int N, int64_t Kp, const int32_t* koffs,
+                int groups, float* out, float* out2, unsigned* status, cudaStream_t st) {
+  GemmDesc d;
+  d.epi = EPI_F32_BIAS;
+  d.A = A; d.a_rows = c1; d.K = int(Kp);
+  d.B = B; d.N = N; d.b_rows = N; d.b_tiled = false;
+  d.koffs = koffs; d.c1 = c1; d.groups = groups;
+  d.out = out; d.ldo = N; d.n_valid = N; d.out2 = out2;
+  d.status = status;
+  return launch_gemm_bf16(d, st);
+}
+
+int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, const void* W_g,
+                       const void* W_in_packed, const void* Wt_in_packed, const void* Wt_out_packed,
+                       const void* Ws_in_packed, const void* Wst_in_packed,
+                       const void* Wst_out_packed, const float* logits, const moe_route_out_t* r,
+                       const void* fwd_ws, size_t fwd_ws_bytes, int residual, float aux_coef,
+                       float z_coef, const moe_grads_t* grads, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+  Prep p;
+  int rc = prepare(cfg, &p);
+  if (rc != MOE_OK) return rc;
+  const moe_config_t& c = *cfg;
+  if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (c.gate_norm != MOE_GATE_SOFTMAX_TOPK && c.gate_norm != MOE_GATE_NONE) return MOE_ERR_UNSUPPORTED;
+  if (c.uniform_assignment) return MOE_ERR_UNSUPPORTED;
+  if (c.E > 256) return MOE_ERR_UNSUPPORTED;
+  const bool sw = c.act == MOE_ACT_SWIGLU;
+  const bool shared = c.n_shared > 0;
+  if (!x || !dy || !W_g || !Wt_in_packed || !Wt_out_packed || !logits || !grads || !fwd_ws)
+    return MOE_ERR_INVALID_ARG;
+  if (sw && !W_in_packed) return MOE_ERR_INVALID_ARG;
+  if (!grads->dx || !grads->dW_g || !grads->dW_in || !grads->dW_out || (sw && !grads->dW_up))
+    return MOE_ERR_INVALID_ARG;
+  if (shared && (!Wst_in_packed || !Wst_out_packed || (sw && !Ws_in_packed) || !grads->dWs_in ||
+                 !grads->dWs_out || (sw && !grads->dWs_up)))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(dy) || !aligned16(grads->dx)) return MOE_ERR_INVALID_ARG;
+  if ((rc = check_route_out(c, r)) != MOE_OK) return rc;
+  if ((rc = check_ws(const_cast<void*>(fwd_ws), fwd_ws_bytes, p.L.layer_bytes)) != MOE_OK) return rc;
+  const WsLayoutBwd B = ws_layout_bwd(c, p.C);
+  if ((rc = check_ws(ws, ws_bytes, B.bytes)) != MOE_OK) return rc;
+  char* w = static_cast<char*>(ws);
+  const char* fw = static_cast<const char*>(fwd_ws);
+  unsigned* status = reinterpret_cast<unsigned*>(w + B.status);
+  const int64_t R = p.R_max;
+  const int F = sw ? 2 * c.H : c.H;
+
+  // routed experts: data gradients (tcgen05 GEMMs over the expert segments)
+  if ((rc = launch_dispatch(c, R, dy, r->token_of, r->expert_offsets, w + B.dy_perm, stream)) != MOE_OK)
+    return rc;
+  FfnBwd f;
+  f.x_rows = fw + p.L.x_perm; f.rows_cap = R; f.offsets = r->expert_offsets; f.groups = c.E;
+  f.dense_rows = 0; f.Hn = c.H; f.W_in_packed = W_in_packed; f.Wt_in_packed = Wt_in_packed;
+  f.Wt_out_packed = Wt_out_packed; f.dy_rows = w + B.dy_perm; f.w = r->w_perm;
+  f.h = fw + p.L.h_perm; f.dh = w + B.dh; f.dab = w + B.dab;
+  f.gpart = reinterpret_cast<float*>(w + B.gpart); f.dx_rows = w + B.dx_perm;
+  if ((rc = ffn_backward_data(c, f, status, stream)) != MOE_OK) return rc;
+  // routed experts: weight gradients over per-expert 64-padded transposed segments
+  int32_t* poff = reinterpret_cast<int32_t*>(w + B.poff);
+  if ((rc = launch_pad_offsets(r->expert_offsets, c.E, 0, poff, stream)) != MOE_OK) return rc;
+  struct T { const void* in; int64_t ld; const int32_t* gather; const float* scale; int C; size_t out; };
+  const T ts[4] = {{dy, c.M, r->token_of, r->w_perm, c.M, B.dyT},
+                   {fw + p.L.h_perm, c.H, nullptr, nullptr, c.H, B.hT},
+                   {w + B.dab, F, nullptr, nullptr, F, B.dabT},
+                   {x, c.M, r->token_of, nullptr, c.M, B.xT}};
+  for (const T& t : ts) {
+    const int src_rows = t.gather ? c.S : int(R);
+    if ((rc = launch_seg_transpose(t.in, t.ld, r->expert_offsets, c.E, 0, poff, B.Rp, t.gather,
+                                   src_rows, t.scale, t.C, w + t.out, B.Rp, status, stream)) != MOE_OK)
+      return rc;
+  }
+  if ((rc = weight_grad(w + B.dyT, c.M, w + B.hT, c.H, B.Rp, poff, c.E, grads->dW_out, nullptr,
+                        status, stream)) != MOE_OK)
+    return rc;
+  if ((rc = weight_grad(w + B.dabT, F, w + B.xT, c.M, B.Rp, poff, c.E, grads->dW_in,
+                        sw ? grads->dW_up : nullptr, status, stream)) != MOE_OK)
+    return rc;
+  // the router: dlogits from the gates' gradients, aux and z; then dx, dW_g, dbias
+  if ((rc = launch_router_backward(c, logits, *r, reinterpret_cast<const float*>(w + B.gpart),
+                                   B.n_tiles2, aux_coef, z_coef,
+                                   reinterpret_cast<float*>(w + B.dlogits), x, W_g,
+                                   reinterpret_cast<float*>(w + B.dx_r), grads->dW_g, grads->dbias,
+                                   reinterpret_cast<float*>(w + B.part), stream)) != MOE_OK)
+    return rc;
+  // shared experts: one dense segment of all S tokens, weight 1
+  void* dxs = nullptr;
+  if (shared) {
+    const int Hc = c.n_shared * c.H_shared, Fs = sw ? 2 * Hc : Hc;
+    FfnBwd s;
+    s.x_rows = x; s.rows_cap = c.S; s.offsets = nullptr; s.groups = 1; s.dense_rows = c.S;
+    s.Hn = Hc; s.W_in_packed = Ws_in_packed; s.Wt_in_packed = Wst_in_packed;
+    s.Wt_out_packed = Wst_out_packed; s.dy_rows = dy; s.w = nullptr; s.h = fw + p.L.h_shared;
+    s.dh = w + B.dhs; s.dab = w + B.dabs; s.gpart = nullptr; s.dx_rows = w + B.dxs;
+    if ((rc = ffn_backward_data(c, s, status, stream)) != MOE_OK) return rc;
+    int32_t* poff_s = reinterpret_cast<int32_t*>(w + B.poff_s);
+    if ((rc = launch_pad_offsets(nullptr, 1, c.S, poff_s, stream)) != MOE_OK) return rc;
+    const T tss[4] = {{dy, c.M, nullptr, nullptr, c.M, B.dyTs},
+                      {fw + p.L.h_shared, Hc, nullptr, nullptr, Hc, B.hsT},
+                      {w + B.dabs, Fs, nullptr, nullptr, Fs, B.dabsT},
+                      {x, c.M, nullptr, nullptr, c.M, B.xTs}};
+    for (const T& t : tss)
+      if ((rc = launch_seg_transpose(t.in, t.ld, nullptr, 1, c.S, poff_s, B.Sp, nullptr, c.S,
+                                     nullptr, t.C, w + t.out, B.Sp, status, stream)) != MOE_OK)
+        return rc;
+    if ((rc = weight_grad(w + B.dyTs, c.M, w + B.hsT, Hc, B.Sp, poff_s, 1, grads->dWs_out, nullptr,
+                          status, stream)) != MOE_OK)
+      return rc;
+    if ((rc = weight_grad(w + B.dabsT, Fs, w + B.xTs, c.M, B.Sp, poff_s, 1, grads->dWs_in,
+                          sw ? grads->dWs_up : nullptr, status, stream)) != MOE_OK)
+      return rc;
+    dxs = w + B.dxs;
+  }
+  // dx = sum over kept choices of the rows' gradients (+ shared) (+ dy) + the router's
+  return launch_combine(c, w + B.dx_perm, r->row, dxs, residual ? dy : nullptr, grads->dx, R,
+                        stream, reinterpret_cast<const float*>(w + B.dx_r));
 }
 
 int moe_get_device_status(void* ws, moe_stream_t stream) {

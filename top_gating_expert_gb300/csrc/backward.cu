@@ -1,0 +1,417 @@
+// The layer's backward pass: layout kernels for the weight gradients and the router's
+// backward (the expert GEMMs of the backward run on the tcgen05 grouped GEMM).
+//
+// The loss is L = sum(dy * y) + aux_coef * aux + z_coef * z. MegaBlocks router chapter §3:
+// the load-balancing loss is a differentiable proxy, its gradient reaching the router only
+// through the expert scores (the counts are constants); §2: the z-loss mean(lse^2). Routing
+// decisions are held fixed (piecewise constant in the logits). GShard summary page, "MoE
+// Transformer": each expert a two-layer FFN; Lec16 Systems for MoE Models, "DeepSeek V3 MoE":
+// SwiGLU experts.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kPad = 64;  // K-block of the grouped GEMM: weight-gradient segments start on it
+
+// poff[g] = sum over g' < g of the rows of g' rounded up to 64 (g = 0..groups); with
+// offsets null, one group of dense_rows rows.
+__global__ void pad_offsets_kernel(const int32_t* __restrict__ offsets, int groups, int dense_rows,
+                                   int32_t* __restrict__ poff) {
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  int run = 0;
+  poff[0] = 0;
+  for (int g = 0; g < groups; ++g) {
+    int n = offsets ? offsets[g + 1] - offsets[g] : dense_rows;
+    if (n < 0) n = 0;
+    run += (n + kPad - 1) / kPad * kPad;
+    poff[g + 1] = run;
+  }
+}
+
+// out [C][ld_out] (bf16): column p of group g's padded range is row i = p - poff[g] of the
+// group (rows off[g] + i, or i when dense), zero for i past its rows; the value is
+// scale[r] * in[src(r)][c] with src(r) = gather[r] (or r). A 64 x 64 tile per block through
+// shared memory.
+__global__ void __launch_bounds__(256)
+    seg_transpose_kernel(const __nv_bfloat16* __restrict__ in, int64_t ld_in,
+                         const int32_t* __restrict__ offsets, int groups, int dense_rows,
+                         const int32_t* __restrict__ poff, const int32_t* __restrict__ gather,
+                         int src_rows, const float* __restrict__ scale, int C,
+                         __nv_bfloat16* __restrict__ out, int64_t ld_out, unsigned* status) {
+  __shared__ __nv_bfloat16 tile[64][72];
+  __shared__ int s_g;
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x;
+  const int p0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+  if (p0 >= poff[groups]) return;  // past the last padded segment (uniform in the block)
+  if (tid == 0) {
+    int lo = 0, hi = groups;  // the group whose padded range holds p0
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (poff[mid] <= p0) lo = mid;
+      else hi = mid;
+    }
+    s_g = lo;
+  }
+  __syncthreads();
+  const int g = s_g;
+  const int base = offsets ? offsets[g] : 0;
+  const int n = offsets ? offsets[g + 1] - base : dense_rows;
+  const int i0 = p0 - poff[g];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int rr = tid / 8 + 32 * h, cc = (tid % 8) * 8;
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const int i = i0 + rr;
+    if (i < n && c0 + cc < C) {
+      const int r = base + i;
+      int src = gather ? gather[r] : r;
+      if (src < 0 || src >= src_rows) {
+        atomicOr(status, kStatusDeviceData);
+        src = -1;
+      }
+      if (src >= 0) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(in + int64_t(src) * ld_in + c0 + cc));
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+        const float sc = scale ? scale[r] : 1.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(b[q]);
+          v[2 * q] = f.x * sc;
+          v[2 * q + 1] = f.y * sc;
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) tile[rr][cc + q] = __float2bfloat16_rn(v[q]);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int cr = tid / 8 + 32 * h, pc = (tid % 8) * 8;
+    if (c0 + cr >= C) continue;
+    __align__(16) __nv_bfloat16 w[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) w[q] = tile[pc + q][cr];
+    *reinterpret_cast<uint4*>(out + int64_t(c0 + cr) * ld_out + p0 + pc) = *reinterpret_cast<const uint4*>(w);
+  }
+}
+
+// Transposed weights for the backward's dgrad GEMMs, packed tile-major like the forward's
+// ([g][N/BN][K/64][BN][64], one contiguous block per TMA box):
+//   mode 0: N = Hn hidden units, K = M: element (g, n, k) = W_out[g][k][n], W_out [g][M][Hn];
+//           with parts > 1 (shared experts side by side, g = 0): W_out[n / Hp][k][n % Hp].
+//   mode 1: N = M, K = F: ReLU (F = Hn) element (g, n, k) = W_in[g][k][n]; SwiGLU (F = 2 Hn,
+//           the forward's interleaved order) k = 256 b + c: c < 128: W_in[g][128 b + c][n],
+//           else W_up[g][128 b + c - 128][n]. W_in, W_up [g][Hn][M] (shared experts: their
+//           hidden units side by side, [Hn][M]).
+__global__ void __launch_bounds__(256)
+    pack_transposed_kernel(const __nv_bfloat16* __restrict__ W, const __nv_bfloat16* __restrict__ W2,
+                           int mode, int swiglu, int groups, int N, int K, int M, int Hp, int parts,
+                           int BN, __nv_bfloat16* __restrict__ dst) {
+  const int64_t total = int64_t(groups) * N * (K / 8);
+  for (int64_t u = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; u < total;
+       u += int64_t(gridDim.x) * blockDim.x) {
+    const int kq = int(u % (K / 8));
+    const int64_t gn = u / (K / 8);
+    const int n = int(gn % N);
+    const int g = int(gn / N);
+    const int k0 = kq * 8;
+    __align__(16) __nv_bfloat16 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int k = k0 + q;
+      int64_t src;
+      const __nv_bfloat16* base = W;
+      if (mode == 0) {
+        const int part = n / Hp, j = n % Hp;  // parts == 1: part 0, j = n
+        src = (int64_t(parts > 1 ? part : g) * M + k) * Hp + j;
+      } else {
+        int h = k;
+        if (swiglu) {
+          const int c = k & 255;
+          h = (k >> 8) * 128 + (c & 127);
+          if (c >= 128) base = W2;
+        }
+        src = (int64_t(g) * (swiglu ? K / 2 : K) + h) * M + n;
+      }
+      v[q] = base[src];
+    }
+    const int64_t blk = (int64_t(g) * (N / BN) + n / BN) * (K / 64) + k0 / 64;
+    *reinterpret_cast<uint4*>(dst + blk * BN * 64 + int64_t(n % BN) * 64 + (k0 % 64)) =
+        *reinterpret_cast<const uint4*>(v);
+  }
+}
+
+// dL/dlogits, one warp per token (lane l holds experts l, l + 32, ...):
+//   gate term   MOE_GATE_SOFTMAX_TOPK: g = softmax over the k selected logits,
+//               dl[id_j] += g_j (dg_j - sum_i g_i dg_i); MOE_GATE_NONE: g_j = p[id_j],
+//               dl[id_j] += g_j dg_j and dl[e] -= p_e sum_j g_j dg_j;
+//   aux term    aux_coef * E / (G * S_g) * p_e (f_e - sum_e' f_e' p_e'), f = counts_routed of
+//               the token's group / (S_g k);
+//   z term      z_coef * 2 / S * lse * p_e.
+// dg_j (the gate's gradient) = sum over the GEMM's N tiles of gpart[row] for a kept
+// assignment, 0 for a dropped one (it adds nothing to y).
+template <int KMAX>
+__global__ void __launch_bounds__(256)
+    router_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ expert_id,
+                      const int32_t* __restrict__ row, const float* __restrict__ gpart, int n_tiles,
+                      const int32_t* __restrict__ counts_routed, int S, int G, int E, int k,
+                      int gate_norm, float aux_coef, float z_coef, float* __restrict__ dlogits) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int t = int((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  if (t >= S) return;
+  const float* lr = logits + int64_t(t) * E;
+  float l[8], p[8];
+  float m = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int e = lane + 32 * q;
+    l[q] = e < E ? lr[e] : -INFINITY;
+    m = fmaxf(m, l[q]);
+  }
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float s = 0.f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    p[q] = lane + 32 * q < E ? expf(l[q] - m) : 0.f;
+    s += p[q];
+  }
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  const float inv = 1.f / s, lse = m + logf(s);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) p[q] *= inv;
+  // the k choices: ids, selected logits, gate gradients (lane j < k gathers dg_j)
+  int id[KMAX];
+  float dg[KMAX], gsel[KMAX];
+  float dgl = 0.f;
+  if (lane < k) {
+    const int r = row[int64_t(t) * k + lane];
+    if (r >= 0)
+      for (int nt = 0; nt < n_tiles; ++nt) dgl += gpart[int64_t(r) * n_tiles + nt];
+  }
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    id[j] = j < k ? expert_id[int64_t(t) * k + j] : 0;
+    dg[j] = __shfl_sync(0xffffffffu, dgl, j);
+    gsel[j] = j < k ? lr[id[j]] : -INFINITY;
+  }
+  float dl[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (gate_norm == MOE_GATE_SOFTMAX_TOPK) {
+    const float top = gsel[0];  // the largest selected logit
+    float gs = 0.f;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      gsel[j] = j < k ? expf(gsel[j] - top) : 0.f;
+      gs += gsel[j];
+    }
+    float inner = 0.f;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      gsel[j] /= gs;
+      inner += gsel[j] * dg[j];
+    }
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (j < k && id[j] == lane + 32 * q) dl[q] += gsel[j] * (dg[j] - inner);
+  } else {  // MOE_GATE_NONE
+    float inner = 0.f;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      gsel[j] = j < k ? expf(gsel[j] - m) * inv : 0.f;
+      inner += gsel[j] * dg[j];
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) dl[q] -= p[q] * inner;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (j < k && id[j] == lane + 32 * q) dl[q] += gsel[j] * dg[j];
+  }
+  const int Sg = S / G;
+  if (aux_coef != 0.f) {
+    const int32_t* cr = counts_routed + int64_t(t / Sg) * E;
+    const float fs = 1.f / (float(Sg) * float(k));
+    float f[8], fp = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int e = lane + 32 * q;
+      f[q] = e < E ? float(cr[e]) * fs : 0.f;
+      fp += f[q] * p[q];
+    }
+    for (int off = 16; off > 0; off >>= 1) fp += __shfl_xor_sync(0xffffffffu, fp, off);
+    const float c = aux_coef * float(E) / (float(G) * float(Sg));
+#pragma unroll
+    for (int q = 0; q < 8; ++q) dl[q] += c * p[q] * (f[q] - fp);
+  }
+  if (z_coef != 0.f) {
+    const float c = z_coef * 2.f / float(S) * lse;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) dl[q] += c * p[q];
+  }
+  float* out = dlogits + int64_t(t) * E;
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    if (lane + 32 * q < E) out[lane + 32 * q] = dl[q];
+}
+
+// dx_r[t][m] = sum_e dl[t][e] W_g[e][m] (fp32): a block takes 8 tokens x 256 columns.
+__global__ void __launch_bounds__(256)
+    router_dx_kernel(const float* __restrict__ dl, const __nv_bfloat16* __restrict__ W_g, int S,
+                     int E, int M, float* __restrict__ dx) {
+  __shared__ float s_dl[8][256];
+  pdl_wait();
+  pdl_trigger();
+  const int t0 = blockIdx.y * 8, m = blockIdx.x * 256 + threadIdx.x;
+  for (int i = threadIdx.x; i < 8 * E; i += 256) {
+    const int tt = i / E, e = i % E;
+    s_dl[tt][e] = t0 + tt < S ? dl[int64_t(t0 + tt) * E + e] : 0.f;
+  }
+  __syncthreads();
+  if (m >= M) return;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int e = 0; e < E; ++e) {
+    const float w = __bfloat162float(W_g[int64_t(e) * M + m]);
+#pragma unroll
+    for (int tt = 0; tt < 8; ++tt) acc[tt] += s_dl[tt][e] * w;
+  }
+#pragma unroll
+  for (int tt = 0; tt < 8; ++tt)
+    if (t0 + tt < S) dx[int64_t(t0 + tt) * M + m] = acc[tt];
+}
+
+// part[ch][e][m] = sum over the chunk's 256 tokens of dl[t][e] x[t][m]; a block takes 128
+// columns x 32 experts of one chunk.
+__global__ void __launch_bounds__(128)
+    router_dw_partial_kernel(const float* __restrict__ dl, const __nv_bfloat16* __restrict__ x, int S,
+                             int E, int M, float* __restrict__ part) {
+  __shared__ float s_dl[256][33];
+  pdl_wait();
+  pdl_trigger();
+  const int m = blockIdx.x * 128 + threadIdx.x, e0 = blockIdx.y * 32, ch = blockIdx.z;
+  const int t0 = ch * 256;
+  for (int i = threadIdx.x; i < 256 * 32; i += 128) {
+    const int tt = i / 32, q = i % 32;
+    s_dl[tt][q] = (t0 + tt < S && e0 + q < E) ? dl[int64_t(t0 + tt) * E + e0 + q] : 0.f;
+  }
+  __syncthreads();
+  const int n = min(256, S - t0);
+  if (blockIdx.x == 0 && threadIdx.x < 32 && e0 + threadIdx.x < E) {  // the bias column
+    float b = 0.f;
+    for (int tt = 0; tt < n; ++tt) b += s_dl[tt][threadIdx.x];
+    part[int64_t(gridDim.z) * E * M + int64_t(ch) * E + e0 + threadIdx.x] = b;
+  }
+  if (m >= M) return;
+  float acc[32];
+#pragma unroll
+  for (int q = 0; q < 32; ++q) acc[q] = 0.f;
+  for (int tt = 0; tt < n; ++tt) {
+    const float xv = __bfloat162float(x[int64_t(t0 + tt) * M + m]);
+#pragma unroll
+    for (int q = 0; q < 32; ++q) acc[q] += s_dl[tt][q] * xv;
+  }
+#pragma unroll
+  for (int q = 0; q < 32; ++q)
+    if (e0 + q < E) part[(int64_t(ch) * E + e0 + q) * M + m] = acc[q];
+}
+
+// dW_g[e][m] = sum over chunks in order of part[ch][e][m]; dbias[e] likewise over the bias
+// partials (part[nch][E][M] is followed by [nch][E] sums of dl over each chunk's tokens).
+__global__ void __launch_bounds__(256)
+    router_dw_reduce_kernel(const float* __restrict__ part, int nch, int E, int M,
+                            float* __restrict__ dW, float* __restrict__ dbias) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < int64_t(E) * M) {
+    float acc = 0.f;
+    for (int ch = 0; ch < nch; ++ch) acc += part[int64_t(ch) * E * M + i];
+    dW[i] = acc;
+  }
+  if (dbias && i < E) {
+    const float* pb = part + int64_t(nch) * E * M;
+    float acc = 0.f;
+    for (int ch = 0; ch < nch; ++ch) acc += pb[int64_t(ch) * E + i];
+    dbias[i] = acc;
+  }
+}
+
+}  // namespace
+
+int launch_pad_offsets(const int32_t* offsets, int groups, int dense_rows, int32_t* poff,
+                       cudaStream_t st) {
+  return launch_kernel(pad_offsets_kernel, dim3(1), dim3(32), 0, st, offsets, groups, dense_rows,
+                       poff);
+}
+
+int launch_seg_transpose(const void* in, int64_t ld_in, const int32_t* offsets, int groups,
+                         int dense_rows, const int32_t* poff, int64_t rows_pad_max,
+                         const int32_t* gather, int src_rows, const float* scale, int C, void* out,
+                         int64_t ld_out, unsigned* status, cudaStream_t st) {
+  if (C % 8 || ld_in % 8 || ld_out % 8 || rows_pad_max % 64) return MOE_ERR_UNSUPPORTED;
+  const dim3 grid(unsigned((C + 63) / 64), unsigned(rows_pad_max / 64));
+  if (grid.y == 0) return MOE_OK;
+  return launch_kernel(seg_transpose_kernel, grid, dim3(256), 0, st,
+                       static_cast<const __nv_bfloat16*>(in), ld_in, offsets, groups, dense_rows,
+                       poff, gather, src_rows, scale, C, static_cast<__nv_bfloat16*>(out), ld_out,
+                       status);
+}
+
+int launch_pack_transposed(int mode, int swiglu, int groups, int N, int K, int M, int Hp, int parts,
+                           const void* W, const void* W2, void* dst, cudaStream_t st) {
+  const int BN = mode == 0 ? gemm_bn(N, EPI_DGRAD2) : gemm_bn(N, EPI_SCALE);
+  if (BN <= 0 || N % BN || K % 64) return MOE_ERR_UNSUPPORTED;
+  const int64_t total = int64_t(groups) * N * (K / 8);
+  const unsigned grid = unsigned((total + 255) / 256 < 65535 * 8 ? (total + 255) / 256 : 65535 * 8);
+  pack_transposed_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(W),
+                                               static_cast<const __nv_bfloat16*>(W2), mode, swiglu,
+                                               groups, N, K, M, Hp, parts, BN,
+                                               static_cast<__nv_bfloat16*>(dst));
+  MOE_CUDA_CHECK(cudaGetLastError());
+  return MOE_OK;
+}
+
+int launch_router_backward(const moe_config_t& c, const float* logits, const moe_route_out_t& r,
+                           const float* gpart, int n_tiles, float aux_coef, float z_coef,
+                           float* dlogits, const void* x, const void* W_g, float* dx_router,
+                           float* dW_g, float* dbias, float* part, cudaStream_t st) {
+  if (c.E > 256) return MOE_ERR_UNSUPPORTED;
+  const unsigned blocks = unsigned((int64_t(c.S) * 32 + 255) / 256);
+  int rc;
+  if (c.k <= 2)
+    rc = launch_kernel(router_bwd_kernel<2>, dim3(blocks), dim3(256), 0, st, logits, r.expert_id, r.row,
+                       gpart, n_tiles, r.counts_routed, c.S, c.G, c.E, c.k, c.gate_norm, aux_coef,
+                       z_coef, dlogits);
+  else
+    rc = launch_kernel(router_bwd_kernel<8>, dim3(blocks), dim3(256), 0, st, logits, r.expert_id, r.row,
+                       gpart, n_tiles, r.counts_routed, c.S, c.G, c.E, c.k, c.gate_norm, aux_coef,
+                       z_coef, dlogits);
+  if (rc != MOE_OK) return rc;
+  auto xb = static_cast<const __nv_bfloat16*>(x);
+  auto wg = static_cast<const __nv_bfloat16*>(W_g);
+  rc = launch_kernel(router_dx_kernel, dim3(unsigned((c.M + 255) / 256), unsigned((c.S + 7) / 8)),
+                     dim3(256), 0, st, static_cast<const float*>(dlogits), wg, c.S, c.E, c.M, dx_router);
+  if (rc != MOE_OK) return rc;
+  const int nch = (c.S + 255) / 256;
+  rc = launch_kernel(router_dw_partial_kernel,
+                     dim3(unsigned((c.M + 127) / 128), unsigned((c.E + 31) / 32), unsigned(nch)),
+                     dim3(128), 0, st, static_cast<const float*>(dlogits), xb, c.S, c.E, c.M, part);
+  if (rc != MOE_OK) return rc;
+  return launch_kernel(router_dw_reduce_kernel,
+                       dim3(unsigned((int64_t(c.E) * c.M + 255) / 256)), dim3(256), 0, st,
+                       static_cast<const float*>(part), nch, c.E, c.M, dW_g, dbias);
+}
+
+}  // namespace moe

@@ -67,7 +67,7 @@ struct Cfg {
   static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);
   static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + 16 + 2 * (kMaxGroups + 1) * 4;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + 16 + 3 * (kMaxGroups + 1) * 4;
 };
 
 struct KParams {
@@ -83,6 +83,13 @@ struct KParams {
   const float* bias;
   int n_valid;
   unsigned* status;
+  const void* aux;  // EPI_DGRAD2: h; EPI_SWIGLU_BWD: dh (bf16)
+  int64_t ld_aux;
+  float* gpart;     // EPI_DGRAD2: [rows][n_tiles] sums of D * h, nullable
+  int relu;
+  const int32_t* koffs;  // K-ragged mode: per-group K range
+  int c1;                // K-ragged mode: output rows per group
+  void* out2;            // interleaved SwiGLU rows: the second 128-row block of each pair
 };
 
 using namespace sm100;
@@ -92,9 +99,14 @@ using namespace sm100;
 // holding tile row `grow` stores it if `valid`. nt: the tile's N index.
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, bool valid,
-                                              int64_t grow, int nt) {
+                                              int64_t grow, int nt, bool zero = false) {
   if constexpr (EPI == EPI_F32_BIAS) {
     float* out = static_cast<float*>(p.out) + grow * p.ldo;
+    if (p.out2) {  // row j of group g in the interleaved SwiGLU order (128 gate, 128 up rows)
+      const int64_t g = grow / p.c1, j = grow % p.c1, c = j & 255;
+      out = static_cast<float*>(c < 128 ? p.out : p.out2) +
+            (g * (p.c1 / 2) + (j >> 8) * 128 + (c & 127)) * p.ldo;
+    }
     const bool vec = (p.ldo & 3) == 0;
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 16) {
@@ -106,7 +118,8 @@ __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, 
         float f[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          f[j] = __uint_as_float(v[j]) + ((p.bias && nb + j < p.n_valid) ? p.bias[nb + j] : 0.f);
+          f[j] = zero ? 0.f  // a K-ragged group with no rows: its gradient is 0
+                      : __uint_as_float(v[j]) + ((p.bias && nb + j < p.n_valid) ? p.bias[nb + j] : 0.f);
         if (vec && nb + 16 <= p.n_valid) {
           float4* d = reinterpret_cast<float4*>(out + nb);
 #pragma unroll
@@ -116,6 +129,75 @@ __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, 
           for (int j = 0; j < 16; ++j)
             if (nb + j < p.n_valid) out[nb + j] = f[j];
         }
+      }
+    }
+  } else if constexpr (EPI == EPI_DGRAD2) {
+    // D = dy_perm . W_out (unscaled); out = w_r * D (ReLU: where h > 0), gate partial
+    // sum_c D * h over this tile's columns (h as the forward stored it, bf16)
+    const float scale = (valid && p.row_scale) ? p.row_scale[grow] : 1.f;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + nt * BN;
+    const __nv_bfloat16* hrow = static_cast<const __nv_bfloat16*>(p.aux) + grow * p.ld_aux + nt * BN;
+    float gsum = 0.f;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      uint32_t v[16];
+      tmem_ld16(tbase + c0, v);
+      tmem_ld_wait();
+      if (valid) {
+        const uint4 h0 = reinterpret_cast<const uint4*>(hrow + c0)[0];
+        const uint4 h1 = reinterpret_cast<const uint4*>(hrow + c0)[1];
+        const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+        uint32_t pk[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 hv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[j]));
+          const float d0 = __uint_as_float(v[2 * j]), d1 = __uint_as_float(v[2 * j + 1]);
+          gsum += d0 * hv.x + d1 * hv.y;
+          float o0 = d0 * scale, o1 = d1 * scale;
+          if (p.relu) {
+            o0 = hv.x > 0.f ? o0 : 0.f;
+            o1 = hv.y > 0.f ? o1 : 0.f;
+          }
+          pk[j] = pack_bf16x2(o0, o1);
+        }
+        store_bf16x16(out + c0, pk);
+      }
+    }
+    if (valid && p.gpart) p.gpart[grow * p.n_tiles + nt] = gsum;
+  } else if constexpr (EPI == EPI_SWIGLU_BWD) {
+    // D = (a | b): the tile's 128 gate and 128 up pre-activations of hidden units
+    // 128 nt ..; with dh: da = dh * b * silu'(a), db = dh * silu(a), written to the same
+    // interleaved column positions (out [rows, 2H])
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + nt * BN;
+    const __nv_bfloat16* dhrow = static_cast<const __nv_bfloat16*>(p.aux) + grow * p.ld_aux + nt * (BN / 2);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN / 2; c0 += 16) {
+      uint32_t av[16], bv[16];
+      tmem_ld16(tbase + c0, av);
+      tmem_ld16(tbase + BN / 2 + c0, bv);
+      tmem_ld_wait();
+      if (valid) {
+        const uint4 d0 = reinterpret_cast<const uint4*>(dhrow + c0)[0];
+        const uint4 d1 = reinterpret_cast<const uint4*>(dhrow + c0)[1];
+        const uint32_t dw[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+        uint32_t pa[8], pb[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 dh = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[j]));
+          float da[2], db[2];
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const float a = __uint_as_float(av[2 * j + q]), b = __uint_as_float(bv[2 * j + q]);
+            const float sg = 1.f / (1.f + __expf(-a));
+            const float d = q ? dh.y : dh.x;
+            da[q] = d * b * sg * (1.f + a * (1.f - sg));
+            db[q] = d * a * sg;
+          }
+          pa[j] = pack_bf16x2(da[0], da[1]);
+          pb[j] = pack_bf16x2(db[0], db[1]);
+        }
+        store_bf16x16(out + c0, pa);
+        store_bf16x16(out + BN / 2 + c0, pb);
       }
     }
   } else if constexpr (EPI == EPI_SWIGLU) {
@@ -170,7 +252,7 @@ __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, 
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int BN, int EPI, bool PAIR>
+template <int BN, int EPI, bool PAIR, bool KRAG>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const KParams p) {
@@ -186,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_total = reinterpret_cast<int*>(s_tmem + 2);
   int* s_tstart = reinterpret_cast<int*>(s_tmem + 4);  // [groups+1] first m-tile of each group
   int* s_off = s_tstart + (kMaxGroups + 1);            // [groups+1] first row of each group
+  int* s_koff = s_off + (kMaxGroups + 1);              // K-ragged: [groups+1] K offsets
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars);
@@ -193,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tfull0 = empty0 + 8 * C::STAGES;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain_bar = tempty0 + 16;
-  const int G = p.offsets ? p.groups : 1;
+  const int G = (p.offsets || KRAG) ? p.groups : 1;
   const uint32_t rank = PAIR ? cluster_rank() : 0u;
   const bool leader = rank == 0;
   const int unit = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);  // this CTA's tile stream
@@ -228,8 +311,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g = base + lane;
       int cnt = 0;
       if (g < G) {
-        const int lo = p.offsets ? p.offsets[g] : 0;
-        const int hi = p.offsets ? p.offsets[g + 1] : p.rows_dense;
+        int lo, hi;
+        if constexpr (KRAG) {  // c1 output rows per group; K range from koffs
+          lo = g * p.c1;
+          hi = lo + p.c1;
+          const int k0 = p.koffs[g], k1 = p.koffs[g + 1];
+          if (k0 < 0 || k1 < k0 || k1 > p.K || (k0 | k1) % BK) bad = true;
+          s_koff[g] = k0;
+          if (g == G - 1) s_koff[G] = k1;
+        } else {
+          lo = p.offsets ? p.offsets[g] : 0;
+          hi = p.offsets ? p.offsets[g + 1] : p.rows_dense;
+        }
         if (lo < 0 || hi < lo || int64_t(hi) > p.rows_cap) bad = true;
         else cnt = (hi - lo + C::TILE_M - 1) / C::TILE_M;
         s_off[g] = lo;
@@ -283,10 +376,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = unit; t < total && ok; t += units) {
       int g, m0, rows, nt;
       decode(t, g, m0, rows, nt);
-      const int arow = m0 + int(rank) * BM;
-      const int brow = g * p.N + nt * BN + int(rank) * C::B_ROWS;
+      const int arow = m0 - (KRAG ? g * p.c1 : 0) + int(rank) * BM;
+      const int brow = (KRAG ? 0 : g * p.N) + nt * BN + int(rank) * C::B_ROWS;
       const int bblk = (g * p.n_tiles + nt) * kblocks;
-      for (int kb = 0; kb < kblocks; ++kb) {
+      const int kb0 = KRAG ? s_koff[g] / BK : 0;
+      const int nkb = KRAG ? s_koff[g + 1] / BK - kb0 : kblocks;
+      for (int kb = 0; kb < nkb; ++kb) {
         ok = __all_sync(0xffffffffu, wait_bounded(empty0 + 8 * stage, phase ^ 1u, s_abort, p.status));
         if (!ok) break;
         if (lane == 0) {
@@ -296,13 +391,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (leader) mbar_expect_tx(fb, C::CTAS * C::STAGE_BYTES);
           if constexpr (PAIR) {
             const uint32_t lfb = cluster_addr(fb, 0);  // the even CTA's full barrier
-            tma_load_2d_pair(dA, &tmA, kb * BK, arow, lfb);
+            tma_load_2d_pair(dA, &tmA, (kb0 + kb) * BK, arow, lfb);
             if (p.b_tiled) tma_load_3d_pair(dB, &tmB, 0, int(rank) * C::B_ROWS, bblk + kb, lfb);
-            else tma_load_2d_pair(dB, &tmB, kb * BK, brow, lfb);
+            else tma_load_2d_pair(dB, &tmB, (kb0 + kb) * BK, brow, lfb);
           } else {
-            tma_load_2d(dA, &tmA, kb * BK, arow, fb);
+            tma_load_2d(dA, &tmA, (kb0 + kb) * BK, arow, fb);
             if (p.b_tiled) tma_load_3d(dB, &tmB, 0, 0, bblk + kb, fb);
-            else tma_load_2d(dB, &tmB, kb * BK, brow, fb);
+            else tma_load_2d(dB, &tmB, (kb0 + kb) * BK, brow, fb);
           }
         }
         __syncwarp();
@@ -336,7 +431,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem_base + uint32_t(acc * BN);
-        for (int kb = 0; kb < kblocks; ++kb) {
+        int nkb = kblocks;
+        if constexpr (KRAG) {
+          int g, m0, rows, nt;
+          decode(t, g, m0, rows, nt);
+          nkb = (s_koff[g + 1] - s_koff[g]) / BK;
+        }
+        for (int kb = 0; kb < nkb; ++kb) {
           ok = __all_sync(0xffffffffu, wait_bounded(full0 + 8 * stage, phase, s_abort, p.status));
           if (!ok) break;
           tc_fence_after();
@@ -390,7 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       decode(t, g, m0, rows, nt);
       const int r = int(rank) * BM + q * 32 + lane;  // row within the tile
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
-      epilogue_rows<BN, EPI>(p, tbase, r < rows, int64_t(m0) + r, nt);
+      const bool zero = KRAG && s_koff[g + 1] == s_koff[g];  // no MMA ran for this tile
+      epilogue_rows<BN, EPI>(p, tbase, r < rows, int64_t(m0) + r, nt, zero);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -456,11 +558,12 @@ int make_map_tiled(CUtensorMap* m, const void* base, int64_t blocks, int block_r
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
-template <int BN, int EPI, bool PAIR>
+template <int BN, int EPI, bool PAIR, bool KRAG = false>
 int run_gemm(const GemmDesc& d, cudaStream_t st) {
   using C = Cfg<BN, PAIR>;
   CUtensorMap ta, tb;
-  int rc = make_map(&ta, d.A, d.a_rows, d.K, BM);
+  if (KRAG && (!d.koffs || d.c1 < 1 || d.b_tiled || d.groups < 1)) return MOE_ERR_INVALID_ARG;
+  int rc = make_map(&ta, d.A, KRAG ? d.c1 : d.a_rows, d.K, BM);
   if (rc != MOE_OK) return rc;
   if (d.b_tiled) {
     if (d.N % BN != 0 || d.b_rows % d.N != 0) return MOE_ERR_UNSUPPORTED;
@@ -475,7 +578,7 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
   p.offsets = d.offsets;
   p.groups = d.groups;
   p.rows_dense = d.rows_dense;
-  p.rows_cap = d.a_rows;
+  p.rows_cap = KRAG ? int64_t(d.groups) * d.c1 : d.a_rows;
   p.N = d.N;
   p.K = d.K;
   p.n_tiles = (d.N + BN - 1) / BN;
@@ -485,10 +588,19 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
   p.bias = d.bias;
   p.n_valid = d.n_valid;
   p.status = d.status;
-  auto kern = grouped_gemm_kernel<BN, EPI, PAIR>;
+  p.aux = d.aux;
+  p.ld_aux = d.ld_aux;
+  p.gpart = d.gpart;
+  p.relu = d.relu;
+  p.koffs = d.koffs;
+  p.c1 = d.c1;
+  p.out2 = d.out2;
+  auto kern = grouped_gemm_kernel<BN, EPI, PAIR, KRAG>;
   MOE_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
-  const int64_t m_tiles = d.offsets ? (d.a_rows + C::TILE_M - 1) / C::TILE_M + d.groups
-                                    : (int64_t(d.rows_dense) + C::TILE_M - 1) / C::TILE_M;
+  const int64_t m_tiles =
+      KRAG ? int64_t(d.groups) * ((d.c1 + C::TILE_M - 1) / C::TILE_M)
+           : d.offsets ? (d.a_rows + C::TILE_M - 1) / C::TILE_M + d.groups
+                       : (int64_t(d.rows_dense) + C::TILE_M - 1) / C::TILE_M;
   const int64_t tiles = m_tiles * p.n_tiles;
   cudaLaunchConfig_t lc = {};
   lc.blockDim = dim3(kThreads);
@@ -535,7 +647,24 @@ int launch_gemm_bf16(const GemmDesc& d, cudaStream_t st) {
   const int bn = gemm_bn(d.N, d.epi);
   // 256-wide tiles of packed weights run on CTA pairs (cta_group::2, 256 x 256 tiles)
   const bool pair = d.b_tiled && bn == 256;
+  if (d.koffs) {  // weight gradients: K ragged per group, fp32 out, single-CTA tiles
+    if (d.epi != EPI_F32_BIAS || d.groups > kMaxGroups) return MOE_ERR_UNSUPPORTED;
+    // the fp32 epilogue masks columns past N, so any N takes the widest tile up to 256
+    if (d.N > 128) return run_gemm<256, EPI_F32_BIAS, false, true>(d, st);
+    if (d.N > 64) return run_gemm<128, EPI_F32_BIAS, false, true>(d, st);
+    return run_gemm<64, EPI_F32_BIAS, false, true>(d, st);
+  }
   switch (d.epi) {
+    case EPI_DGRAD2:
+      if (bn == 256) return pair ? run_gemm<256, EPI_DGRAD2, true>(d, st)
+                                 : run_gemm<256, EPI_DGRAD2, false>(d, st);
+      if (bn == 128) return run_gemm<128, EPI_DGRAD2, false>(d, st);
+      if (bn == 64) return run_gemm<64, EPI_DGRAD2, false>(d, st);
+      return MOE_ERR_UNSUPPORTED;
+    case EPI_SWIGLU_BWD:
+      if (bn == 256) return pair ? run_gemm<256, EPI_SWIGLU_BWD, true>(d, st)
+                                 : run_gemm<256, EPI_SWIGLU_BWD, false>(d, st);
+      return MOE_ERR_UNSUPPORTED;
     case EPI_F32_BIAS:
       switch (bn) {
         case 16: return run_gemm<16, EPI_F32_BIAS, false>(d, st);

@@ -70,9 +70,28 @@ inline WsLayout ws_layout(const moe_config_t& c, int C) {
   return L;
 }
 
+// Byte offsets of the backward workspace (moe_layer_backward): R rows of the routed
+// experts, Rp = R_max + 64 E columns of the transposed, per-expert 64-padded segments.
+struct WsLayoutBwd {
+  int64_t Rp = 0, Sp = 0;
+  int n_tiles2 = 0;  // N tiles of the backward GEMM 2 (gate-partial stride)
+  int nch = 0;       // 256-token chunks of the router's weight gradient
+  size_t status = 0, dy_perm = 0, dh = 0, dab = 0, gpart = 0, dx_perm = 0, poff = 0, poff_s = 0,
+         dyT = 0, hT = 0, dabT = 0, xT = 0, dlogits = 0, dx_r = 0, part = 0, dhs = 0, dabs = 0,
+         dxs = 0, dyTs = 0, hsT = 0, dabsT = 0, xTs = 0;
+  size_t bytes = 0;
+};
+
 // ------------------------------------------------------------------ GEMM tiling
 // Epilogues of the bf16 tcgen05 GEMM (gemm_tcgen05.cu).
-enum GemmEpilogue { EPI_F32_BIAS = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_SCALE = 3 };
+enum GemmEpilogue {
+  EPI_F32_BIAS = 0,    // fp32 out (+ per-column bias); in K-ragged mode the weight gradients
+  EPI_RELU = 1,        // bf16 relu(D)
+  EPI_SWIGLU = 2,      // bf16 silu(D_gate) * D_up
+  EPI_SCALE = 3,       // bf16 row_scale[r] * D
+  EPI_DGRAD2 = 4,      // backward of GEMM 2: bf16 w_r * D (ReLU: masked by h > 0), gate partials
+  EPI_SWIGLU_BWD = 5,  // backward of the SwiGLU: from D = (a | b) and dh, bf16 (da | db)
+};
 
 // N-tile width of the bf16 GEMM for N output columns per group (0 = unsupported). The
 // packed weight layout depends on it, so packing and launching both take it from here.
@@ -82,11 +101,50 @@ inline int gemm_bn(int N, int epi) {
       if (N <= bn) return bn;
     return 0;
   }
-  if (epi == EPI_SWIGLU) return N % 256 == 0 ? 256 : 0;
+  if (epi == EPI_SWIGLU || epi == EPI_SWIGLU_BWD) return N % 256 == 0 ? 256 : 0;
   if (N % 256 == 0) return 256;
   if (N % 128 == 0) return 128;
   if (N % 64 == 0) return 64;
   return 0;
+}
+
+inline WsLayoutBwd ws_layout_bwd(const moe_config_t& c, int C) {
+  WsLayoutBwd B;
+  const int64_t R = rows_max(c, C);
+  const bool sw = c.act == MOE_ACT_SWIGLU;
+  const int64_t F = sw ? 2 * int64_t(c.H) : c.H;
+  const int64_t Hc = int64_t(c.n_shared) * c.H_shared, Fs = sw ? 2 * Hc : Hc;
+  B.Rp = (R + 64 * int64_t(c.E) + 63) / 64 * 64;
+  B.Sp = (int64_t(c.S) + 63) / 64 * 64;
+  const int bn2 = gemm_bn(c.H, EPI_DGRAD2);
+  B.n_tiles2 = bn2 > 0 ? c.H / bn2 : 1;
+  B.nch = (c.S + 255) / 256;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o = align256(o + bytes); return at; };
+  B.status = take(256);
+  B.dy_perm = take(size_t(R) * c.M * 2);
+  B.dh = take(sw ? size_t(R) * c.H * 2 : 0);
+  B.dab = take(size_t(R) * F * 2);
+  B.gpart = take(size_t(R) * B.n_tiles2 * 4);
+  B.dx_perm = take(size_t(R) * c.M * 2);
+  B.poff = take(size_t(c.E + 1) * 4);
+  B.poff_s = take(2 * 4);
+  B.dyT = take(size_t(c.M) * B.Rp * 2);
+  B.hT = take(size_t(c.H) * B.Rp * 2);
+  B.dabT = take(size_t(F) * B.Rp * 2);
+  B.xT = take(size_t(c.M) * B.Rp * 2);
+  B.dlogits = take(size_t(c.S) * c.E * 4);
+  B.dx_r = take(size_t(c.S) * c.M * 4);
+  B.part = take((size_t(B.nch) * c.E * c.M + size_t(B.nch) * c.E) * 4);
+  B.dhs = take(sw ? size_t(c.S) * Hc * 2 : 0);
+  B.dabs = take(size_t(c.S) * Fs * 2);
+  B.dxs = take(Hc ? size_t(c.S) * c.M * 2 : 0);
+  B.dyTs = take(Hc ? size_t(c.M) * B.Sp * 2 : 0);
+  B.hsT = take(size_t(Hc) * B.Sp * 2);
+  B.dabsT = take(size_t(Fs) * B.Sp * 2);
+  B.xTs = take(Hc ? size_t(c.M) * B.Sp * 2 : 0);
+  B.bytes = o;
+  return B;
 }
 
 // ------------------------------------------------------------------ launchers
@@ -104,7 +162,7 @@ int launch_dispatch(const moe_config_t& c, int64_t R_max, const void* x, const i
                     const int32_t* offsets, void* x_perm, cudaStream_t st);
 int launch_combine(const moe_config_t& c, const void* y_perm, const int32_t* row,
                    const void* shared_out, const void* residual, void* y, int64_t R_max,
-                   cudaStream_t st);
+                   cudaStream_t st, const float* add32 = nullptr);  // + fp32 [S, M] term
 // Weight packing. bf16: tile-major [groups][N/BN][K/64][BN][64] (one contiguous 32 KB block
 // per TMA box of the GEMM, BN = gemm_bn); fp32: row-major [groups][N][K].
 //   first layer: N = H (ReLU) or 2H (SwiGLU: blocks of 256 rows = 128 W_in rows, then the
@@ -130,6 +188,19 @@ struct GemmDesc {
   const float* bias = nullptr;           // EPI_F32_BIAS: per-column bias (nullable)
   int n_valid = 0;                       // EPI_F32_BIAS: columns stored
   unsigned* status = nullptr;
+  // EPI_DGRAD2: aux = h [rows, N] bf16 (ld_aux elements a row), gpart = per-(row, N tile)
+  // sums of D * h (nullable), relu = mask by h > 0. EPI_SWIGLU_BWD: aux = dh [rows, N/2].
+  const void* aux = nullptr; int64_t ld_aux = 0;
+  float* gpart = nullptr;
+  int relu = 0;
+  // K-ragged mode (weight gradients, EPI_F32_BIAS): group g = rows g*c1 .. g*c1 + c1 - 1 of
+  // the output, its K range [koffs[g], koffs[g+1]) (multiples of 64) of A [c1, K] and
+  // B [N, K] (both row-major; A and B are shared by all groups, K = koffs[groups]).
+  const int32_t* koffs = nullptr;
+  int c1 = 0;
+  // with out2: output rows are pairs of 128-row blocks (the interleaved SwiGLU order) that go
+  // to out (first block) and out2 (second), each [groups * c1 / 2, N]
+  void* out2 = nullptr;
 };
 int launch_gemm_bf16(const GemmDesc& d, cudaStream_t st);
 // 2-D tensor map over a row-major bf16 [rows, K] matrix, boxes of 64 columns x box_rows rows,
@@ -145,6 +216,20 @@ int launch_ffn_up_f32(const moe_config_t& c, int H, const float* A, const int32_
 int launch_ffn_down_f32(const moe_config_t& c, int H, const float* h, const int32_t* offsets,
                         int groups, int rows_dense, int64_t rows_cap, const float* row_scale,
                         const float* W_out, float* y, unsigned* status, cudaStream_t st);
+
+// backward.cu
+int launch_pad_offsets(const int32_t* offsets, int groups, int dense_rows, int32_t* poff,
+                       cudaStream_t st);
+int launch_seg_transpose(const void* in, int64_t ld_in, const int32_t* offsets, int groups,
+                         int dense_rows, const int32_t* poff, int64_t rows_pad_max,
+                         const int32_t* gather, int src_rows, const float* scale, int C, void* out,
+                         int64_t ld_out, unsigned* status, cudaStream_t st);
+int launch_pack_transposed(int mode, int swiglu, int groups, int N, int K, int M, int Hp, int parts,
+                           const void* W, const void* W2, void* dst, cudaStream_t st);
+int launch_router_backward(const moe_config_t& c, const float* logits, const moe_route_out_t& r,
+                           const float* gpart, int n_tiles, float aux_coef, float z_coef,
+                           float* dlogits, const void* x, const void* W_g, float* dx_router,
+                           float* dW_g, float* dbias, float* part, cudaStream_t st);
 
 int num_sms();
 

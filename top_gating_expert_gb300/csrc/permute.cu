@@ -87,6 +87,15 @@ struct Vec8 {  // 16 bytes of elements, widened to fp32
       v[3] += __uint_as_float(u.w);
     }
   }
+  // n fp32 values (8 for bf16 rows, 4 for fp32 rows), 16-byte aligned
+  __device__ __forceinline__ void add_f32(const float* p) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
+    if constexpr (kBF16) {
+      const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+      v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+    }
+  }
   __device__ __forceinline__ uint4 pack() const {
     uint4 u;
     if constexpr (kBF16) {
@@ -110,7 +119,7 @@ template <bool kBF16, int KMAX>
 __global__ void __launch_bounds__(kThreads) combine_kernel(
     const uint4* __restrict__ y_perm, const int32_t* __restrict__ row, int k, int S, int units,
     int64_t R_max, const uint4* __restrict__ shared, const uint4* __restrict__ residual,
-    uint4* __restrict__ y) {
+    const float* __restrict__ add32, uint4* __restrict__ y) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -158,6 +167,11 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
       if (residual) {
         a0.add(r0);
         a1.add(r1);
+      }
+      if (add32) {  // an fp32 term, added before the one rounding
+        constexpr int n = Vec8<kBF16>::n;
+        a0.add_f32(add32 + (t * units + q0) * n);
+        if (has1) a1.add_f32(add32 + (t * units + q1) * n);
       }
       __stcs(y + t * units + q0, a0.pack());
       if (has1) __stcs(y + t * units + q1, a1.pack());
@@ -242,22 +256,24 @@ int launch_dispatch(const moe_config_t& c, int64_t R_max, const void* x, const i
 template <bool kBF16>
 int combine_dispatch_k(int k, unsigned grid, cudaStream_t st, const uint4* yp, const int32_t* row,
                        int S, int units, int64_t R_max, const uint4* sh, const uint4* res,
-                       uint4* y) {
+                       const float* add32, uint4* y) {
   auto kern = k <= 2 ? combine_kernel<kBF16, 2> : (k <= 4 ? combine_kernel<kBF16, 4> : combine_kernel<kBF16, 8>);
-  return launch_kernel(kern, dim3(grid), dim3(kThreads), 0, st, yp, row, k, S, units, R_max, sh, res, y);
+  return launch_kernel(kern, dim3(grid), dim3(kThreads), 0, st, yp, row, k, S, units, R_max, sh, res,
+                       add32, y);
 }
 
 int launch_combine(const moe_config_t& c, const void* y_perm, const int32_t* row,
                    const void* shared_out, const void* residual, void* y, int64_t R_max,
-                   cudaStream_t st) {
+                   cudaStream_t st, const float* add32) {
   const int units = int(c.M * elem_bytes(c) / 16);
   const unsigned grid = grid_for(c.S);
   auto yp = static_cast<const uint4*>(y_perm);
   auto sh = static_cast<const uint4*>(shared_out);
   auto res = static_cast<const uint4*>(residual);
   auto yo = static_cast<uint4*>(y);
-  if (c.dtype == MOE_BF16) return combine_dispatch_k<true>(c.k, grid, st, yp, row, c.S, units, R_max, sh, res, yo);
-  return combine_dispatch_k<false>(c.k, grid, st, yp, row, c.S, units, R_max, sh, res, yo);
+  if (c.dtype == MOE_BF16)
+    return combine_dispatch_k<true>(c.k, grid, st, yp, row, c.S, units, R_max, sh, res, add32, yo);
+  return combine_dispatch_k<false>(c.k, grid, st, yp, row, c.S, units, R_max, sh, res, add32, yo);
 }
 
 namespace {

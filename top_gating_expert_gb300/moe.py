@@ -230,6 +230,66 @@ def layer_forward(cfg, x, W_g, bias, W_in_packed, W_out_packed, Ws_in_packed, Ws
         ctypes.byref(s), _ptr(ws), ws.numel(), _stream(stream)), "moe_layer_forward")
 
 
+def pack_weights_backward(cfg, W_in, W_up, W_out, stream=None):
+    """Transposed packs for the backward's data-gradient GEMMs: (Wt_in_packed, Wt_out_packed)."""
+    c = _cfg(cfg)
+    n_in, n_out, _, _ = packed_sizes(c)
+    p_in = torch.empty(n_in, dtype=W_in.dtype, device=W_in.device)
+    p_out = torch.empty(n_out, dtype=W_in.dtype, device=W_in.device)
+    _check(N.lib().moe_pack_weights_backward(ctypes.byref(c), _ptr(W_in), _ptr(W_up), _ptr(W_out),
+                                             _ptr(p_in), _ptr(p_out), _stream(stream)),
+           "moe_pack_weights_backward")
+    return p_in, p_out
+
+
+def pack_shared_weights_backward(cfg, Ws_in, Ws_up, Ws_out, stream=None):
+    c = _cfg(cfg)
+    _, _, n_in, n_out = packed_sizes(c)
+    p_in = torch.empty(n_in, dtype=Ws_in.dtype, device=Ws_in.device)
+    p_out = torch.empty(n_out, dtype=Ws_in.dtype, device=Ws_in.device)
+    _check(N.lib().moe_pack_shared_weights_backward(ctypes.byref(c), _ptr(Ws_in), _ptr(Ws_up),
+                                                    _ptr(Ws_out), _ptr(p_in), _ptr(p_out),
+                                                    _stream(stream)),
+           "moe_pack_shared_weights_backward")
+    return p_in, p_out
+
+
+class Grads:
+    """Device buffers for moe_layer_backward's outputs (fp32 weight gradients)."""
+
+    def __init__(self, cfg, device="cuda", bias=False):
+        c = _cfg(cfg)
+        sw = c.act == N.MOE_ACT_SWIGLU
+        f32 = lambda *shape: torch.zeros(shape, dtype=torch.float32, device=device)
+        Hc = c.n_shared * c.H_shared
+        self.dx = torch.zeros((c.S, c.M), dtype=torch_dtype(c), device=device)
+        self.dW_g = f32(c.E, c.M)
+        self.dbias = f32(c.E) if bias else None
+        self.dW_in = f32(c.E, c.H, c.M)
+        self.dW_up = f32(c.E, c.H, c.M) if sw else None
+        self.dW_out = f32(c.E, c.M, c.H)
+        self.dWs_in = f32(Hc, c.M) if Hc else None
+        self.dWs_up = f32(Hc, c.M) if (Hc and sw) else None
+        self.dWs_out = f32(c.M, Hc) if Hc else None
+
+    def struct(self) -> N.MoeGrads:
+        return N.MoeGrads(**{f: (getattr(self, f).data_ptr() if getattr(self, f) is not None else None)
+                             for f in N.GRAD_FIELDS})
+
+
+def layer_backward(cfg, x, dy, W_g, W_in_packed, Wt_in_packed, Wt_out_packed, Ws_in_packed,
+                   Wst_in_packed, Wst_out_packed, logits, out: RouteOutputs, fwd_ws, residual,
+                   aux_coef, z_coef, grads: Grads, ws, stream=None):
+    s = out.struct()
+    g = grads.struct()
+    _check(N.lib().moe_layer_backward(
+        ctypes.byref(_cfg(cfg)), _ptr(x), _ptr(dy), _ptr(W_g), _ptr(W_in_packed), _ptr(Wt_in_packed),
+        _ptr(Wt_out_packed), _ptr(Ws_in_packed), _ptr(Wst_in_packed), _ptr(Wst_out_packed),
+        _ptr(logits), ctypes.byref(s), _ptr(fwd_ws), fwd_ws.numel(), int(bool(residual)),
+        float(aux_coef), float(z_coef), ctypes.byref(g), _ptr(ws), ws.numel(), _stream(stream)),
+        "moe_layer_backward")
+
+
 def device_status(ws, stream=None) -> int:
     """Synchronises the stream; returns (and clears) the device status recorded in ws."""
     return N.lib().moe_get_device_status(_ptr(ws), _stream(stream))
@@ -274,6 +334,31 @@ class MoeLayer:
                       self.Ws_in_packed, self.Ws_out_packed, u, residual, y, self.logits,
                       self.route_out, self.ws, stream)
         return y
+
+    def enable_backward(self, weights: dict):
+        """Pack the transposed weights the backward needs and allocate its workspace and
+        gradient buffers (self.grads)."""
+        dt = torch_dtype(self.cfg)
+        to = lambda t: None if t is None else t.to(device=self.device, dtype=dt).contiguous()
+        self.Wt_in_packed, self.Wt_out_packed = pack_weights_backward(
+            self.cfg, to(weights["W_in"]), to(weights.get("W_up")), to(weights["W_out"]))
+        self.Wst_in_packed = self.Wst_out_packed = None
+        if self.cfg.n_shared > 0:
+            self.Wst_in_packed, self.Wst_out_packed = pack_shared_weights_backward(
+                self.cfg, to(weights["Ws_in"]), to(weights.get("Ws_up")), to(weights["Ws_out"]))
+        self.ws_bwd = workspace(self.cfg, N.MOE_WS_BACKWARD, self.device)
+        self.grads = Grads(self.cfg, self.device, bias=self.bias is not None)
+
+    def backward(self, x, dy, residual=False, aux_coef=0.0, z_coef=0.0, stream=None):
+        """Gradients of sum(dy * y) + aux_coef * aux + z_coef * z for the last forward on x
+        (which must have kept its logits), into self.grads."""
+        if self.logits is None:
+            raise RuntimeError("the backward needs the forward's logits (keep_logits=True)")
+        layer_backward(self.cfg, x, dy, self.W_g, self.W_in_packed, self.Wt_in_packed,
+                       self.Wt_out_packed, self.Ws_in_packed, self.Wst_in_packed,
+                       self.Wst_out_packed, self.logits, self.route_out, self.ws, residual,
+                       aux_coef, z_coef, self.grads, self.ws_bwd, stream)
+        return self.grads
 
     def capture(self, x, u=None, residual=None, warmup: int = 1) -> torch.cuda.CUDAGraph:
         """Capture forward(x, u, residual) into a CUDA graph (one launch per replay). x, u,
