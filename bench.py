@@ -45,6 +45,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", type=int, default=2, help="workload preset (1..5)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-backward", action="store_true",
+                   help="skip the training-step (forward + backward) measurement")
     p.add_argument("--override", action="append", default=[], metavar="KEY=VALUE",
                    help="change a field of the preset (smaller cases for profiler captures)")
     return p.parse_args()
@@ -341,6 +343,46 @@ def run_ours(args, rank, world, local_rank):
     h2d = x_host.numel() * x_host.element_size() + (u_host.numel() * 4 if u_host is not None else 0)
     d2h = y_host.numel() * y_host.element_size() + 8
 
+    # ---- the backward pass (a training step): a layer that keeps its logits, forward then
+    # moe_layer_backward on the same inputs, L2 flushed before each step
+    bwd = None
+    if cfg["dtype"] == "bf16" and not args.no_backward:
+        tl = moe.MoeLayer(cfg, inp.host, device=dev)
+        tl.enable_backward(inp.host)
+        dy = torch.randn((c.S, c.M), generator=torch.Generator().manual_seed(7)).to(dt).to(dev)
+        aux_c, z_c = 0.01, 0.001
+
+        def train_step(evs=None):
+            if evs:
+                evs[0].record()
+            tl.forward(x, u, residual)
+            if evs:
+                evs[1].record()
+            tl.backward(x, dy, residual=residual is not None, aux_coef=aux_c, z_coef=z_c)
+            if evs:
+                evs[2].record()
+
+        for _ in range(args.warmup):
+            flush.zero_()
+            train_step()
+        tev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        barrier()
+        for s_ in range(args.steps):
+            flush.zero_()
+            train_step(tev[s_])
+        barrier()
+        rc = moe.device_status(tl.ws_bwd)
+        if rc != 0:
+            raise RuntimeError(f"device status {rc} in the backward region")
+        f_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in tev)
+        b_ms = statistics.mean(b.elapsed_time(e) for _, b, e in tev)
+        if world > 1:
+            t = torch.tensor([f_ms, b_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            f_ms, b_ms = float(t[0]), float(t[1])
+        bwd = (f_ms, b_ms, tl.route_out.expert_offsets[-1].item())
+        del tl, dy
+
     if rank != 0:
         return None
 
@@ -425,6 +467,28 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
         "wall_s_timed_region": round(t_wall, 4),
     }
+    if bwd is not None:
+        f_ms, b_ms, Rb = bwd
+        F = f1 * H
+        Hc = c.n_shared * c.H_shared
+        # algorithmic flops: GEMM 2's and GEMM 1's data and weight gradients (and the SwiGLU
+        # pre-activations recomputed) for the routed rows and the shared experts' S rows; the
+        # router's dx and dW_g
+        def ffn_bwd(rows, hidden):
+            fh = f1 * hidden
+            return 2.0 * rows * M * (2 * hidden + 2 * fh) + (4.0 * rows * M * hidden if f1 == 2 else 0.0)
+        flops = ffn_bwd(Rb, H) + (ffn_bwd(S, Hc) if Hc else 0.0) + 4.0 * S * E * M
+        grad_bytes = 4 * (E * (F + H) * M + ((f1 + 1) * Hc * M if Hc else 0) + E * M)
+        line["backward"] = {
+            "what": "moe_layer_backward: gradients of sum(dy*y) + 0.01 aux + 0.001 z w.r.t. x, "
+                    "W_g, every expert weight (fp32), routing fixed; forward = moe_layer_forward "
+                    "keeping its logits; L2 flushed before each step",
+            "ms_per_step": round(b_ms, 5), "forward_ms_per_step": round(f_ms, 5),
+            "train_tokens_per_s": round(S * world / ((f_ms + b_ms) * 1e-3), 1),
+            "algorithmic_flops": flops, "TFLOP/s": round(flops / (b_ms * 1e-3) / 1e12, 2),
+            "tensor_frac_sustained": round(flops / (b_ms * 1e-3) / 1e12 / P["tc_sustained"], 4),
+            "fp32_weight_grad_bytes": int(grad_bytes),
+        }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, n, inp)
     return line
