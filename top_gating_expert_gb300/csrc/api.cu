@@ -578,12 +578,21 @@ int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, c
   if ((rc = weight_grad(w + B.dabT, F, w + B.xT, c.M, B.Rp, poff, c.E, grads->dW_in,
                         sw ? grads->dW_up : nullptr, status, stream)) != MOE_OK)
     return rc;
-  // the router: dlogits from the gates' gradients, aux and z; then dx, dW_g, dbias
+  // x^T [M][Sp] (zero-padded): the router's dW_g and the shared experts' weight gradients
+  int32_t* poff_s = reinterpret_cast<int32_t*>(w + B.poff_s);
+  if ((rc = launch_pad_offsets(nullptr, 1, c.S, poff_s, stream)) != MOE_OK) return rc;
+  if ((rc = launch_seg_transpose(x, c.M, nullptr, 1, c.S, poff_s, B.Sp, nullptr, c.S, nullptr, c.M,
+                                 w + B.xTs, B.Sp, status, stream)) != MOE_OK)
+    return rc;
+  // the router: dlogits from the gates' gradients, aux and z; then dx, dW_g (tcgen05), dbias
+  RouterBwdBufs rb;
+  rb.dlogits = reinterpret_cast<float*>(w + B.dlogits);
+  rb.dlb = w + B.dlb; rb.dlT = w + B.dlT; rb.wgT = w + B.wgT; rb.xT = w + B.xTs;
+  rb.dx_r = reinterpret_cast<float*>(w + B.dx_r);
+  rb.koff_e = reinterpret_cast<int32_t*>(w + B.koff_e); rb.koff_s = poff_s; rb.Sp = B.Sp;
   if ((rc = launch_router_backward(c, logits, *r, reinterpret_cast<const float*>(w + B.gpart),
-                                   B.n_tiles2, aux_coef, z_coef,
-                                   reinterpret_cast<float*>(w + B.dlogits), x, W_g,
-                                   reinterpret_cast<float*>(w + B.dx_r), grads->dW_g, grads->dbias,
-                                   reinterpret_cast<float*>(w + B.part), stream)) != MOE_OK)
+                                   B.n_tiles2, aux_coef, z_coef, rb, x, W_g, grads->dW_g,
+                                   grads->dbias, status, stream)) != MOE_OK)
     return rc;
   // shared experts: one dense segment of all S tokens, weight 1
   void* dxs = nullptr;
@@ -595,12 +604,9 @@ int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, c
     s.Wt_out_packed = Wst_out_packed; s.dy_rows = dy; s.w = nullptr; s.h = fw + p.L.h_shared;
     s.dh = w + B.dhs; s.dab = w + B.dabs; s.gpart = nullptr; s.dx_rows = w + B.dxs;
     if ((rc = ffn_backward_data(c, s, status, stream)) != MOE_OK) return rc;
-    int32_t* poff_s = reinterpret_cast<int32_t*>(w + B.poff_s);
-    if ((rc = launch_pad_offsets(nullptr, 1, c.S, poff_s, stream)) != MOE_OK) return rc;
-    const T tss[4] = {{dy, c.M, nullptr, nullptr, c.M, B.dyTs},
+    const T tss[3] = {{dy, c.M, nullptr, nullptr, c.M, B.dyTs},
                       {fw + p.L.h_shared, Hc, nullptr, nullptr, Hc, B.hsT},
-                      {w + B.dabs, Fs, nullptr, nullptr, Fs, B.dabsT},
-                      {x, c.M, nullptr, nullptr, c.M, B.xTs}};
+                      {w + B.dabs, Fs, nullptr, nullptr, Fs, B.dabsT}};
     for (const T& t : tss)
       if ((rc = launch_seg_transpose(t.in, t.ld, nullptr, 1, c.S, poff_s, B.Sp, nullptr, c.S,
                                      nullptr, t.C, w + t.out, B.Sp, status, stream)) != MOE_OK)

@@ -164,7 +164,8 @@ __global__ void __launch_bounds__(256)
     router_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ expert_id,
                       const int32_t* __restrict__ row, const float* __restrict__ gpart, int n_tiles,
                       const int32_t* __restrict__ counts_routed, int S, int G, int E, int k,
-                      int gate_norm, float aux_coef, float z_coef, float* __restrict__ dlogits) {
+                      int gate_norm, float aux_coef, float z_coef, float* __restrict__ dlogits,
+                      __nv_bfloat16* __restrict__ dlb, int Ep) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -262,89 +263,32 @@ __global__ void __launch_bounds__(256)
     for (int q = 0; q < 8; ++q) dl[q] += c * p[q];
   }
   float* out = dlogits + int64_t(t) * E;
+  __nv_bfloat16* outb = dlb + int64_t(t) * Ep;  // bf16, zero-padded to Ep: the GEMMs' operand
 #pragma unroll
-  for (int q = 0; q < 8; ++q)
-    if (lane + 32 * q < E) out[lane + 32 * q] = dl[q];
+  for (int q = 0; q < 8; ++q) {
+    const int e = lane + 32 * q;
+    if (e < E) out[e] = dl[q];
+    if (e < Ep) outb[e] = __float2bfloat16_rn(e < E ? dl[q] : 0.f);
+  }
 }
 
-// dx_r[t][m] = sum_e dl[t][e] W_g[e][m] (fp32): a block takes 8 tokens x 256 columns.
-__global__ void __launch_bounds__(256)
-    router_dx_kernel(const float* __restrict__ dl, const __nv_bfloat16* __restrict__ W_g, int S,
-                     int E, int M, float* __restrict__ dx) {
-  __shared__ float s_dl[8][256];
+// dbias[e] = sum over tokens of dl[t][e]: 32 experts a block, 32 token lanes each summing a
+// strided subset in order, then the lanes in order.
+__global__ void __launch_bounds__(1024)
+    colsum_kernel(const float* __restrict__ dl, int S, int E, float* __restrict__ out) {
+  __shared__ float s_part[32][33];
   pdl_wait();
   pdl_trigger();
-  const int t0 = blockIdx.y * 8, m = blockIdx.x * 256 + threadIdx.x;
-  for (int i = threadIdx.x; i < 8 * E; i += 256) {
-    const int tt = i / E, e = i % E;
-    s_dl[tt][e] = t0 + tt < S ? dl[int64_t(t0 + tt) * E + e] : 0.f;
-  }
+  const int ex = threadIdx.x & 31, tl = threadIdx.x >> 5, e = blockIdx.x * 32 + ex;
+  float acc = 0.f;
+  if (e < E)
+    for (int t = tl; t < S; t += 32) acc += dl[int64_t(t) * E + e];
+  s_part[tl][ex] = acc;
   __syncthreads();
-  if (m >= M) return;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int e = 0; e < E; ++e) {
-    const float w = __bfloat162float(W_g[int64_t(e) * M + m]);
-#pragma unroll
-    for (int tt = 0; tt < 8; ++tt) acc[tt] += s_dl[tt][e] * w;
-  }
-#pragma unroll
-  for (int tt = 0; tt < 8; ++tt)
-    if (t0 + tt < S) dx[int64_t(t0 + tt) * M + m] = acc[tt];
-}
-
-// part[ch][e][m] = sum over the chunk's 256 tokens of dl[t][e] x[t][m]; a block takes 128
-// columns x 32 experts of one chunk.
-__global__ void __launch_bounds__(128)
-    router_dw_partial_kernel(const float* __restrict__ dl, const __nv_bfloat16* __restrict__ x, int S,
-                             int E, int M, float* __restrict__ part) {
-  __shared__ float s_dl[256][33];
-  pdl_wait();
-  pdl_trigger();
-  const int m = blockIdx.x * 128 + threadIdx.x, e0 = blockIdx.y * 32, ch = blockIdx.z;
-  const int t0 = ch * 256;
-  for (int i = threadIdx.x; i < 256 * 32; i += 128) {
-    const int tt = i / 32, q = i % 32;
-    s_dl[tt][q] = (t0 + tt < S && e0 + q < E) ? dl[int64_t(t0 + tt) * E + e0 + q] : 0.f;
-  }
-  __syncthreads();
-  const int n = min(256, S - t0);
-  if (blockIdx.x == 0 && threadIdx.x < 32 && e0 + threadIdx.x < E) {  // the bias column
-    float b = 0.f;
-    for (int tt = 0; tt < n; ++tt) b += s_dl[tt][threadIdx.x];
-    part[int64_t(gridDim.z) * E * M + int64_t(ch) * E + e0 + threadIdx.x] = b;
-  }
-  if (m >= M) return;
-  float acc[32];
-#pragma unroll
-  for (int q = 0; q < 32; ++q) acc[q] = 0.f;
-  for (int tt = 0; tt < n; ++tt) {
-    const float xv = __bfloat162float(x[int64_t(t0 + tt) * M + m]);
-#pragma unroll
-    for (int q = 0; q < 32; ++q) acc[q] += s_dl[tt][q] * xv;
-  }
-#pragma unroll
-  for (int q = 0; q < 32; ++q)
-    if (e0 + q < E) part[(int64_t(ch) * E + e0 + q) * M + m] = acc[q];
-}
-
-// dW_g[e][m] = sum over chunks in order of part[ch][e][m]; dbias[e] likewise over the bias
-// partials (part[nch][E][M] is followed by [nch][E] sums of dl over each chunk's tokens).
-__global__ void __launch_bounds__(256)
-    router_dw_reduce_kernel(const float* __restrict__ part, int nch, int E, int M,
-                            float* __restrict__ dW, float* __restrict__ dbias) {
-  pdl_wait();
-  pdl_trigger();
-  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i < int64_t(E) * M) {
-    float acc = 0.f;
-    for (int ch = 0; ch < nch; ++ch) acc += part[int64_t(ch) * E * M + i];
-    dW[i] = acc;
-  }
-  if (dbias && i < E) {
-    const float* pb = part + int64_t(nch) * E * M;
-    float acc = 0.f;
-    for (int ch = 0; ch < nch; ++ch) acc += pb[int64_t(ch) * E + i];
-    dbias[i] = acc;
+  if (tl == 0 && e < E) {
+    float sum = 0.f;
+    for (int i = 0; i < 32; ++i) sum += s_part[i][ex];
+    out[e] = sum;
   }
 }
 
@@ -385,33 +329,49 @@ int launch_pack_transposed(int mode, int swiglu, int groups, int N, int K, int M
 
 int launch_router_backward(const moe_config_t& c, const float* logits, const moe_route_out_t& r,
                            const float* gpart, int n_tiles, float aux_coef, float z_coef,
-                           float* dlogits, const void* x, const void* W_g, float* dx_router,
-                           float* dW_g, float* dbias, float* part, cudaStream_t st) {
+                           const RouterBwdBufs& b, const void* x, const void* W_g, float* dW_g,
+                           float* dbias, unsigned* status, cudaStream_t st) {
   if (c.E > 256) return MOE_ERR_UNSUPPORTED;
+  const int Ep = (c.E + 63) / 64 * 64;
   const unsigned blocks = unsigned((int64_t(c.S) * 32 + 255) / 256);
   int rc;
   if (c.k <= 2)
     rc = launch_kernel(router_bwd_kernel<2>, dim3(blocks), dim3(256), 0, st, logits, r.expert_id, r.row,
                        gpart, n_tiles, r.counts_routed, c.S, c.G, c.E, c.k, c.gate_norm, aux_coef,
-                       z_coef, dlogits);
+                       z_coef, b.dlogits, static_cast<__nv_bfloat16*>(b.dlb), Ep);
   else
     rc = launch_kernel(router_bwd_kernel<8>, dim3(blocks), dim3(256), 0, st, logits, r.expert_id, r.row,
                        gpart, n_tiles, r.counts_routed, c.S, c.G, c.E, c.k, c.gate_norm, aux_coef,
-                       z_coef, dlogits);
+                       z_coef, b.dlogits, static_cast<__nv_bfloat16*>(b.dlb), Ep);
   if (rc != MOE_OK) return rc;
-  auto xb = static_cast<const __nv_bfloat16*>(x);
-  auto wg = static_cast<const __nv_bfloat16*>(W_g);
-  rc = launch_kernel(router_dx_kernel, dim3(unsigned((c.M + 255) / 256), unsigned((c.S + 7) / 8)),
-                     dim3(256), 0, st, static_cast<const float*>(dlogits), wg, c.S, c.E, c.M, dx_router);
-  if (rc != MOE_OK) return rc;
-  const int nch = (c.S + 255) / 256;
-  rc = launch_kernel(router_dw_partial_kernel,
-                     dim3(unsigned((c.M + 127) / 128), unsigned((c.E + 31) / 32), unsigned(nch)),
-                     dim3(128), 0, st, static_cast<const float*>(dlogits), xb, c.S, c.E, c.M, part);
-  if (rc != MOE_OK) return rc;
-  return launch_kernel(router_dw_reduce_kernel,
-                       dim3(unsigned((int64_t(c.E) * c.M + 255) / 256)), dim3(256), 0, st,
-                       static_cast<const float*>(part), nch, c.E, c.M, dW_g, dbias);
+  // K ranges of the two router GEMMs: [0, Ep) and [0, Sp)
+  if ((rc = launch_pad_offsets(nullptr, 1, c.E, b.koff_e, st)) != MOE_OK) return rc;
+  if ((rc = launch_pad_offsets(nullptr, 1, c.S, b.koff_s, st)) != MOE_OK) return rc;
+  // W_g^T [M][Ep] and dl^T [Ep][Sp] (zero-padded), x^T [M][Sp] is the caller's
+  if ((rc = launch_seg_transpose(W_g, c.M, nullptr, 1, c.E, b.koff_e, Ep, nullptr, c.E, nullptr, c.M,
+                                 b.wgT, Ep, status, st)) != MOE_OK)
+    return rc;
+  if ((rc = launch_seg_transpose(b.dlb, Ep, nullptr, 1, c.S, b.koff_s, b.Sp, nullptr, c.S, nullptr, Ep,
+                                 b.dlT, b.Sp, status, st)) != MOE_OK)
+    return rc;
+  // dx_r [S][M] = dl . W_g (one group of S rows, K = Ep); dW_g [E][M] = dl^T . x (K = Sp)
+  GemmDesc d;
+  d.epi = EPI_F32_BIAS;
+  d.A = b.dlb; d.a_rows = c.S; d.K = Ep;
+  d.B = b.wgT; d.N = c.M; d.b_rows = c.M; d.b_tiled = false;
+  d.koffs = b.koff_e; d.c1 = c.S; d.groups = 1;
+  d.out = b.dx_r; d.ldo = c.M; d.n_valid = c.M; d.status = status;
+  if ((rc = launch_gemm_bf16(d, st)) != MOE_OK) return rc;
+  GemmDesc w;
+  w.epi = EPI_F32_BIAS;
+  w.A = b.dlT; w.a_rows = c.E; w.K = int(b.Sp);
+  w.B = b.xT; w.N = c.M; w.b_rows = c.M; w.b_tiled = false;
+  w.koffs = b.koff_s; w.c1 = c.E; w.groups = 1;
+  w.out = dW_g; w.ldo = c.M; w.n_valid = c.M; w.status = status;
+  if ((rc = launch_gemm_bf16(w, st)) != MOE_OK) return rc;
+  if (!dbias) return MOE_OK;
+  return launch_kernel(colsum_kernel, dim3(unsigned((c.E + 31) / 32)), dim3(1024), 0, st,
+                       static_cast<const float*>(b.dlogits), c.S, c.E, dbias);
 }
 
 }  // namespace moe

@@ -56,7 +56,7 @@ constexpr int BK = 64;  // bf16 elements per 128-byte swizzled row
 constexpr int kThreads = 192;
 constexpr int kMaxGroups = 256;
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, bool KRAG = false>
 struct Cfg {
   static constexpr int CTAS = PAIR ? 2 : 1;
   static constexpr int TILE_M = BM * CTAS;  // rows of one output tile
@@ -64,10 +64,14 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);
+  // K-ragged mode: the fp32 epilogue stages 32 x 32 values per warp in shared memory
+  static constexpr int STG_FLOATS = KRAG ? 4 * 32 * 33 : 0;
+  static constexpr int STAGES = ((196608 - STG_FLOATS * 4) / STAGE_BYTES) > 8
+                                    ? 8 : ((196608 - STG_FLOATS * 4) / STAGE_BYTES);
   static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + 16 + 3 * (kMaxGroups + 1) * 4;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + 16 + 3 * (kMaxGroups + 1) * 4 +
+                              STG_FLOATS * 4;
 };
 
 struct KParams {
@@ -251,12 +255,56 @@ __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, 
   }
 }
 
+// K-ragged mode's fp32 epilogue: warp rows grow0 .. grow0 + 31 (the first nvr valid), the
+// accumulator staged 32 columns at a time through shared memory (stg: [32][33] floats) so
+// that each row is stored as whole 128-byte lines (8 lanes a row, 4 rows a store) instead
+// of one 16-byte piece per lane and row.
+template <int BN>
+__device__ __forceinline__ void epilogue_f32_staged(const KParams& p, uint32_t tbase, int64_t grow0,
+                                                    int nvr, int nt, bool zero, float* stg,
+                                                    int lane) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    uint32_t v0[16], v1[16];
+    tmem_ld16(tbase + c0, v0);
+    tmem_ld16(tbase + c0 + 16, v1);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      stg[lane * 33 + j] = zero ? 0.f : __uint_as_float(v0[j]);
+      stg[lane * 33 + 16 + j] = zero ? 0.f : __uint_as_float(v1[j]);
+    }
+    __syncwarp();
+    const int cl = (lane & 7) * 4, col = nt * BN + c0 + cl;
+#pragma unroll 1
+    for (int pass = 0; pass < 8; ++pass) {
+      const int rr = pass * 4 + (lane >> 3);
+      if (rr < nvr && col < p.n_valid) {
+        const int64_t grow = grow0 + rr;
+        float* out = static_cast<float*>(p.out) + grow * p.ldo;
+        if (p.out2) {  // interleaved SwiGLU rows: 128 to out, the next 128 to out2
+          const int64_t g = grow / p.c1, j = grow % p.c1, c = j & 255;
+          out = static_cast<float*>(c < 128 ? p.out : p.out2) +
+                (g * (p.c1 / 2) + (j >> 8) * 128 + (c & 127)) * p.ldo;
+        }
+        const float* sv = stg + rr * 33 + cl;
+        if (col + 4 <= p.n_valid) {
+          *reinterpret_cast<float4*>(out + col) = make_float4(sv[0], sv[1], sv[2], sv[3]);
+        } else {
+          for (int i = 0; col + i < p.n_valid; ++i) out[col + i] = sv[i];
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // ------------------------------------------------------------------ the kernel
 template <int BN, int EPI, bool PAIR, bool KRAG>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const KParams p) {
-  using C = Cfg<BN, PAIR>;
+  using C = Cfg<BN, PAIR, KRAG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -269,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_tstart = reinterpret_cast<int*>(s_tmem + 4);  // [groups+1] first m-tile of each group
   int* s_off = s_tstart + (kMaxGroups + 1);            // [groups+1] first row of each group
   int* s_koff = s_off + (kMaxGroups + 1);              // K-ragged: [groups+1] K offsets
+  float* s_stg = reinterpret_cast<float*>(s_koff + (kMaxGroups + 1));  // K-ragged: [4][32][33]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars);
@@ -492,7 +541,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = int(rank) * BM + q * 32 + lane;  // row within the tile
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
       const bool zero = KRAG && s_koff[g + 1] == s_koff[g];  // no MMA ran for this tile
-      epilogue_rows<BN, EPI>(p, tbase, r < rows, int64_t(m0) + r, nt, zero);
+      if constexpr (KRAG && EPI == EPI_F32_BIAS) {
+        const int r0 = int(rank) * BM + q * 32;  // this warp's first row in the tile
+        const int nvr = rows - r0 < 0 ? 0 : (rows - r0 > 32 ? 32 : rows - r0);
+        epilogue_f32_staged<BN>(p, tbase, int64_t(m0) + r0, nvr, nt, zero, s_stg + q * 32 * 33, lane);
+      } else {
+        epilogue_rows<BN, EPI>(p, tbase, r < rows, int64_t(m0) + r, nt, zero);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -560,7 +615,7 @@ int make_map_tiled(CUtensorMap* m, const void* base, int64_t blocks, int block_r
 
 template <int BN, int EPI, bool PAIR, bool KRAG = false>
 int run_gemm(const GemmDesc& d, cudaStream_t st) {
-  using C = Cfg<BN, PAIR>;
+  using C = Cfg<BN, PAIR, KRAG>;
   CUtensorMap ta, tb;
   if (KRAG && (!d.koffs || d.c1 < 1 || d.b_tiled || d.groups < 1)) return MOE_ERR_INVALID_ARG;
   int rc = make_map(&ta, d.A, KRAG ? d.c1 : d.a_rows, d.K, BM);

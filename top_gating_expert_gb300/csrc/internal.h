@@ -75,10 +75,9 @@ inline WsLayout ws_layout(const moe_config_t& c, int C) {
 struct WsLayoutBwd {
   int64_t Rp = 0, Sp = 0;
   int n_tiles2 = 0;  // N tiles of the backward GEMM 2 (gate-partial stride)
-  int nch = 0;       // 256-token chunks of the router's weight gradient
   size_t status = 0, dy_perm = 0, dh = 0, dab = 0, gpart = 0, dx_perm = 0, poff = 0, poff_s = 0,
-         dyT = 0, hT = 0, dabT = 0, xT = 0, dlogits = 0, dx_r = 0, part = 0, dhs = 0, dabs = 0,
-         dxs = 0, dyTs = 0, hsT = 0, dabsT = 0, xTs = 0;
+         dyT = 0, hT = 0, dabT = 0, xT = 0, dlogits = 0, dx_r = 0, dlb = 0, dlT = 0, wgT = 0,
+         koff_e = 0, dhs = 0, dabs = 0, dxs = 0, dyTs = 0, hsT = 0, dabsT = 0, xTs = 0;
   size_t bytes = 0;
 };
 
@@ -118,7 +117,6 @@ inline WsLayoutBwd ws_layout_bwd(const moe_config_t& c, int C) {
   B.Sp = (int64_t(c.S) + 63) / 64 * 64;
   const int bn2 = gemm_bn(c.H, EPI_DGRAD2);
   B.n_tiles2 = bn2 > 0 ? c.H / bn2 : 1;
-  B.nch = (c.S + 255) / 256;
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t at = o; o = align256(o + bytes); return at; };
   B.status = take(256);
@@ -135,14 +133,18 @@ inline WsLayoutBwd ws_layout_bwd(const moe_config_t& c, int C) {
   B.xT = take(size_t(c.M) * B.Rp * 2);
   B.dlogits = take(size_t(c.S) * c.E * 4);
   B.dx_r = take(size_t(c.S) * c.M * 4);
-  B.part = take((size_t(B.nch) * c.E * c.M + size_t(B.nch) * c.E) * 4);
+  const size_t Ep = (size_t(c.E) + 63) / 64 * 64;
+  B.dlb = take(size_t(c.S) * Ep * 2);
+  B.dlT = take(Ep * B.Sp * 2);
+  B.wgT = take(size_t(c.M) * Ep * 2);
+  B.koff_e = take(2 * 4);
   B.dhs = take(sw ? size_t(c.S) * Hc * 2 : 0);
   B.dabs = take(size_t(c.S) * Fs * 2);
   B.dxs = take(Hc ? size_t(c.S) * c.M * 2 : 0);
   B.dyTs = take(Hc ? size_t(c.M) * B.Sp * 2 : 0);
   B.hsT = take(size_t(Hc) * B.Sp * 2);
   B.dabsT = take(size_t(Fs) * B.Sp * 2);
-  B.xTs = take(Hc ? size_t(c.M) * B.Sp * 2 : 0);
+  B.xTs = take(size_t(c.M) * B.Sp * 2);  // x^T: the router's dW_g and the shared experts
   B.bytes = o;
   return B;
 }
@@ -226,10 +228,21 @@ int launch_seg_transpose(const void* in, int64_t ld_in, const int32_t* offsets, 
                          int64_t ld_out, unsigned* status, cudaStream_t st);
 int launch_pack_transposed(int mode, int swiglu, int groups, int N, int K, int M, int Hp, int parts,
                            const void* W, const void* W2, void* dst, cudaStream_t st);
+// the router backward's scratch (all in the backward workspace)
+struct RouterBwdBufs {
+  float* dlogits;  // [S][E] fp32
+  void* dlb;       // [S][Ep] bf16, Ep = E rounded up to 64
+  void* dlT;       // [Ep][Sp] bf16
+  void* wgT;       // [M][Ep] bf16
+  const void* xT;  // [M][Sp] bf16 (x transposed, the caller's)
+  float* dx_r;     // [S][M] fp32
+  int32_t* koff_e; int32_t* koff_s;  // [2] each
+  int64_t Sp;
+};
 int launch_router_backward(const moe_config_t& c, const float* logits, const moe_route_out_t& r,
                            const float* gpart, int n_tiles, float aux_coef, float z_coef,
-                           float* dlogits, const void* x, const void* W_g, float* dx_router,
-                           float* dW_g, float* dbias, float* part, cudaStream_t st);
+                           const RouterBwdBufs& b, const void* x, const void* W_g, float* dW_g,
+                           float* dbias, unsigned* status, cudaStream_t st);
 
 int num_sms();
 
