@@ -64,14 +64,15 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  // K-ragged mode: the fp32 epilogue stages 32 x 32 values per warp in shared memory
-  static constexpr int STG_FLOATS = KRAG ? 4 * 32 * 33 : 0;
-  static constexpr int STAGES = ((196608 - STG_FLOATS * 4) / STAGE_BYTES) > 8
-                                    ? 8 : ((196608 - STG_FLOATS * 4) / STAGE_BYTES);
+  // K-ragged mode: each epilogue warp stages 32 x 32 fp32 outputs in two 4 KB buffers that
+  // TMA stores to global memory
+  static constexpr int STG_BYTES = KRAG ? 4 * 2 * 4096 : 0;
+  static constexpr int STAGES = ((196608 - STG_BYTES) / STAGE_BYTES) > 8
+                                    ? 8 : ((196608 - STG_BYTES) / STAGE_BYTES);
   static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + 16 + 3 * (kMaxGroups + 1) * 4 +
-                              STG_FLOATS * 4;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + STG_BYTES + BAR_BYTES + 16 +
+                              3 * (kMaxGroups + 1) * 4;
 };
 
 struct KParams {
@@ -255,47 +256,67 @@ __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, 
   }
 }
 
-// K-ragged mode's fp32 epilogue: warp rows grow0 .. grow0 + 31 (the first nvr valid), the
-// accumulator staged 32 columns at a time through shared memory (stg: [32][33] floats) so
-// that each row is stored as whole 128-byte lines (8 lanes a row, 4 rows a store) instead
-// of one 16-byte piece per lane and row.
+// K-ragged mode's fp32 epilogue for one warp: rows grow0 .. grow0 + 31 (the first nvr valid),
+// 32 columns at a time: lanes write their row into a 128-byte-swizzled 32 x 32 staging
+// buffer (conflict-free), fence it for the async proxy, and lane 0 stores it with one TMA
+// tensor store (two buffers alternate; a buffer is rewritten once its earlier store has
+// read it). A warp whose rows end inside it (the last rows of a one-group output) stores
+// its valid rows from the buffer with plain stores instead.
 template <int BN>
-__device__ __forceinline__ void epilogue_f32_staged(const KParams& p, uint32_t tbase, int64_t grow0,
-                                                    int nvr, int nt, bool zero, float* stg,
-                                                    int lane) {
+__device__ __forceinline__ void epilogue_f32_tma(const KParams& p, const CUtensorMap* tmO,
+                                                 const CUtensorMap* tmO2, uint32_t tbase,
+                                                 int64_t grow0, int nvr, int nt, bool zero,
+                                                 uint8_t* bufs, int lane, int& nb) {
+  const CUtensorMap* map = tmO;
+  int64_t orow = grow0;
+  float* out0 = static_cast<float*>(p.out);
+  if (p.out2) {  // interleaved SwiGLU rows: 128 to out, the next 128 to out2 (32-row aligned)
+    const int64_t g = grow0 / p.c1, j = grow0 % p.c1, c = j & 255;
+    orow = g * (p.c1 / 2) + (j >> 8) * 128 + (c & 127);
+    if (c >= 128) {
+      map = tmO2;
+      out0 = static_cast<float*>(p.out2);
+    }
+  }
 #pragma unroll 1
   for (int c0 = 0; c0 < BN; c0 += 32) {
     uint32_t v0[16], v1[16];
     tmem_ld16(tbase + c0, v0);
     tmem_ld16(tbase + c0 + 16, v1);
     tmem_ld_wait();
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      stg[lane * 33 + j] = zero ? 0.f : __uint_as_float(v0[j]);
-      stg[lane * 33 + 16 + j] = zero ? 0.f : __uint_as_float(v1[j]);
-    }
+    uint8_t* buf = bufs + nb * 4096;
+    if (lane == 0) bulk_wait_read<1>();
     __syncwarp();
-    const int cl = (lane & 7) * 4, col = nt * BN + c0 + cl;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t* v = c < 4 ? v0 + 4 * c : v1 + 4 * (c - 4);
+      const float4 f = zero ? make_float4(0.f, 0.f, 0.f, 0.f)
+                            : make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]),
+                                          __uint_as_float(v[2]), __uint_as_float(v[3]));
+      *reinterpret_cast<float4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) = f;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    const int col = nt * BN + c0;
+    if (nvr == 32) {
+      if (lane == 0 && col < p.n_valid) {
+        tma_store_2d(map, col, int(orow), smem_u32(buf));
+        bulk_commit();
+      }
+    } else if (nvr > 0) {
+      const int cl = (lane & 7) * 4;
 #pragma unroll 1
-    for (int pass = 0; pass < 8; ++pass) {
-      const int rr = pass * 4 + (lane >> 3);
-      if (rr < nvr && col < p.n_valid) {
-        const int64_t grow = grow0 + rr;
-        float* out = static_cast<float*>(p.out) + grow * p.ldo;
-        if (p.out2) {  // interleaved SwiGLU rows: 128 to out, the next 128 to out2
-          const int64_t g = grow / p.c1, j = grow % p.c1, c = j & 255;
-          out = static_cast<float*>(c < 128 ? p.out : p.out2) +
-                (g * (p.c1 / 2) + (j >> 8) * 128 + (c & 127)) * p.ldo;
-        }
-        const float* sv = stg + rr * 33 + cl;
-        if (col + 4 <= p.n_valid) {
-          *reinterpret_cast<float4*>(out + col) = make_float4(sv[0], sv[1], sv[2], sv[3]);
-        } else {
-          for (int i = 0; col + i < p.n_valid; ++i) out[col + i] = sv[i];
+      for (int pass = 0; pass < 8; ++pass) {
+        const int rr = pass * 4 + (lane >> 3);
+        if (rr < nvr && col + cl < p.n_valid) {
+          const float* sv = reinterpret_cast<const float*>(buf + rr * 128 + (((cl >> 2) ^ (rr & 7)) << 4));
+          float* out = out0 + (orow + rr) * p.ldo + col + cl;
+          for (int i = 0; i < 4 && col + cl + i < p.n_valid; ++i) out[i] = sv[i];
         }
       }
     }
     __syncwarp();
+    nb ^= 1;
   }
 }
 
@@ -303,21 +324,24 @@ __device__ __forceinline__ void epilogue_f32_staged(const KParams& p, uint32_t t
 template <int BN, int EPI, bool PAIR, bool KRAG>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const KParams p) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmO,   // K-ragged: fp32 output
+                        const __grid_constant__ CUtensorMap tmO2,  // K-ragged: second output
+                        const KParams p) {
   using C = Cfg<BN, PAIR, KRAG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + C::STAGES * C::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+  uint8_t* sStg = sB + C::STAGES * C::B_BYTES;  // K-ragged: [4 warps][2][32 rows][128 B], swizzled
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + C::STG_BYTES);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_total = reinterpret_cast<int*>(s_tmem + 2);
   int* s_tstart = reinterpret_cast<int*>(s_tmem + 4);  // [groups+1] first m-tile of each group
   int* s_off = s_tstart + (kMaxGroups + 1);            // [groups+1] first row of each group
   int* s_koff = s_off + (kMaxGroups + 1);              // K-ragged: [groups+1] K offsets
-  float* s_stg = reinterpret_cast<float*>(s_koff + (kMaxGroups + 1));  // K-ragged: [4][32][33]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars);
@@ -529,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue warps 2..5
     const int q = warp & 3;  // TMEM lanes 32q..32q+31 = this CTA's tile rows
     const uint32_t tempty_leader = PAIR ? cluster_addr(tempty0, 0) : tempty0;
+    int stg_buf = 0;  // K-ragged: the staging buffer the next 32 columns go to
     int i = 0;
     for (int t = unit; t < total; t += units, ++i) {
       const int acc = i & 1;
@@ -544,7 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (KRAG && EPI == EPI_F32_BIAS) {
         const int r0 = int(rank) * BM + q * 32;  // this warp's first row in the tile
         const int nvr = rows - r0 < 0 ? 0 : (rows - r0 > 32 ? 32 : rows - r0);
-        epilogue_f32_staged<BN>(p, tbase, int64_t(m0) + r0, nvr, nt, zero, s_stg + q * 32 * 33, lane);
+        epilogue_f32_tma<BN>(p, &tmO, &tmO2, tbase, int64_t(m0) + r0, nvr, nt, zero,
+                             sStg + q * 2 * 4096, lane, stg_buf);
       } else {
         epilogue_rows<BN, EPI>(p, tbase, r < rows, int64_t(m0) + r, nt, zero);
       }
@@ -555,6 +581,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         else mbar_arrive(tempty0 + 8 * acc);
       }
     }
+    // K-ragged: every TMA store has finished before the CTA's shared memory goes away
+    if constexpr (KRAG && EPI == EPI_F32_BIAS)
+      if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -597,6 +626,22 @@ int make_map(CUtensorMap* m, const void* base, int64_t rows, int K, int box_rows
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// 2-D fp32 tensor map over a row-major [rows, N] output, 32 x 32 boxes, 128-byte swizzle
+// (the K-ragged epilogue's TMA stores).
+int make_map_f32_out(CUtensorMap* m, void* base, int64_t rows, int N) {
+  auto fn = encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || (int64_t(N) * 4) % 16 != 0) return MOE_ERR_INVALID_ARG;
+  cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(N) * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
 // 3-D bf16 tensor map over a tile-major packed matrix: `blocks` contiguous [block_rows][64]
 // blocks; a box is box_rows rows (all of a block, or half of it for a CTA pair).
 int make_map_tiled(CUtensorMap* m, const void* base, int64_t blocks, int block_rows, int box_rows) {
@@ -628,6 +673,15 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
     rc = make_map(&tb, d.B, d.b_rows, d.K, BN);
   }
   if (rc != MOE_OK) return rc;
+  CUtensorMap to, to2;  // K-ragged: the fp32 outputs, 32 x 32 boxes, 128-byte swizzle
+  memset(&to, 0, sizeof(to));
+  memset(&to2, 0, sizeof(to2));
+  if constexpr (KRAG) {
+    if (d.epi != EPI_F32_BIAS || d.ldo != d.N) return MOE_ERR_UNSUPPORTED;
+    const int64_t out_rows = int64_t(d.groups) * d.c1 / (d.out2 ? 2 : 1);
+    if ((rc = make_map_f32_out(&to, d.out, out_rows, d.N)) != MOE_OK) return rc;
+    if (d.out2 && (rc = make_map_f32_out(&to2, d.out2, out_rows, d.N)) != MOE_OK) return rc;
+  }
   KParams p;
   p.b_tiled = d.b_tiled ? 1 : 0;
   p.offsets = d.offsets;
@@ -685,7 +739,7 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
     lc.attrs = attr;
     lc.numAttrs += 1;
   }
-  MOE_CUDA_CHECK(cudaLaunchKernelEx(&lc, kern, ta, tb, p));
+  MOE_CUDA_CHECK(cudaLaunchKernelEx(&lc, kern, ta, tb, to, to2, p));
   return MOE_OK;
 }
 
