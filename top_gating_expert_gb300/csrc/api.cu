@@ -590,6 +590,9 @@ int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, c
   rb.dlb = w + B.dlb; rb.dlT = w + B.dlT; rb.wgT = w + B.wgT; rb.xT = w + B.xTs;
   rb.dx_r = reinterpret_cast<float*>(w + B.dx_r);
   rb.koff_e = reinterpret_cast<int32_t*>(w + B.koff_e); rb.koff_s = poff_s; rb.Sp = B.Sp;
+  rb.koff_split = reinterpret_cast<int32_t*>(w + B.koff_split);
+  rb.dwg_part = reinterpret_cast<float*>(w + B.dwg_part);
+  rb.max_split = WsLayoutBwd::kMaxSplit;
   if ((rc = launch_router_backward(c, logits, *r, reinterpret_cast<const float*>(w + B.gpart),
                                    B.n_tiles2, aux_coef, z_coef, rb, x, W_g, grads->dW_g,
                                    grads->dbias, status, stream)) != MOE_OK)

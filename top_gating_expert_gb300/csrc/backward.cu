@@ -292,6 +292,25 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
+// koffs[i] = min(total, i * chunk) for i = 0..n: split-K ranges of one K-ragged GEMM.
+__global__ void split_offsets_kernel(int n, int chunk, int total, int32_t* __restrict__ koffs) {
+  pdl_wait();
+  pdl_trigger();
+  for (int i = threadIdx.x; i <= n; i += blockDim.x) koffs[i] = min(total, i * chunk);
+}
+
+// out[i] = sum over s = 0..n-1, in order, of part[s * len + i] (split-K partials).
+__global__ void __launch_bounds__(256)
+    sum_partials_kernel(const float* __restrict__ part, int n, int64_t len, float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= len) return;
+  float acc = 0.f;
+  for (int s = 0; s < n; ++s) acc += part[int64_t(s) * len + i];
+  out[i] = acc;
+}
+
 }  // namespace
 
 int launch_pad_offsets(const int32_t* offsets, int groups, int dense_rows, int32_t* poff,
@@ -362,13 +381,29 @@ int launch_router_backward(const moe_config_t& c, const float* logits, const moe
   d.koffs = b.koff_e; d.c1 = c.S; d.groups = 1;
   d.out = b.dx_r; d.ldo = c.M; d.n_valid = c.M; d.status = status;
   if ((rc = launch_gemm_bf16(d, st)) != MOE_OK) return rc;
+  // dW_g: K = Sp split into nsplit ranges (one output tile per 128 experts x 256 columns
+  // would otherwise leave most SMs idle over a long K), partials summed in order
+  const int64_t kblk = b.Sp / 64;
+  const int tiles = ((c.E + 127) / 128) * ((c.M + 255) / 256);
+  int nsplit = (2 * num_sms() + tiles - 1) / tiles;
+  if (nsplit > b.max_split) nsplit = b.max_split;
+  if (nsplit > kblk) nsplit = int(kblk);
+  if (nsplit < 1) nsplit = 1;
+  const int chunk = int((kblk + nsplit - 1) / nsplit) * 64;
+  if ((rc = launch_kernel(split_offsets_kernel, dim3(1), dim3(64), 0, st, nsplit, chunk, int(b.Sp),
+                          b.koff_split)) != MOE_OK)
+    return rc;
   GemmDesc w;
   w.epi = EPI_F32_BIAS;
   w.A = b.dlT; w.a_rows = c.E; w.K = int(b.Sp);
   w.B = b.xT; w.N = c.M; w.b_rows = c.M; w.b_tiled = false;
-  w.koffs = b.koff_s; w.c1 = c.E; w.groups = 1;
-  w.out = dW_g; w.ldo = c.M; w.n_valid = c.M; w.status = status;
+  w.koffs = b.koff_split; w.c1 = c.E; w.groups = nsplit;
+  w.out = b.dwg_part; w.ldo = c.M; w.n_valid = c.M; w.status = status;
   if ((rc = launch_gemm_bf16(w, st)) != MOE_OK) return rc;
+  const int64_t len = int64_t(c.E) * c.M;
+  if ((rc = launch_kernel(sum_partials_kernel, dim3(unsigned((len + 255) / 256)), dim3(256), 0, st,
+                          static_cast<const float*>(b.dwg_part), nsplit, len, dW_g)) != MOE_OK)
+    return rc;
   if (!dbias) return MOE_OK;
   return launch_kernel(colsum_kernel, dim3(unsigned((c.E + 31) / 32)), dim3(1024), 0, st,
                        static_cast<const float*>(b.dlogits), c.S, c.E, dbias);

@@ -77,7 +77,9 @@ struct WsLayoutBwd {
   int n_tiles2 = 0;  // N tiles of the backward GEMM 2 (gate-partial stride)
   size_t status = 0, dy_perm = 0, dh = 0, dab = 0, gpart = 0, dx_perm = 0, poff = 0, poff_s = 0,
          dyT = 0, hT = 0, dabT = 0, xT = 0, dlogits = 0, dx_r = 0, dlb = 0, dlT = 0, wgT = 0,
-         koff_e = 0, dhs = 0, dabs = 0, dxs = 0, dyTs = 0, hsT = 0, dabsT = 0, xTs = 0;
+         koff_e = 0, koff_split = 0, dwg_part = 0, dhs = 0, dabs = 0, dxs = 0, dyTs = 0, hsT = 0,
+         dabsT = 0, xTs = 0;
+  static constexpr int kMaxSplit = 64;  // split-K ranges of the router's dW_g
   size_t bytes = 0;
 };
 
@@ -138,6 +140,8 @@ inline WsLayoutBwd ws_layout_bwd(const moe_config_t& c, int C) {
   B.dlT = take(Ep * B.Sp * 2);
   B.wgT = take(size_t(c.M) * Ep * 2);
   B.koff_e = take(2 * 4);
+  B.koff_split = take((WsLayoutBwd::kMaxSplit + 1) * 4);
+  B.dwg_part = take(size_t(WsLayoutBwd::kMaxSplit) * c.E * c.M * 4);
   B.dhs = take(sw ? size_t(c.S) * Hc * 2 : 0);
   B.dabs = take(size_t(c.S) * Fs * 2);
   B.dxs = take(Hc ? size_t(c.S) * c.M * 2 : 0);
@@ -238,6 +242,9 @@ struct RouterBwdBufs {
   float* dx_r;     // [S][M] fp32
   int32_t* koff_e; int32_t* koff_s;  // [2] each
   int64_t Sp;
+  int32_t* koff_split;  // [max_split + 1]: split-K ranges of dW_g
+  float* dwg_part;      // [max_split][E][M] partials of dW_g
+  int max_split;
 };
 int launch_router_backward(const moe_config_t& c, const float* logits, const moe_route_out_t& r,
                            const float* gpart, int n_tiles, float aux_coef, float z_coef,
