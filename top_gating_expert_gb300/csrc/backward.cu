@@ -36,19 +36,21 @@ __global__ void pad_offsets_kernel(const int32_t* __restrict__ offsets, int grou
 
 // out [C][ld_out] (bf16): column p of group g's padded range is row i = p - poff[g] of the
 // group (rows off[g] + i, or i when dense), zero for i past its rows; the value is
-// scale[r] * in[src(r)][c] with src(r) = gather[r] (or r). A 64 x 64 tile per block through
-// shared memory.
+// scale[r] * in[src(r)][c] with src(r) = gather[r] (or r). A 64 (p) x 64 (c) tile per block:
+// each warp reads 8 rows as 128-byte segments, packs row pairs into 32-bit words
+// T[c][p / 2] (row stride 33 words: conflict-free both ways), and writes 128-byte segments
+// of 64 consecutive p of one output row.
 __global__ void __launch_bounds__(256)
     seg_transpose_kernel(const __nv_bfloat16* __restrict__ in, int64_t ld_in,
                          const int32_t* __restrict__ offsets, int groups, int dense_rows,
                          const int32_t* __restrict__ poff, const int32_t* __restrict__ gather,
                          int src_rows, const float* __restrict__ scale, int C,
                          __nv_bfloat16* __restrict__ out, int64_t ld_out, unsigned* status) {
-  __shared__ __nv_bfloat16 tile[64][72];
+  __shared__ uint32_t T[64][33];
   __shared__ int s_g;
   pdl_wait();
   pdl_trigger();
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int p0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
   if (p0 >= poff[groups]) return;  // past the last padded segment (uniform in the block)
   if (tid == 0) {
@@ -65,12 +67,14 @@ __global__ void __launch_bounds__(256)
   const int base = offsets ? offsets[g] : 0;
   const int n = offsets ? offsets[g + 1] - base : dense_rows;
   const int i0 = p0 - poff[g];
+  // load: row pair pp (rows 2 pp, 2 pp + 1 of the tile), 8 columns cc*8 .. +7
+  const int pp = warp * 4 + (lane >> 3), cc = lane & 7;
+  uint32_t lo16[4], hi16[4];  // rows 2pp and 2pp+1, as 4 bf16 pairs each
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const int rr = tid / 8 + 32 * h, cc = (tid % 8) * 8;
     float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    const int i = i0 + rr;
-    if (i < n && c0 + cc < C) {
+    const int i = i0 + 2 * pp + h;
+    if (i < n && c0 + cc * 8 < C) {
       const int r = base + i;
       int src = gather ? gather[r] : r;
       if (src < 0 || src >= src_rows) {
@@ -78,7 +82,7 @@ __global__ void __launch_bounds__(256)
         src = -1;
       }
       if (src >= 0) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(in + int64_t(src) * ld_in + c0 + cc));
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(in + int64_t(src) * ld_in + c0 + cc * 8));
         const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
         const float sc = scale ? scale[r] : 1.f;
 #pragma unroll
@@ -89,18 +93,27 @@ __global__ void __launch_bounds__(256)
         }
       }
     }
+    uint32_t* dst = h ? hi16 : lo16;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) tile[rr][cc + q] = __float2bfloat16_rn(v[q]);
+    for (int q = 0; q < 4; ++q) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+      dst[q] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+  }
+  // word (c, pp) = (row 2pp, row 2pp+1) at column c: low half from row 2pp
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    T[cc * 8 + 2 * q][pp] = __byte_perm(lo16[q], hi16[q], 0x5410);
+    T[cc * 8 + 2 * q + 1][pp] = __byte_perm(lo16[q], hi16[q], 0x7632);
   }
   __syncthreads();
+  // store: output row c = c0 + warp * 4 + lane / 8 (+ 32), 16 bytes = 8 p (4 words) a lane
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const int cr = tid / 8 + 32 * h, pc = (tid % 8) * 8;
+    const int cr = h * 32 + warp * 4 + (lane >> 3), wi = (lane & 7) * 4;
     if (c0 + cr >= C) continue;
-    __align__(16) __nv_bfloat16 w[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) w[q] = tile[pc + q][cr];
-    *reinterpret_cast<uint4*>(out + int64_t(c0 + cr) * ld_out + p0 + pc) = *reinterpret_cast<const uint4*>(w);
+    const uint4 o = make_uint4(T[cr][wi], T[cr][wi + 1], T[cr][wi + 2], T[cr][wi + 3]);
+    *reinterpret_cast<uint4*>(out + int64_t(c0 + cr) * ld_out + p0 + wi * 2) = o;
   }
 }
 
@@ -272,24 +285,18 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// dbias[e] = sum over tokens of dl[t][e]: 32 experts a block, 32 token lanes each summing a
-// strided subset in order, then the lanes in order.
-__global__ void __launch_bounds__(1024)
-    colsum_kernel(const float* __restrict__ dl, int S, int E, float* __restrict__ out) {
-  __shared__ float s_part[32][33];
+// dbias: part[ch][e] = sum over chunk ch's 256 tokens of dl[t][e] (thread e, tokens in order),
+// then out[e] = sum over chunks in order (sum_partials_kernel).
+__global__ void __launch_bounds__(256)
+    colsum_partial_kernel(const float* __restrict__ dl, int S, int E, float* __restrict__ part) {
   pdl_wait();
   pdl_trigger();
-  const int ex = threadIdx.x & 31, tl = threadIdx.x >> 5, e = blockIdx.x * 32 + ex;
+  const int e = threadIdx.x, ch = blockIdx.x;
+  if (e >= E) return;
+  const int t1 = min(S, (ch + 1) * 256);
   float acc = 0.f;
-  if (e < E)
-    for (int t = tl; t < S; t += 32) acc += dl[int64_t(t) * E + e];
-  s_part[tl][ex] = acc;
-  __syncthreads();
-  if (tl == 0 && e < E) {
-    float sum = 0.f;
-    for (int i = 0; i < 32; ++i) sum += s_part[i][ex];
-    out[e] = sum;
-  }
+  for (int t = ch * 256; t < t1; ++t) acc += dl[int64_t(t) * E + e];
+  part[int64_t(ch) * E + e] = acc;
 }
 
 // koffs[i] = min(total, i * chunk) for i = 0..n: split-K ranges of one K-ragged GEMM.
@@ -405,8 +412,12 @@ int launch_router_backward(const moe_config_t& c, const float* logits, const moe
                           static_cast<const float*>(b.dwg_part), nsplit, len, dW_g)) != MOE_OK)
     return rc;
   if (!dbias) return MOE_OK;
-  return launch_kernel(colsum_kernel, dim3(unsigned((c.E + 31) / 32)), dim3(1024), 0, st,
-                       static_cast<const float*>(b.dlogits), c.S, c.E, dbias);
+  const int nch = (c.S + 255) / 256;  // the bias partials reuse the dW_g partial buffer
+  if ((rc = launch_kernel(colsum_partial_kernel, dim3(unsigned(nch)), dim3(256), 0, st,
+                          static_cast<const float*>(b.dlogits), c.S, c.E, b.dwg_part)) != MOE_OK)
+    return rc;
+  return launch_kernel(sum_partials_kernel, dim3(unsigned((c.E + 255) / 256)), dim3(256), 0, st,
+                       static_cast<const float*>(b.dwg_part), nch, int64_t(c.E), dbias);
 }
 
 }  // namespace moe

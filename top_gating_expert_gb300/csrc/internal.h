@@ -141,7 +141,10 @@ inline WsLayoutBwd ws_layout_bwd(const moe_config_t& c, int C) {
   B.wgT = take(size_t(c.M) * Ep * 2);
   B.koff_e = take(2 * 4);
   B.koff_split = take((WsLayoutBwd::kMaxSplit + 1) * 4);
-  B.dwg_part = take(size_t(WsLayoutBwd::kMaxSplit) * c.E * c.M * 4);
+  // dW_g's split-K partials, later the bias partials ([S/256 chunks][E])
+  const size_t nch = (size_t(c.S) + 255) / 256;
+  const size_t part_floats = size_t(WsLayoutBwd::kMaxSplit) * c.E * c.M;
+  B.dwg_part = take((part_floats > nch * c.E ? part_floats : nch * c.E) * 4);
   B.dhs = take(sw ? size_t(c.S) * Hc * 2 : 0);
   B.dabs = take(size_t(c.S) * Fs * 2);
   B.dxs = take(Hc ? size_t(c.S) * c.M * 2 : 0);
