@@ -143,18 +143,29 @@ __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, 
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + nt * BN;
     const __nv_bfloat16* hrow = static_cast<const __nv_bfloat16*>(p.aux) + grow * p.ld_aux + nt * BN;
     float gsum = 0.f;
+    // h of 32 columns per step, the next step's loads issued before this step's math
+    uint4 hn[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      hn[q] = valid ? __ldg(reinterpret_cast<const uint4*>(hrow) + q) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 16) {
-      uint32_t v[16];
-      tmem_ld16(tbase + c0, v);
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      uint4 hc[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) hc[q] = hn[q];
+      if (valid && c0 + 32 < BN) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) hn[q] = __ldg(reinterpret_cast<const uint4*>(hrow + c0 + 32) + q);
+      }
+      uint32_t v[32];
+      tmem_ld16(tbase + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+      tmem_ld16(tbase + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
       tmem_ld_wait();
       if (valid) {
-        const uint4 h0 = reinterpret_cast<const uint4*>(hrow + c0)[0];
-        const uint4 h1 = reinterpret_cast<const uint4*>(hrow + c0)[1];
-        const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-        uint32_t pk[8];
+        const uint32_t* hw = reinterpret_cast<const uint32_t*>(hc);
+        uint32_t pk[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 16; ++j) {
           const float2 hv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[j]));
           const float d0 = __uint_as_float(v[2 * j]), d1 = __uint_as_float(v[2 * j + 1]);
           gsum += d0 * hv.x + d1 * hv.y;
@@ -165,7 +176,8 @@ __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, 
           }
           pk[j] = pack_bf16x2(o0, o1);
         }
-        store_bf16x16(out + c0, pk);
+        store_bf16x16(out + c0, *reinterpret_cast<const uint32_t(*)[8]>(pk));
+        store_bf16x16(out + c0 + 16, *reinterpret_cast<const uint32_t(*)[8]>(pk + 8));
       }
     }
     if (valid && p.gpart) p.gpart[grow * p.n_tiles + nt] = gsum;
@@ -175,15 +187,22 @@ __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, 
     // interleaved column positions (out [rows, 2H])
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + nt * BN;
     const __nv_bfloat16* dhrow = static_cast<const __nv_bfloat16*>(p.aux) + grow * p.ld_aux + nt * (BN / 2);
+    uint4 dn[2];  // the next step's dh, loaded before this step's math
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      dn[q] = valid ? __ldg(reinterpret_cast<const uint4*>(dhrow) + q) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 1
     for (int c0 = 0; c0 < BN / 2; c0 += 16) {
+      const uint4 d0 = dn[0], d1 = dn[1];
+      if (valid && c0 + 16 < BN / 2) {
+        dn[0] = __ldg(reinterpret_cast<const uint4*>(dhrow + c0 + 16));
+        dn[1] = __ldg(reinterpret_cast<const uint4*>(dhrow + c0 + 16) + 1);
+      }
       uint32_t av[16], bv[16];
       tmem_ld16(tbase + c0, av);
       tmem_ld16(tbase + BN / 2 + c0, bv);
       tmem_ld_wait();
       if (valid) {
-        const uint4 d0 = reinterpret_cast<const uint4*>(dhrow + c0)[0];
-        const uint4 d1 = reinterpret_cast<const uint4*>(dhrow + c0)[1];
         const uint32_t dw[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
         uint32_t pa[8], pb[8];
 #pragma unroll
