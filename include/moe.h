@@ -375,8 +375,8 @@ typedef struct {
  * (dy [S, M] the upstream gradient of y; MegaBlocks router §3: the load-balancing loss
  * reaches the router only through the expert scores, its counts being constants; §2:
  * z-loss) with the routing decisions held fixed. A dropped assignment gives its gate no
- * gradient. Gates: MOE_GATE_SOFTMAX_TOPK or MOE_GATE_NONE (others: MOE_ERR_UNSUPPORTED), no
- * uniform assignment; bf16 only.
+ * gradient. Every gate normalisation (MOE_GATE_*); uniform assignment (ids that do not come
+ * from the logits) gives MOE_ERR_UNSUPPORTED; bf16 only.
  * Inputs from the forward: logits (the forward's logits_out, [S, E]), r (its routing
  * outputs) and fwd_ws (the MOE_WS_LAYER workspace of that moe_layer_forward call,
  * unchanged since: it holds x_perm, h and the shared experts' h). residual: 1 if the

@@ -20,9 +20,9 @@ Readings (repeated in the design notes):
       pages' loss description says ("the gradient reaches the router only through
       expert_scores"). A dropped assignment contributes nothing to y, so its gate gets no
       gradient. The counts f_e of the aux loss are constants.
-  R20 the backward covers the default gates (softmax over the k selected logits) and the
-      un-normalised full-softmax gates ("none"); p-norm gates and uniform assignment are
-      forward-only.
+  R20 the backward covers the default gates (softmax over the k selected logits), the
+      un-normalised full-softmax gates ("none") and the p-norm gates; uniform assignment
+      (a benchmark switch whose ids do not come from the logits) is forward-only.
 
 Pins: tests/test_oracle_backward.py checks every gradient against central finite
 differences of the (separately pinned) forward on tiny layers, away from routing ties.
@@ -75,6 +75,13 @@ def router_logit_grad(logits, r: dict, dgate, cfg: dict, aux_coef: float, z_coef
         sel = r["gate_raw"]
         inner = np.sum(sel * dgate, axis=1, keepdims=True)
         np.add.at(dl, (rows, ids.ravel()), (sel * (dgate - inner)).ravel())
+    elif cfg.get("gate_norm") == "pnorm":
+        # g_i = w_i / ||w||_p with w_i = exp(l_i): dg_i/dl_j = g_i (delta_ij - g_j^p), so
+        # dl_{id_j} = g_j dg_j - g_j^p sum_i g_i dg_i (p = 1: the softmax case above)
+        pw = float(cfg["gate_p"])
+        sel = O.normalised_gates(logits, ids, "pnorm", pw)
+        inner = np.sum(sel * dgate, axis=1, keepdims=True)
+        np.add.at(dl, (rows, ids.ravel()), (sel * dgate - sel ** pw * inner).ravel())
     else:
         # g_j = p_{id_j}: dl_i = sum_j dg_j p_{id_j} (delta(i, id_j) - p_i)
         sel = np.take_along_axis(p, ids, axis=1)
@@ -96,8 +103,9 @@ def layer_backward(arrays: dict, cfg: dict, dy, aux_coef: float = 0.0, z_coef: f
     x = _f64(arrays["x"])
     S, E, k = cfg["S"], cfg["E"], cfg["k"]
     norm = cfg.get("gate_norm", "softmax_topk")
-    if norm not in ("softmax_topk", "none") or cfg.get("uniform_assignment", 0):
-        raise ValueError("the backward covers the softmax_topk and none gates (reading R20)")
+    if norm not in ("softmax_topk", "none", "pnorm") or cfg.get("uniform_assignment", 0):
+        raise ValueError("the backward covers the softmax_topk, none and pnorm gates, no uniform "
+                         "assignment (reading R20)")
     if logits is None:
         logits = O.router_logits(x, arrays["W_g"], arrays.get("bias"))
     logits = _f64(logits)

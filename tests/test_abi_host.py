@@ -151,6 +151,6 @@ def test_backward_host_checks(native_lib):
     assert L.moe_layer_backward(ctypes.byref(c), *args(), *tail(grads=g0)) == -1
     c32 = moe.make_config(CONFIGS[1])
     assert L.moe_layer_backward(ctypes.byref(c32), *args(), *tail()) == -2   # bf16 only
-    cp = moe.make_config(preset(2, gate_norm="pnorm", gate_p=2.0))
-    assert L.moe_layer_backward(ctypes.byref(cp), *args(), *tail()) == -2    # forward-only gates
+    cu = moe.make_config(preset(2, uniform_assignment=1, random_routing=0))
+    assert L.moe_layer_backward(ctypes.byref(cu), *args(), *tail()) == -2    # forward-only ids
     assert L.moe_pack_weights_backward(ctypes.byref(c32), fake, fake, fake, fake, fake, None) == -2

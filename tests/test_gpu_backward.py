@@ -1,8 +1,8 @@
 """GPU parity of moe_layer_backward against the backward oracle (itself pinned by finite
 differences): every gradient — dx, dW_g, dbias, the routed experts' and the shared experts'
 weights — element by element, on layers that span several GEMM tiles, with capacity drops,
-random routing, dropless top-3, shared SwiGLU experts, TopK(Softmax) gates and a ragged
-token count. The oracle starts from the GPU's own logits, so both sides hold the same
+random routing, dropless top-3, shared SwiGLU experts, TopK(Softmax) and p-norm gates and a
+ragged token count. The oracle starts from the GPU's own logits, so both sides hold the same
 routing decisions.
 
 Tolerance: R14's bf16 form |g - r| <= 2e-2 (|r| + rms(row)): the GPU backward's operands are
@@ -36,6 +36,10 @@ CASES = {
                                     n_shared=2, H_shared=128), True),
     "gates_none_k4": (_cfg(S=1024, E=32, M=128, H=128, k=4, gate_norm="none"), False),
     "ragged_tokens_k1": (_cfg(S=777, E=4, M=64, H=64, k=1, capacity_factor=1.5), True),
+    "pnorm2_capacity_k3": (_cfg(S=1536, E=16, M=128, H=256, k=3, capacity_factor=1.0,
+                                gate_norm="pnorm", gate_p=2.0), False),
+    "pnorm_half_swiglu": (_cfg(S=1024, E=8, M=128, H=128, act="swiglu", gate_norm="pnorm",
+                               gate_p=0.5), True),
 }
 AUX, Z = 0.7, 0.3
 

@@ -13,10 +13,11 @@ EPS = 1e-6
 
 
 def _layer(seed, act, S=12, G=2, E=4, M=6, H=4, k=2, cf=1.0, rr=0, n_shared=0, bias=True,
-           norm="softmax_topk"):
+           norm="softmax_topk", p=1.0):
     rng = np.random.default_rng(seed)
     cfg = dict(S=S, G=G, E=E, M=M, H=H, k=k, capacity_factor=cf, random_routing=rr,
-               n_shared=n_shared, H_shared=3 if n_shared else 0, act=act, gate_norm=norm)
+               n_shared=n_shared, H_shared=3 if n_shared else 0, act=act, gate_norm=norm,
+               gate_p=p)
     a = dict(x=rng.standard_normal((S, M)), W_g=rng.standard_normal((E, M)),
              W_in=rng.standard_normal((E, H, M)) * 0.5, W_up=rng.standard_normal((E, H, M)) * 0.5,
              W_out=rng.standard_normal((E, M, H)) * 0.5, u=rng.random(S, dtype=np.float32))
@@ -53,6 +54,8 @@ CASES = [
     dict(seed=4, act="swiglu", n_shared=2, cf=0.5),                     # drops + shared
     dict(seed=5, act="relu", rr=1, cf=1.0),                             # random routing
     dict(seed=6, act="swiglu", norm="none", G=3, S=15, E=6),            # TopK(Softmax) gates
+    dict(seed=7, act="relu", norm="pnorm", p=2.0, k=3, E=6),            # p-norm gates
+    dict(seed=8, act="swiglu", norm="pnorm", p=0.5, cf=0.75),           # p < 1, drops
 ]
 
 
@@ -103,8 +106,6 @@ def test_dgate_is_output_derivative_and_zero_when_dropped():
 
 def test_rejects_forward_only_variants():
     cfg, a, dy = _layer(seed=1, act="relu", norm="softmax_topk")
-    with pytest.raises(ValueError):
-        B.layer_backward(a, dict(cfg, gate_norm="pnorm", gate_p=2.0), dy)
     with pytest.raises(ValueError):
         B.layer_backward(a, dict(cfg, uniform_assignment=1), dy)
 

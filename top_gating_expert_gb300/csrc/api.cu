@@ -524,7 +524,6 @@ int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, c
   if (rc != MOE_OK) return rc;
   const moe_config_t& c = *cfg;
   if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
-  if (c.gate_norm != MOE_GATE_SOFTMAX_TOPK && c.gate_norm != MOE_GATE_NONE) return MOE_ERR_UNSUPPORTED;
   if (c.uniform_assignment) return MOE_ERR_UNSUPPORTED;
   if (c.E > 256) return MOE_ERR_UNSUPPORTED;
   const bool sw = c.act == MOE_ACT_SWIGLU;

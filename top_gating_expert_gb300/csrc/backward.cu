@@ -166,7 +166,9 @@ __global__ void __launch_bounds__(256)
 // dL/dlogits, one warp per token (lane l holds experts l, l + 32, ...):
 //   gate term   MOE_GATE_SOFTMAX_TOPK: g = softmax over the k selected logits,
 //               dl[id_j] += g_j (dg_j - sum_i g_i dg_i); MOE_GATE_NONE: g_j = p[id_j],
-//               dl[id_j] += g_j dg_j and dl[e] -= p_e sum_j g_j dg_j;
+//               dl[id_j] += g_j dg_j and dl[e] -= p_e sum_j g_j dg_j; MOE_GATE_PNORM:
+//               g_j = w_j / ||w||_p with w_j = exp(l_id_j - l_id_1) (the forward's gates),
+//               dl[id_j] += g_j dg_j - g_j^p sum_i g_i dg_i;
 //   aux term    aux_coef * E / (G * S_g) * p_e (f_e - sum_e' f_e' p_e'), f = counts_routed of
 //               the token's group / (S_g k);
 //   z term      z_coef * 2 / S * lse * p_e.
@@ -177,7 +179,8 @@ __global__ void __launch_bounds__(256)
     router_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ expert_id,
                       const int32_t* __restrict__ row, const float* __restrict__ gpart, int n_tiles,
                       const int32_t* __restrict__ counts_routed, int S, int G, int E, int k,
-                      int gate_norm, float aux_coef, float z_coef, float* __restrict__ dlogits,
+                      int gate_norm, float gate_p, float aux_coef, float z_coef,
+                      float* __restrict__ dlogits,
                       __nv_bfloat16* __restrict__ dlb, int Ep) {
   pdl_wait();
   pdl_trigger();
@@ -239,6 +242,28 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         if (j < k && id[j] == lane + 32 * q) dl[q] += gsel[j] * (dg[j] - inner);
+  } else if (gate_norm == MOE_GATE_PNORM) {
+    // g_j^p = w_j^p / sum_i w_i^p: kept as w_j^p in wp[] and divided once
+    const float top = gsel[0];
+    float wp[KMAX], sp = 0.f;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      gsel[j] = j >= k ? 0.f : (top > -INFINITY ? expf(gsel[j] - top) : (j == 0 ? 1.f : 0.f));
+      wp[j] = j < k ? powf(gsel[j], gate_p) : 0.f;
+      sp += wp[j];
+    }
+    const float ginv = 1.f / powf(sp, 1.f / gate_p), spinv = 1.f / sp;
+    float inner = 0.f;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      gsel[j] *= ginv;
+      inner += gsel[j] * dg[j];
+    }
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (j < k && id[j] == lane + 32 * q) dl[q] += gsel[j] * dg[j] - wp[j] * spinv * inner;
   } else {  // MOE_GATE_NONE
     float inner = 0.f;
 #pragma unroll
@@ -363,11 +388,11 @@ int launch_router_backward(const moe_config_t& c, const float* logits, const moe
   int rc;
   if (c.k <= 2)
     rc = launch_kernel(router_bwd_kernel<2>, dim3(blocks), dim3(256), 0, st, logits, r.expert_id, r.row,
-                       gpart, n_tiles, r.counts_routed, c.S, c.G, c.E, c.k, c.gate_norm, aux_coef,
+                       gpart, n_tiles, r.counts_routed, c.S, c.G, c.E, c.k, c.gate_norm, c.gate_p, aux_coef,
                        z_coef, b.dlogits, static_cast<__nv_bfloat16*>(b.dlb), Ep);
   else
     rc = launch_kernel(router_bwd_kernel<8>, dim3(blocks), dim3(256), 0, st, logits, r.expert_id, r.row,
-                       gpart, n_tiles, r.counts_routed, c.S, c.G, c.E, c.k, c.gate_norm, aux_coef,
+                       gpart, n_tiles, r.counts_routed, c.S, c.G, c.E, c.k, c.gate_norm, c.gate_p, aux_coef,
                        z_coef, b.dlogits, static_cast<__nv_bfloat16*>(b.dlb), Ep);
   if (rc != MOE_OK) return rc;
   // K ranges of the two router GEMMs: [0, Ep) and [0, Sp)
