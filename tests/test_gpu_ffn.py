@@ -243,11 +243,14 @@ def test_layer_output_vs_oracle(run):
 
 
 def test_layer_forward_equals_step_calls(run):
-    """moe_layer_forward launches the step calls' kernels: identical bits."""
+    """moe_layer_forward computes the step calls' results bit for bit (its last routing
+    kernel also does the dispatch gather: same routing outputs, same x_perm rows, so the
+    same y)."""
     cfg, d = run["cfg"], run["dev"]
     layer = moe.MoeLayer(cfg, {k: run["inp"].host[k] for k in run["inp"].host})
     y = layer.forward(d["x"], d["u"] if cfg["random_routing"] else None)
     assert moe.device_status(layer.ws) == 0
+    _same_route(route_np(layer.route_out), run["route"], run["name"])
     assert np.array_equal(to_np(y), run["y"])
     assert np.array_equal(to_np(layer.logits), run["logits"])
     y2 = layer.forward(d["x"], d["u"] if cfg["random_routing"] else None, residual=d["x"])

@@ -1,5 +1,6 @@
 // The C ABI of include/moe.h: argument checks, workspace carving and the order of launches.
 // Every check that can fail does so on the host, before anything is launched.
+#include <algorithm>
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
@@ -288,9 +289,11 @@ int moe_route(const moe_config_t* cfg, const float* logits, const float* u,
                       static_cast<char*>(ws), p.L, stream);
 }
 
-int moe_router_route(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
-                     const float* u, float* logits_out, const moe_route_out_t* out, void* ws,
-                     size_t ws_bytes, moe_stream_t stream) {
+namespace {
+// moe_router_route, optionally with the dispatch gather fused into its last kernel
+int router_route(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
+                 const float* u, float* logits_out, const moe_route_out_t* out, void* ws,
+                 size_t ws_bytes, const DispatchFuse* d, moe_stream_t stream) {
   Prep p;
   int rc = prepare(cfg, &p);
   if (rc != MOE_OK) return rc;
@@ -298,13 +301,23 @@ int moe_router_route(const moe_config_t* cfg, const void* x, const void* W_g, co
   if (cfg->dtype == MOE_F32 && !logits_out) return MOE_ERR_INVALID_ARG;
   if ((rc = check_route_out(*cfg, out)) != MOE_OK) return rc;
   if ((rc = check_ws(ws, ws_bytes, p.L.step_bytes)) != MOE_OK) return rc;
+  if (d && (!d->x_perm || !aligned16(d->x) || !aligned16(d->x_perm))) return MOE_ERR_INVALID_ARG;
+  char* w = static_cast<char*>(ws);
   if (cfg->dtype == MOE_F32) {
     if ((rc = moe_router(cfg, x, W_g, bias, logits_out, ws, ws_bytes, stream)) != MOE_OK) return rc;
-    return moe_route(cfg, logits_out, u, out, ws, ws_bytes, stream);
+    return launch_route(*cfg, p.C, logits_out, cfg->random_routing ? u : nullptr, *out, w, p.L,
+                        stream, d);
   }
   if (logits_out && !aligned16(logits_out)) return MOE_ERR_INVALID_ARG;
   return launch_router_route(*cfg, p.C, x, W_g, bias, cfg->random_routing ? u : nullptr,
-                             logits_out, *out, static_cast<char*>(ws), p.L, stream);
+                             logits_out, *out, w, p.L, stream, d);
+}
+}  // namespace
+
+int moe_router_route(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
+                     const float* u, float* logits_out, const moe_route_out_t* out, void* ws,
+                     size_t ws_bytes, moe_stream_t stream) {
+  return router_route(cfg, x, W_g, bias, u, logits_out, out, ws, ws_bytes, nullptr, stream);
 }
 
 int moe_dispatch(const moe_config_t* cfg, const void* x, const moe_route_out_t* r, void* x_perm,
@@ -398,9 +411,20 @@ int moe_layer_forward(const moe_config_t* cfg, const void* x, const void* W_g, c
   void* y_perm = w + p.L.y_perm;
   void* shared_out = cfg->n_shared > 0 ? static_cast<void*>(w + p.L.s_out) : nullptr;
   if (cfg->dtype == MOE_F32 && !logits) logits = reinterpret_cast<float*>(w + p.L.logits);
-  if ((rc = moe_router_route(cfg, x, W_g, bias, u, logits, r, ws, ws_bytes, stream)) != MOE_OK)
+  // routing's last kernel also writes x_perm, and brings GEMM 1's first wave of weight
+  // tiles (one BN x M tile per CTA pair, at most 40 MB) into L2 while the routing finishes
+  DispatchFuse fuse{x, x_perm, nullptr, 0};
+  if (cfg->dtype == MOE_BF16) {
+    const bool sw = cfg->act == MOE_ACT_SWIGLU;
+    const int64_t n1 = sw ? 2 * int64_t(cfg->H) : cfg->H;
+    const int64_t bn = gemm_bn(int(n1), sw ? EPI_SWIGLU : EPI_RELU);
+    int64_t pf = int64_t(num_sms() / 2) * bn * cfg->M * 2;
+    pf = std::min<int64_t>({pf, int64_t(cfg->E) * n1 * cfg->M * 2, int64_t(40) << 20});
+    fuse.prefetch = W_in_packed;
+    fuse.prefetch_bytes = pf;
+  }
+  if ((rc = router_route(cfg, x, W_g, bias, u, logits, r, ws, ws_bytes, &fuse, stream)) != MOE_OK)
     return rc;
-  if ((rc = moe_dispatch(cfg, x, r, x_perm, stream)) != MOE_OK) return rc;
   if ((rc = moe_expert_ffn(cfg, x_perm, r->expert_offsets, r->w_perm, W_in_packed, W_out_packed,
                            h_perm, y_perm, ws, ws_bytes, stream)) != MOE_OK)
     return rc;

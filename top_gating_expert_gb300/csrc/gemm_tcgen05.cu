@@ -95,6 +95,8 @@ struct KParams {
   const int32_t* koffs;  // K-ragged mode: per-group K range
   int c1;                // K-ragged mode: output rows per group
   void* out2;            // interleaved SwiGLU rows: the second 128-row block of each pair
+  const char* pfB;       // tile-major B, nullable: prefetch the start of the first tile
+  int64_t pf_bytes;      // bytes of that tile to prefetch into L2
 };
 
 using namespace sm100;
@@ -392,6 +394,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     if constexpr (PAIR) tmem_alloc_pair(smem_u32(s_tmem), C::TMEM_COLS);
     else tmem_alloc(smem_u32(s_tmem), C::TMEM_COLS);
+  }
+  if (p.pfB && threadIdx.x == 0 && leader) {
+    // The weights do not depend on the previous kernel: bring the first k-blocks of this
+    // unit's first B tile into L2 while that kernel finishes. The tile is a guess (one
+    // m-tile per group when the rows are grouped), so it may be the wrong one, never one
+    // outside B.
+    const int mt = p.offsets ? 1 : (p.rows_dense + C::TILE_M - 1) / C::TILE_M;
+    const int g = p.offsets ? unit / p.n_tiles : 0;
+    const int nt = p.offsets ? unit % p.n_tiles : unit / (mt > 0 ? mt : 1);
+    if (g < G && nt < p.n_tiles) {
+      const int64_t kb_bytes = int64_t(BN) * BK * 2;
+      const int64_t tile_bytes = int64_t(p.K / BK) * kb_bytes;
+      const char* base = p.pfB + (int64_t(g) * p.n_tiles + nt) * tile_bytes;
+      const int64_t n = p.pf_bytes < tile_bytes ? p.pf_bytes : tile_bytes;
+      for (int64_t o = 0; o + 16 <= n; o += 65536)
+        prefetch_l2_bulk(base + o, uint32_t(n - o < 65536 ? (n - o) & ~int64_t(15) : 65536));
+    }
   }
   pdl_wait();  // everything above is local setup; below, the first reads of the inputs
   pdl_trigger();
@@ -723,6 +742,8 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
   p.koffs = d.koffs;
   p.c1 = d.c1;
   p.out2 = d.out2;
+  p.pfB = (!KRAG && d.b_tiled) ? static_cast<const char*>(d.B) : nullptr;
+  p.pf_bytes = int64_t(512) << 10;
   auto kern = grouped_gemm_kernel<BN, EPI, PAIR, KRAG>;
   MOE_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
   const int64_t m_tiles =

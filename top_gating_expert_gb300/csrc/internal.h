@@ -157,14 +157,23 @@ inline WsLayoutBwd ws_layout_bwd(const moe_config_t& c, int C) {
 }
 
 // ------------------------------------------------------------------ launchers
-// route.cu
+// route.cu. With a DispatchFuse, the last routing kernel also writes x_perm (the dispatch
+// gather, x_perm[row[t, j]] = x[t] for every kept choice); the routing outputs are the same.
+struct DispatchFuse {
+  const void* x;             // [S, M], 16-byte aligned
+  void* x_perm;              // [R_max, M], 16-byte aligned
+  const void* prefetch;      // nullable: bytes to bring into L2 while the routing finishes
+  int64_t prefetch_bytes;    // (the first expert GEMM's first weight tiles), multiple of 16
+};
 int launch_route(const moe_config_t& c, int C, const float* logits, const float* u,
-                 const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st);
+                 const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st,
+                 const DispatchFuse* d = nullptr);
 // bf16 router projection fused with the first routing kernel (logits_out nullable), then the
 // same scan and finalize kernels as launch_route.
 int launch_router_route(const moe_config_t& c, int C, const void* x, const void* W_g,
                         const float* bias, const float* u, float* logits_out,
-                        const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st);
+                        const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st,
+                        const DispatchFuse* d = nullptr);
 
 // permute.cu
 int launch_dispatch(const moe_config_t& c, int64_t R_max, const void* x, const int32_t* token_of,
@@ -286,6 +295,23 @@ int launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
 #ifdef __CUDACC__
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// 16-byte row copies: a read-only load that skips L1, and a plain store (the copy's
+// destination is read again soon, by the next kernel)
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+// L2 prefetch of [p, p + bytes): p 16-byte aligned, bytes a multiple of 16
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void st_v4(uint4* p, const uint4& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
 #endif
 
 }  // namespace moe

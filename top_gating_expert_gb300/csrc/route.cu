@@ -316,11 +316,9 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(RouteArgs a, i
   }
 }
 
-__global__ void __launch_bounds__(256) route_finalize_kernel(RouteArgs a) {
-  pdl_wait();
-  pdl_trigger();
-  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= int64_t(a.S) * a.k) return;
+// Assignment idx = t * k + j: slot, keep/drop, row, inverse map. Returns the row (-1 if
+// not kept).
+__device__ __forceinline__ int finalize_assignment(const RouteArgs& a, int64_t idx) {
   const int t = int(idx / a.k), j = int(idx % a.k);
   const int e = a.expert_id[idx];
   const int g = t / a.Sg;
@@ -354,6 +352,66 @@ __global__ void __launch_bounds__(256) route_finalize_kernel(RouteArgs a) {
   a.row[idx] = row;
   a.drop[idx] = reason;
   a.gate[idx] = gt;
+  return row;
+}
+
+__global__ void __launch_bounds__(256) route_finalize_kernel(RouteArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= int64_t(a.S) * a.k) return;
+  finalize_assignment(a, idx);
+}
+
+// The finalize step fused with the dispatch gather (the whole-layer path): one warp per
+// token; lane j < k finalizes assignment (t, j), then the warp reads x[t] once (16-byte
+// units, 128 a pass) and writes it to every kept row of x_perm. Read as a gather over rows
+// (x_perm[r] = x[token_of[r]]) the dispatch reads x[t] once per kept choice; read from the
+// token's side it reads it once.
+// Before its wait on the scan, the kernel's first kPrefetchCtas CTAs bring the first
+// prefetch_bytes of the next GEMM's weights into L2 (32 KB pieces), so that they stream
+// from DRAM while the routing still runs (those weights do not depend on it).
+constexpr int kPrefetchCtas = 512;
+constexpr int64_t kPrefetchPiece = 32768;
+
+__global__ void __launch_bounds__(256)
+    route_finalize_dispatch_kernel(RouteArgs a, const uint4* __restrict__ x, int units,
+                                   uint4* __restrict__ x_perm, const char* __restrict__ pf,
+                                   int64_t pf_bytes) {
+  if (pf_bytes > 0 && threadIdx.x == 0) {
+    const int64_t pieces = (pf_bytes + kPrefetchPiece - 1) / kPrefetchPiece;
+    const int nb = min(int(gridDim.x), kPrefetchCtas);
+    for (int64_t i = blockIdx.x; i < pieces && int(blockIdx.x) < nb; i += nb) {
+      const int64_t o = i * kPrefetchPiece;
+      prefetch_l2_bulk(pf + o, uint32_t(min(kPrefetchPiece, pf_bytes - o)));
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (t >= a.S) return;
+  int row = -1;
+  if (lane < a.k) row = finalize_assignment(a, t * a.k + lane);
+  const uint4* src = x + t * units;
+  for (int q0 = 0; q0 < units; q0 += 128) {
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int q = q0 + lane + 32 * i;
+      if (q < units) v[i] = ld_nc_v4(src + q);
+    }
+    for (int j = 0; j < a.k; ++j) {
+      const int r = __shfl_sync(0xffffffffu, row, j);
+      if (r < 0) continue;
+      uint4* dst = x_perm + int64_t(r) * units;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int q = q0 + lane + 32 * i;
+        if (q < units) st_v4(dst + q, v[i]);
+      }
+    }
+  }
 }
 
 bool uses_variants(const moe_config_t& c) {
@@ -390,8 +448,9 @@ RouteArgs route_args(const moe_config_t& c, int C, const float* logits, const fl
   return a;
 }
 
-// the two launches after the per-chunk kernel
-int launch_scan_finalize(const moe_config_t& c, const RouteArgs& a, cudaStream_t st) {
+// the two launches after the per-chunk kernel; with d, the finalize step also dispatches
+int launch_scan_finalize(const moe_config_t& c, const RouteArgs& a, const DispatchFuse* d,
+                         cudaStream_t st) {
   // experts per scan CTA: about 2048 values of a group per CTA, at most kScanThreads columns
   const int64_t vals = int64_t(a.n_cpg) * (int64_t(c.k) * c.E + 2 * c.E + 1);
   int X = int((vals + 2047) / 2048);
@@ -403,6 +462,13 @@ int launch_scan_finalize(const moe_config_t& c, const RouteArgs& a, cudaStream_t
   int rc = launch_kernel(route_scan_kernel, dim3(unsigned(c.G * X)), dim3(kScanThreads), 0, st, a, X,
                          ew);
   if (rc != MOE_OK) return rc;
+  if (d) {
+    const int units = int(int64_t(c.M) * elem_bytes(c) / 16);
+    return launch_kernel(route_finalize_dispatch_kernel, dim3(unsigned((int64_t(c.S) * 32 + 255) / 256)),
+                         dim3(256), 0, st, a, static_cast<const uint4*>(d->x), units,
+                         static_cast<uint4*>(d->x_perm), static_cast<const char*>(d->prefetch),
+                         d->prefetch ? (d->prefetch_bytes & ~int64_t(15)) : int64_t(0));
+  }
   const int64_t n = int64_t(c.S) * c.k;
   return launch_kernel(route_finalize_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, st, a);
 }
@@ -410,18 +476,20 @@ int launch_scan_finalize(const moe_config_t& c, const RouteArgs& a, cudaStream_t
 }  // namespace
 
 int launch_route(const moe_config_t& c, int C, const float* logits, const float* u,
-                 const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st) {
+                 const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st,
+                 const DispatchFuse* d) {
   if (reinterpret_cast<uintptr_t>(logits) % 16 != 0) return MOE_ERR_INVALID_ARG;
   const RouteArgs a = route_args(c, C, logits, u, out, ws, L);
   const int rc = uses_variants(c) ? launch_topk_chunks_variants(a, L.n_chunks, st)
                                   : launch_topk_chunks(a, L.n_chunks, st);
   if (rc != MOE_OK) return rc;
-  return launch_scan_finalize(c, a, st);
+  return launch_scan_finalize(c, a, d, st);
 }
 
 int launch_router_route(const moe_config_t& c, int C, const void* x, const void* W_g,
                         const float* bias, const float* u, float* logits_out,
-                        const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st) {
+                        const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st,
+                        const DispatchFuse* d) {
   FusedRouterArgs f;
   f.bias = bias;
   f.logits_out = logits_out;
@@ -437,7 +505,7 @@ int launch_router_route(const moe_config_t& c, int C, const void* x, const void*
   rc = uses_variants(c) ? launch_router_chunks_variants(tx, tw, a, f, L.n_chunks, st)
                         : launch_router_chunks(tx, tw, a, f, L.n_chunks, st);
   if (rc != MOE_OK) return rc;
-  return launch_scan_finalize(c, a, st);
+  return launch_scan_finalize(c, a, d, st);
 }
 
 }  // namespace moe
