@@ -706,9 +706,9 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
   if (d.b_tiled) {
     if (d.N % BN != 0 || d.b_rows % d.N != 0) return MOE_ERR_UNSUPPORTED;
     rc = make_map_tiled(&tb, d.B, d.b_rows / BN * (d.K / BK), BN, C::B_ROWS);
-  } else {
-    if (PAIR) return MOE_ERR_UNSUPPORTED;
-    rc = make_map(&tb, d.B, d.b_rows, d.K, BN);
+  } else {  // row-major B: a pair's CTAs each load their half of the BN rows
+    if (PAIR && !KRAG) return MOE_ERR_UNSUPPORTED;
+    rc = make_map(&tb, d.B, d.b_rows, d.K, C::B_ROWS);
   }
   if (rc != MOE_OK) return rc;
   CUtensorMap to, to2;  // K-ragged: the fp32 outputs, 32 x 32 boxes, 128-byte swizzle
@@ -796,9 +796,16 @@ int launch_gemm_bf16(const GemmDesc& d, cudaStream_t st) {
   const int bn = gemm_bn(d.N, d.epi);
   // 256-wide tiles of packed weights run on CTA pairs (cta_group::2, 256 x 256 tiles)
   const bool pair = d.b_tiled && bn == 256;
-  if (d.koffs) {  // weight gradients: K ragged per group, fp32 out, single-CTA tiles
+  if (d.koffs) {  // weight gradients: K ragged per group, fp32 out
     if (d.epi != EPI_F32_BIAS || d.groups > kMaxGroups) return MOE_ERR_UNSUPPORTED;
-    // the fp32 epilogue masks columns past N, so any N takes the widest tile up to 256
+    // the fp32 epilogue masks columns past N, so any N takes the widest tile up to 256.
+    // With long K ranges (>= 768 a group on average) and outputs of 256 rows or more a group
+    // the tiles run on CTA pairs (256 x 256: each SM pulls 32 KB a k-block for 128 x 256
+    // outputs instead of 48 KB); short K ranges are bound by the fp32 stores, where the
+    // pair's shared accumulator hand-off only costs (measured: preset 5 backward 3.81 ->
+    // 3.53 ms with pairs, preset 2 1.75 -> 2.03 ms)
+    if (d.N > 128 && d.c1 >= 256 && int64_t(d.K) >= 768 * int64_t(d.groups))
+      return run_gemm<256, EPI_F32_BIAS, true, true>(d, st);
     if (d.N > 128) return run_gemm<256, EPI_F32_BIAS, false, true>(d, st);
     if (d.N > 64) return run_gemm<128, EPI_F32_BIAS, false, true>(d, st);
     return run_gemm<64, EPI_F32_BIAS, false, true>(d, st);
