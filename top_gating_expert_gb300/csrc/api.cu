@@ -413,8 +413,10 @@ int moe_layer_forward(const moe_config_t* cfg, const void* x, const void* W_g, c
   if (cfg->dtype == MOE_F32 && !logits) logits = reinterpret_cast<float*>(w + p.L.logits);
   // routing's last kernel also writes x_perm, and brings GEMM 1's first wave of weight
   // tiles (one BN x M tile per CTA pair, at most 40 MB) into L2 while the routing finishes
-  DispatchFuse fuse{x, x_perm, nullptr, 0};
+  DispatchFuse fuse{x, x_perm, nullptr, 0, nullptr, 0};
   if (cfg->dtype == MOE_BF16) {
+    fuse.h_tail = h_perm;  // zero rows past the kept ones, read by the backward
+    fuse.h_cols = cfg->H;
     const bool sw = cfg->act == MOE_ACT_SWIGLU;
     const int64_t n1 = sw ? 2 * int64_t(cfg->H) : cfg->H;
     const int64_t bn = gemm_bn(int(n1), sw ? EPI_SWIGLU : EPI_RELU);
@@ -524,12 +526,17 @@ int ffn_backward_data(const moe_config_t& c, const FfnBwd& f, unsigned* status, 
 }
 
 // dW[g] (fp32 [c1][N]) = A_g . B_g^T over group g's padded K segment (A [c1][Kp], B [N][Kp]).
-int weight_grad(const void* A, int c1, const void* B, int N, int64_t Kp, const int32_t* koffs,
-                int groups, float* out, float* out2, unsigned* status, cudaStream_t st) {
+// dW[g] = A_g^T . B_g over K-row ranges, both operands row-major and read in place (MN-major
+// tcgen05 operands): A [a_krows, c1], B [b_krows, N]; group g takes koffs[g+1] - koffs[g]
+// rows (a multiple of 64) from row aoffs[g] of A and boffs[g] of B (null: koffs[g]).
+int weight_grad_mn(const void* A, int64_t a_krows, const int32_t* aoffs, int c1, const void* B,
+                   int64_t b_krows, const int32_t* boffs, int N, int64_t Kp, const int32_t* koffs,
+                   int groups, float* out, float* out2, unsigned* status, cudaStream_t st) {
   GemmDesc d;
   d.epi = EPI_F32_BIAS;
-  d.A = A; d.a_rows = c1; d.K = int(Kp);
-  d.B = B; d.N = N; d.b_rows = N; d.b_tiled = false;
+  d.mn = true;
+  d.A = A; d.a_krows = a_krows; d.a_rows = c1; d.aoffs = aoffs; d.K = int(Kp);
+  d.B = B; d.b_krows = b_krows; d.boffs = boffs; d.N = N; d.b_rows = N; d.b_tiled = false;
   d.koffs = koffs; d.c1 = c1; d.groups = groups;
   d.out = out; d.ldo = N; d.n_valid = N; d.out2 = out2;
   d.status = status;
@@ -581,36 +588,35 @@ int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, c
   f.h = fw + p.L.h_perm; f.dh = w + B.dh; f.dab = w + B.dab;
   f.gpart = reinterpret_cast<float*>(w + B.gpart); f.dx_rows = w + B.dx_perm;
   if ((rc = ffn_backward_data(c, f, status, stream)) != MOE_OK) return rc;
-  // routed experts: weight gradients over per-expert 64-padded transposed segments
+  // routed experts: weight gradients, K = the expert's rows padded to 64. dW_out = (w dy)^T h:
+  // A = gate-scaled dy gathered into 64-padded segments (zero rows in the padding), B = h
+  // read in place from the segment's first row (its rows past the segment are the next
+  // expert's, or the 64 zeroed rows after the last: A's zeros cancel them). dW_in = da^T x:
+  // A = da in place (64 rows past the last zeroed here), B = x gathered padded.
   int32_t* poff = reinterpret_cast<int32_t*>(w + B.poff);
   if ((rc = launch_pad_offsets(r->expert_offsets, c.E, 0, poff, stream)) != MOE_OK) return rc;
-  struct T { const void* in; int64_t ld; const int32_t* gather; const float* scale; int C; size_t out; };
-  const T ts[4] = {{dy, c.M, r->token_of, r->w_perm, c.M, B.dyT},
-                   {fw + p.L.h_perm, c.H, nullptr, nullptr, c.H, B.hT},
-                   {w + B.dab, F, nullptr, nullptr, F, B.dabT},
-                   {x, c.M, r->token_of, nullptr, c.M, B.xT}};
-  for (const T& t : ts) {
-    const int src_rows = t.gather ? c.S : int(R);
-    if ((rc = launch_seg_transpose(t.in, t.ld, r->expert_offsets, c.E, 0, poff, B.Rp, t.gather,
-                                   src_rows, t.scale, t.C, w + t.out, B.Rp, status, stream)) != MOE_OK)
-      return rc;
-  }
-  if ((rc = weight_grad(w + B.dyT, c.M, w + B.hT, c.H, B.Rp, poff, c.E, grads->dW_out, nullptr,
-                        status, stream)) != MOE_OK)
+  if ((rc = launch_pad_gather(dy, c.M, r->token_of, r->w_perm, r->expert_offsets, poff, c.E, c.S,
+                              B.Rp, w + B.wdyP, nullptr, 0, status, stream)) != MOE_OK)
     return rc;
-  if ((rc = weight_grad(w + B.dabT, F, w + B.xT, c.M, B.Rp, poff, c.E, grads->dW_in,
-                        sw ? grads->dW_up : nullptr, status, stream)) != MOE_OK)
+  if ((rc = launch_pad_gather(x, c.M, r->token_of, nullptr, r->expert_offsets, poff, c.E, c.S,
+                              B.Rp, w + B.xP, w + B.dab, F, status, stream)) != MOE_OK)
     return rc;
-  // x^T [M][Sp] (zero-padded): the router's dW_g and the shared experts' weight gradients
+  if ((rc = weight_grad_mn(w + B.wdyP, B.Rp, nullptr, c.M, fw + p.L.h_perm, R + 64,
+                           r->expert_offsets, c.H, B.Rp, poff, c.E, grads->dW_out, nullptr, status,
+                           stream)) != MOE_OK)
+    return rc;
+  if ((rc = weight_grad_mn(w + B.dab, R + 64, r->expert_offsets, F, w + B.xP, B.Rp, nullptr, c.M,
+                           B.Rp, poff, c.E, grads->dW_in, sw ? grads->dW_up : nullptr, status,
+                           stream)) != MOE_OK)
+    return rc;
+  // K = all S tokens (padded to 64) for the router's dW_g and the shared experts: the tensors
+  // end at row S, so the padding reads as zeros
   int32_t* poff_s = reinterpret_cast<int32_t*>(w + B.poff_s);
   if ((rc = launch_pad_offsets(nullptr, 1, c.S, poff_s, stream)) != MOE_OK) return rc;
-  if ((rc = launch_seg_transpose(x, c.M, nullptr, 1, c.S, poff_s, B.Sp, nullptr, c.S, nullptr, c.M,
-                                 w + B.xTs, B.Sp, status, stream)) != MOE_OK)
-    return rc;
   // the router: dlogits from the gates' gradients, aux and z; then dx, dW_g (tcgen05), dbias
   RouterBwdBufs rb;
   rb.dlogits = reinterpret_cast<float*>(w + B.dlogits);
-  rb.dlb = w + B.dlb; rb.dlT = w + B.dlT; rb.wgT = w + B.wgT; rb.xT = w + B.xTs;
+  rb.dlb = w + B.dlb; rb.wgT = w + B.wgT;
   rb.dx_r = reinterpret_cast<float*>(w + B.dx_r);
   rb.koff_e = reinterpret_cast<int32_t*>(w + B.koff_e); rb.koff_s = poff_s; rb.Sp = B.Sp;
   rb.koff_split = reinterpret_cast<int32_t*>(w + B.koff_split);
@@ -630,18 +636,11 @@ int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, c
     s.Wt_out_packed = Wst_out_packed; s.dy_rows = dy; s.w = nullptr; s.h = fw + p.L.h_shared;
     s.dh = w + B.dhs; s.dab = w + B.dabs; s.gpart = nullptr; s.dx_rows = w + B.dxs;
     if ((rc = ffn_backward_data(c, s, status, stream)) != MOE_OK) return rc;
-    const T tss[3] = {{dy, c.M, nullptr, nullptr, c.M, B.dyTs},
-                      {fw + p.L.h_shared, Hc, nullptr, nullptr, Hc, B.hsT},
-                      {w + B.dabs, Fs, nullptr, nullptr, Fs, B.dabsT}};
-    for (const T& t : tss)
-      if ((rc = launch_seg_transpose(t.in, t.ld, nullptr, 1, c.S, poff_s, B.Sp, nullptr, c.S,
-                                     nullptr, t.C, w + t.out, B.Sp, status, stream)) != MOE_OK)
-        return rc;
-    if ((rc = weight_grad(w + B.dyTs, c.M, w + B.hsT, Hc, B.Sp, poff_s, 1, grads->dWs_out, nullptr,
-                          status, stream)) != MOE_OK)
+    if ((rc = weight_grad_mn(dy, c.S, nullptr, c.M, fw + p.L.h_shared, c.S, nullptr, Hc, B.Sp,
+                             poff_s, 1, grads->dWs_out, nullptr, status, stream)) != MOE_OK)
       return rc;
-    if ((rc = weight_grad(w + B.dabsT, Fs, w + B.xTs, c.M, B.Sp, poff_s, 1, grads->dWs_in,
-                          sw ? grads->dWs_up : nullptr, status, stream)) != MOE_OK)
+    if ((rc = weight_grad_mn(w + B.dabs, c.S, nullptr, Fs, x, c.S, nullptr, c.M, B.Sp, poff_s, 1,
+                             grads->dWs_in, sw ? grads->dWs_up : nullptr, status, stream)) != MOE_OK)
       return rc;
     dxs = w + B.dxs;
   }

@@ -324,6 +324,75 @@ __global__ void __launch_bounds__(256)
   part[int64_t(ch) * E + e] = acc;
 }
 
+// Gather into per-expert 64-padded segments (the row-major A or B operand of the weight-
+// gradient GEMM): padded row p of expert e (poff[e] <= p < poff[e+1]) is
+// scale[r] * src[token_of[r]] with r = offsets[e] + p - poff[e] while p - poff[e] is below
+// e's row count, and zeros after it. One warp per padded row, 16-byte units (bf16, rounded
+// to nearest even after an fp32 multiply). With tail, the 64 rows of tail from row
+// offsets[E] on (tail_units a row) are zeroed too: the GEMM reads them past the last
+// segment.
+__global__ void __launch_bounds__(256)
+    pad_gather_kernel(const uint4* __restrict__ src, int units, const int32_t* __restrict__ token_of,
+                      const float* __restrict__ scale, const int32_t* __restrict__ offsets,
+                      const int32_t* __restrict__ poff, int E, int S, int64_t rows_bound,
+                      uint4* __restrict__ out, uint4* __restrict__ tail, int tail_units,
+                      unsigned* __restrict__ status) {
+  __shared__ int s_poff[257], s_off[257];
+  pdl_wait();
+  pdl_trigger();
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+    s_poff[i] = poff[i];
+    s_off[i] = offsets[i];
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const int64_t P = min(int64_t(s_poff[E]), rows_bound);
+  for (int64_t p = w0; p < P; p += nw) {
+    int lo = 0, hi = E;  // the expert e with poff[e] <= p < poff[e + 1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_poff[mid] <= p) lo = mid;
+      else hi = mid;
+    }
+    const int64_t local = p - s_poff[lo];
+    uint4* dst = out + p * units;
+    int t = -1;
+    float sc = 1.f;
+    if (local < s_off[lo + 1] - s_off[lo]) {
+      const int64_t r = s_off[lo] + local;
+      t = token_of[r];
+      if (scale) sc = scale[r];
+      if (unsigned(t) >= unsigned(S)) {
+        if (lane == 0) atomicOr(status, kStatusDeviceData);
+        t = -1;
+      }
+    }
+    if (t < 0) {
+      for (int q = lane; q < units; q += 32) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    const uint4* row = src + int64_t(t) * units;
+    for (int q = lane; q < units; q += 32) {
+      uint4 v = __ldg(row + q);
+      if (scale) {
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(h[i]);
+          h[i] = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+        }
+      }
+      dst[q] = v;
+    }
+  }
+  if (tail && w0 < 64) {
+    uint4* trow = tail + (int64_t(s_off[E]) + w0) * tail_units;
+    for (int q = lane; q < tail_units; q += 32) trow[q] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // koffs[i] = min(total, i * chunk) for i = 0..n: split-K ranges of one K-ragged GEMM.
 __global__ void split_offsets_kernel(int n, int chunk, int total, int32_t* __restrict__ koffs) {
   pdl_wait();
@@ -331,19 +400,35 @@ __global__ void split_offsets_kernel(int n, int chunk, int total, int32_t* __res
   for (int i = threadIdx.x; i <= n; i += blockDim.x) koffs[i] = min(total, i * chunk);
 }
 
-// out[i] = sum over s = 0..n-1, in order, of part[s * len + i] (split-K partials).
+// out[i] = sum over s = 0..n-1, in order, of part[s * stride + i], i < len (split-K
+// partials).
 __global__ void __launch_bounds__(256)
-    sum_partials_kernel(const float* __restrict__ part, int n, int64_t len, float* __restrict__ out) {
+    sum_partials_kernel(const float* __restrict__ part, int n, int64_t len, int64_t stride,
+                        float* __restrict__ out) {
   pdl_wait();
   pdl_trigger();
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= len) return;
   float acc = 0.f;
-  for (int s = 0; s < n; ++s) acc += part[int64_t(s) * len + i];
+  for (int s = 0; s < n; ++s) acc += part[int64_t(s) * stride + i];
   out[i] = acc;
 }
 
 }  // namespace
+
+int launch_pad_gather(const void* src, int cols, const int32_t* token_of, const float* scale,
+                      const int32_t* offsets, const int32_t* poff, int E, int S, int64_t rows_bound,
+                      void* out, void* tail, int tail_cols, unsigned* status, cudaStream_t st) {
+  if (E > 256 || cols % 8 || tail_cols % 8) return MOE_ERR_UNSUPPORTED;
+  int64_t blocks = (rows_bound * 32 + 255) / 256;
+  const int64_t cap = int64_t(num_sms()) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 8) blocks = 8;  // the first 64 warps zero the tail
+  return launch_kernel(pad_gather_kernel, dim3(unsigned(blocks)), dim3(256), 0, st,
+                       static_cast<const uint4*>(src), cols / 8, token_of, scale, offsets, poff, E,
+                       S, rows_bound, static_cast<uint4*>(out), static_cast<uint4*>(tail),
+                       tail_cols / 8, status);
+}
 
 int launch_pad_offsets(const int32_t* offsets, int groups, int dense_rows, int32_t* poff,
                        cudaStream_t st) {
@@ -398,13 +483,11 @@ int launch_router_backward(const moe_config_t& c, const float* logits, const moe
   // K ranges of the two router GEMMs: [0, Ep) and [0, Sp)
   if ((rc = launch_pad_offsets(nullptr, 1, c.E, b.koff_e, st)) != MOE_OK) return rc;
   if ((rc = launch_pad_offsets(nullptr, 1, c.S, b.koff_s, st)) != MOE_OK) return rc;
-  // W_g^T [M][Ep] and dl^T [Ep][Sp] (zero-padded), x^T [M][Sp] is the caller's
+  // W_g^T [M][Ep] (zero-padded), the B operand of dx_r
   if ((rc = launch_seg_transpose(W_g, c.M, nullptr, 1, c.E, b.koff_e, Ep, nullptr, c.E, nullptr, c.M,
                                  b.wgT, Ep, status, st)) != MOE_OK)
     return rc;
-  if ((rc = launch_seg_transpose(b.dlb, Ep, nullptr, 1, c.S, b.koff_s, b.Sp, nullptr, c.S, nullptr, Ep,
-                                 b.dlT, b.Sp, status, st)) != MOE_OK)
-    return rc;
+
   // dx_r [S][M] = dl . W_g (one group of S rows, K = Ep); dW_g [E][M] = dl^T . x (K = Sp)
   GemmDesc d;
   d.epi = EPI_F32_BIAS;
@@ -425,16 +508,20 @@ int launch_router_backward(const moe_config_t& c, const float* logits, const moe
   if ((rc = launch_kernel(split_offsets_kernel, dim3(1), dim3(64), 0, st, nsplit, chunk, int(b.Sp),
                           b.koff_split)) != MOE_OK)
     return rc;
+  // MN-major operands read in place: A = dl [S][Ep] (bf16), B = x [S][M]; rows past S read
+  // as zeros. Split s writes rows s * Ep .. of the partials (rows E .. Ep - 1 are zeros).
   GemmDesc w;
   w.epi = EPI_F32_BIAS;
-  w.A = b.dlT; w.a_rows = c.E; w.K = int(b.Sp);
-  w.B = b.xT; w.N = c.M; w.b_rows = c.M; w.b_tiled = false;
-  w.koffs = b.koff_split; w.c1 = c.E; w.groups = nsplit;
+  w.mn = true;
+  w.A = b.dlb; w.a_krows = c.S; w.a_rows = Ep; w.K = int(b.Sp);
+  w.B = x; w.b_krows = c.S; w.N = c.M; w.b_rows = c.M; w.b_tiled = false;
+  w.koffs = b.koff_split; w.c1 = Ep; w.groups = nsplit;
   w.out = b.dwg_part; w.ldo = c.M; w.n_valid = c.M; w.status = status;
   if ((rc = launch_gemm_bf16(w, st)) != MOE_OK) return rc;
   const int64_t len = int64_t(c.E) * c.M;
   if ((rc = launch_kernel(sum_partials_kernel, dim3(unsigned((len + 255) / 256)), dim3(256), 0, st,
-                          static_cast<const float*>(b.dwg_part), nsplit, len, dW_g)) != MOE_OK)
+                          static_cast<const float*>(b.dwg_part), nsplit, len, int64_t(Ep) * c.M,
+                          dW_g)) != MOE_OK)
     return rc;
   if (!dbias) return MOE_OK;
   const int nch = (c.S + 255) / 256;  // the bias partials reuse the dW_g partial buffer
@@ -442,7 +529,7 @@ int launch_router_backward(const moe_config_t& c, const float* logits, const moe
                           static_cast<const float*>(b.dlogits), c.S, c.E, b.dwg_part)) != MOE_OK)
     return rc;
   return launch_kernel(sum_partials_kernel, dim3(unsigned((c.E + 255) / 256)), dim3(256), 0, st,
-                       static_cast<const float*>(b.dwg_part), nch, int64_t(c.E), dbias);
+                       static_cast<const float*>(b.dwg_part), nch, int64_t(c.E), int64_t(c.E), dbias);
 }
 
 }  // namespace moe

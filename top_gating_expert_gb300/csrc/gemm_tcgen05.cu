@@ -97,6 +97,10 @@ struct KParams {
   void* out2;            // interleaved SwiGLU rows: the second 128-row block of each pair
   const char* pfB;       // tile-major B, nullable: prefetch the start of the first tile
   int64_t pf_bytes;      // bytes of that tile to prefetch into L2
+  // K-ragged MN-major mode: A [.., c1] and B [.., N] row-major (K = rows); group g's K rows
+  // start at aoffs[g] in A and boffs[g] in B (null: koffs[g]), koffs giving the lengths
+  const int32_t* aoffs;
+  const int32_t* boffs;
 };
 
 using namespace sm100;
@@ -341,8 +345,21 @@ __device__ __forceinline__ void epilogue_f32_tma(const KParams& p, const CUtenso
   }
 }
 
+// Shared-memory descriptor of an MN-major operand staged as 64-column TMA boxes (128-byte
+// rows, one K index a row, 128-byte swizzle): the swizzle atom is 8 K rows of 64 MN
+// elements; atoms follow each other along K every 1024 bytes (stride offset) and along MN
+// every 8 KB, the next box (leading offset).
+__device__ __forceinline__ uint64_t mn_sw128_desc(uint32_t saddr) {
+  uint64_t d = uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t(8192 >> 4) << 16;  // leading-dimension offset: next 64 MN elements
+  d |= uint64_t(1024 >> 4) << 32;  // stride-dimension offset: next 8 K rows
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
+}
+
 // ------------------------------------------------------------------ the kernel
-template <int BN, int EPI, bool PAIR, bool KRAG>
+template <int BN, int EPI, bool PAIR, bool KRAG, bool MN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -492,6 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bblk = (g * p.n_tiles + nt) * kblocks;
       const int kb0 = KRAG ? s_koff[g] / BK : 0;
       const int nkb = KRAG ? s_koff[g + 1] / BK - kb0 : kblocks;
+      const int abase = MN ? (p.aoffs ? __ldg(p.aoffs + g) : s_koff[g]) : 0;  // K rows of A
+      const int bbase = MN ? (p.boffs ? __ldg(p.boffs + g) : s_koff[g]) : 0;  // K rows of B
       for (int kb = 0; kb < nkb; ++kb) {
         ok = __all_sync(0xffffffffu, wait_bounded(empty0 + 8 * stage, phase ^ 1u, s_abort, p.status));
         if (!ok) break;
@@ -500,7 +519,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t dA = smem_u32(sA + stage * C::A_BYTES);
           const uint32_t dB = smem_u32(sB + stage * C::B_BYTES);
           if (leader) mbar_expect_tx(fb, C::CTAS * C::STAGE_BYTES);
-          if constexpr (PAIR) {
+          if constexpr (MN) {
+            // 64 K rows x 64 columns a box: A's columns arow .. (this CTA's output rows), B's
+            // columns brow .. ; the boxes of a stage sit 8 KB apart
+            const int ya = abase + kb * BK, yb = bbase + kb * BK;
+            const uint32_t bar = PAIR ? cluster_addr(fb, 0) : fb;
+#pragma unroll
+            for (int i = 0; i < BM / 64; ++i) {
+              if constexpr (PAIR) tma_load_2d_pair(dA + i * 8192, &tmA, arow + 64 * i, ya, bar);
+              else tma_load_2d(dA + i * 8192, &tmA, arow + 64 * i, ya, bar);
+            }
+#pragma unroll
+            for (int i = 0; i < C::B_ROWS / 64; ++i) {
+              if constexpr (PAIR) tma_load_2d_pair(dB + i * 8192, &tmB, brow + 64 * i, yb, bar);
+              else tma_load_2d(dB + i * 8192, &tmB, brow + 64 * i, yb, bar);
+            }
+          } else if constexpr (PAIR) {
             const uint32_t lfb = cluster_addr(fb, 0);  // the even CTA's full barrier
             tma_load_2d_pair(dA, &tmA, (kb0 + kb) * BK, arow, lfb);
             if (p.b_tiled) tma_load_3d_pair(dB, &tmB, 0, int(rank) * C::B_ROWS, bblk + kb, lfb);
@@ -530,7 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer (the even CTA of a pair): the warp waits, lane 0 issues
     if (leader) {
-      constexpr uint32_t kIdesc = idesc_bf16(C::TILE_M, BN);
+      // MN-major operands: bits 15 and 16 of the instruction descriptor
+      constexpr uint32_t kIdesc = idesc_bf16(C::TILE_M, BN) | (MN ? (3u << 15) : 0u);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true, any = false;
@@ -557,12 +592,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
-              if constexpr (PAIR)
-                mma_bf16_pair(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), kIdesc,
-                              (kb | kk) != 0 ? 1u : 0u);
-              else
-                mma_bf16(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), kIdesc,
-                         (kb | kk) != 0 ? 1u : 0u);
+              // K-major: a K step of 16 is 32 bytes along the swizzled row; MN-major: 16
+              // K rows of 128 bytes
+              const uint64_t ad = MN ? mn_sw128_desc(a0 + kk * 2048) : sw128_desc(a0 + kk * 32);
+              const uint64_t bd = MN ? mn_sw128_desc(b0 + kk * 2048) : sw128_desc(b0 + kk * 32);
+              if constexpr (PAIR) mma_bf16_pair(d, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+              else mma_bf16(d, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
             }
             if constexpr (PAIR) mma_commit_pair(empty0 + 8 * stage, uint16_t(3));
             else mma_commit(empty0 + 8 * stage);
@@ -696,19 +731,26 @@ int make_map_tiled(CUtensorMap* m, const void* base, int64_t blocks, int block_r
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
-template <int BN, int EPI, bool PAIR, bool KRAG = false>
+template <int BN, int EPI, bool PAIR, bool KRAG = false, bool MN = false>
 int run_gemm(const GemmDesc& d, cudaStream_t st) {
   using C = Cfg<BN, PAIR, KRAG>;
   CUtensorMap ta, tb;
   if (KRAG && (!d.koffs || d.c1 < 1 || d.b_tiled || d.groups < 1)) return MOE_ERR_INVALID_ARG;
-  int rc = make_map(&ta, d.A, KRAG ? d.c1 : d.a_rows, d.K, BM);
-  if (rc != MOE_OK) return rc;
-  if (d.b_tiled) {
+  int rc;
+  if constexpr (MN) {  // row-major [K rows, c1] and [K rows, N]; 64 x 64 boxes
+    if (d.c1 % 64 || d.N % 8 || d.a_krows < 1 || d.b_krows < 1) return MOE_ERR_UNSUPPORTED;
+    if ((rc = make_map(&ta, d.A, d.a_krows, d.c1, 64)) != MOE_OK) return rc;
+    rc = make_map(&tb, d.B, d.b_krows, d.N, 64);
+  } else {
+    rc = make_map(&ta, d.A, KRAG ? d.c1 : d.a_rows, d.K, BM);
+    if (rc != MOE_OK) return rc;
+    if (d.b_tiled) {
     if (d.N % BN != 0 || d.b_rows % d.N != 0) return MOE_ERR_UNSUPPORTED;
     rc = make_map_tiled(&tb, d.B, d.b_rows / BN * (d.K / BK), BN, C::B_ROWS);
-  } else {  // row-major B: a pair's CTAs each load their half of the BN rows
-    if (PAIR && !KRAG) return MOE_ERR_UNSUPPORTED;
-    rc = make_map(&tb, d.B, d.b_rows, d.K, C::B_ROWS);
+    } else {  // row-major B: a pair's CTAs each load their half of the BN rows
+      if (PAIR && !KRAG) return MOE_ERR_UNSUPPORTED;
+      rc = make_map(&tb, d.B, d.b_rows, d.K, C::B_ROWS);
+    }
   }
   if (rc != MOE_OK) return rc;
   CUtensorMap to, to2;  // K-ragged: the fp32 outputs, 32 x 32 boxes, 128-byte swizzle
@@ -744,7 +786,9 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
   p.out2 = d.out2;
   p.pfB = (!KRAG && d.b_tiled) ? static_cast<const char*>(d.B) : nullptr;
   p.pf_bytes = int64_t(512) << 10;
-  auto kern = grouped_gemm_kernel<BN, EPI, PAIR, KRAG>;
+  p.aoffs = d.aoffs;
+  p.boffs = d.boffs;
+  auto kern = grouped_gemm_kernel<BN, EPI, PAIR, KRAG, MN>;
   MOE_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
   const int64_t m_tiles =
       KRAG ? int64_t(d.groups) * ((d.c1 + C::TILE_M - 1) / C::TILE_M)
@@ -804,8 +848,14 @@ int launch_gemm_bf16(const GemmDesc& d, cudaStream_t st) {
     // outputs instead of 48 KB); short K ranges are bound by the fp32 stores, where the
     // pair's shared accumulator hand-off only costs (measured: preset 5 backward 3.81 ->
     // 3.53 ms with pairs, preset 2 1.75 -> 2.03 ms)
-    if (d.N > 128 && d.c1 >= 256 && int64_t(d.K) >= 768 * int64_t(d.groups))
-      return run_gemm<256, EPI_F32_BIAS, true, true>(d, st);
+    const bool pair = d.N > 128 && d.c1 >= 256 && int64_t(d.K) >= 768 * int64_t(d.groups);
+    if (d.mn) {  // MN-major operands (row-major activations read in place)
+      if (d.N > 128) return pair ? run_gemm<256, EPI_F32_BIAS, true, true, true>(d, st)
+                                 : run_gemm<256, EPI_F32_BIAS, false, true, true>(d, st);
+      if (d.N > 64) return run_gemm<128, EPI_F32_BIAS, false, true, true>(d, st);
+      return run_gemm<64, EPI_F32_BIAS, false, true, true>(d, st);
+    }
+    if (pair) return run_gemm<256, EPI_F32_BIAS, true, true>(d, st);
     if (d.N > 128) return run_gemm<256, EPI_F32_BIAS, false, true>(d, st);
     if (d.N > 64) return run_gemm<128, EPI_F32_BIAS, false, true>(d, st);
     return run_gemm<64, EPI_F32_BIAS, false, true>(d, st);

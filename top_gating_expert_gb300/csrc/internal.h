@@ -62,7 +62,9 @@ inline WsLayout ws_layout(const moe_config_t& c, int C) {
   const size_t Hs = size_t(c.n_shared) * c.H_shared;
   L.logits = o; o = align256(o + size_t(c.S) * c.E * 4);
   L.x_perm = o; o = align256(o + size_t(R) * c.M * eb);
-  L.h_perm = o; o = align256(o + size_t(R) * c.H * eb);
+  // h has 64 more rows, zeroed by every layer forward: the backward's weight-gradient GEMM
+  // reads h row-major in 64-row blocks from each expert's first row
+  L.h_perm = o; o = align256(o + size_t(R + 64) * c.H * eb);
   L.y_perm = o; o = align256(o + size_t(R) * c.M * eb);
   L.h_shared = o; o = align256(o + size_t(c.S) * Hs * eb);
   L.s_out = o;  o = align256(o + (Hs ? size_t(c.S) * c.M * eb : 0));
@@ -71,14 +73,14 @@ inline WsLayout ws_layout(const moe_config_t& c, int C) {
 }
 
 // Byte offsets of the backward workspace (moe_layer_backward): R rows of the routed
-// experts, Rp = R_max + 64 E columns of the transposed, per-expert 64-padded segments.
+// experts; Rp = R_max + 64 E rows of the per-expert 64-padded segments (gate-scaled dy and
+// x gathered into them, zero rows between segments).
 struct WsLayoutBwd {
   int64_t Rp = 0, Sp = 0;
   int n_tiles2 = 0;  // N tiles of the backward GEMM 2 (gate-partial stride)
   size_t status = 0, dy_perm = 0, dh = 0, dab = 0, gpart = 0, dx_perm = 0, poff = 0, poff_s = 0,
-         dyT = 0, hT = 0, dabT = 0, xT = 0, dlogits = 0, dx_r = 0, dlb = 0, dlT = 0, wgT = 0,
-         koff_e = 0, koff_split = 0, dwg_part = 0, dhs = 0, dabs = 0, dxs = 0, dyTs = 0, hsT = 0,
-         dabsT = 0, xTs = 0;
+         wdyP = 0, xP = 0, dlogits = 0, dx_r = 0, dlb = 0, wgT = 0, koff_e = 0, koff_split = 0,
+         dwg_part = 0, dhs = 0, dabs = 0, dxs = 0;
   static constexpr int kMaxSplit = 64;  // split-K ranges of the router's dW_g
   size_t bytes = 0;
 };
@@ -124,34 +126,27 @@ inline WsLayoutBwd ws_layout_bwd(const moe_config_t& c, int C) {
   B.status = take(256);
   B.dy_perm = take(size_t(R) * c.M * 2);
   B.dh = take(sw ? size_t(R) * c.H * 2 : 0);
-  B.dab = take(size_t(R) * F * 2);
+  B.dab = take(size_t(R + 64) * F * 2);  // + 64 zeroed rows (read past the last segment)
   B.gpart = take(size_t(R) * B.n_tiles2 * 4);
   B.dx_perm = take(size_t(R) * c.M * 2);
   B.poff = take(size_t(c.E + 1) * 4);
   B.poff_s = take(2 * 4);
-  B.dyT = take(size_t(c.M) * B.Rp * 2);
-  B.hT = take(size_t(c.H) * B.Rp * 2);
-  B.dabT = take(size_t(F) * B.Rp * 2);
-  B.xT = take(size_t(c.M) * B.Rp * 2);
+  B.wdyP = take(size_t(B.Rp) * c.M * 2);
+  B.xP = take(size_t(B.Rp) * c.M * 2);
   B.dlogits = take(size_t(c.S) * c.E * 4);
   B.dx_r = take(size_t(c.S) * c.M * 4);
   const size_t Ep = (size_t(c.E) + 63) / 64 * 64;
   B.dlb = take(size_t(c.S) * Ep * 2);
-  B.dlT = take(Ep * B.Sp * 2);
   B.wgT = take(size_t(c.M) * Ep * 2);
   B.koff_e = take(2 * 4);
   B.koff_split = take((WsLayoutBwd::kMaxSplit + 1) * 4);
-  // dW_g's split-K partials, later the bias partials ([S/256 chunks][E])
+  // dW_g's split-K partials ([splits][Ep][M]), later the bias partials ([S/256 chunks][E])
   const size_t nch = (size_t(c.S) + 255) / 256;
-  const size_t part_floats = size_t(WsLayoutBwd::kMaxSplit) * c.E * c.M;
+  const size_t part_floats = size_t(WsLayoutBwd::kMaxSplit) * Ep * c.M;
   B.dwg_part = take((part_floats > nch * c.E ? part_floats : nch * c.E) * 4);
   B.dhs = take(sw ? size_t(c.S) * Hc * 2 : 0);
   B.dabs = take(size_t(c.S) * Fs * 2);
   B.dxs = take(Hc ? size_t(c.S) * c.M * 2 : 0);
-  B.dyTs = take(Hc ? size_t(c.M) * B.Sp * 2 : 0);
-  B.hsT = take(size_t(Hc) * B.Sp * 2);
-  B.dabsT = take(size_t(Fs) * B.Sp * 2);
-  B.xTs = take(size_t(c.M) * B.Sp * 2);  // x^T: the router's dW_g and the shared experts
   B.bytes = o;
   return B;
 }
@@ -164,6 +159,8 @@ struct DispatchFuse {
   void* x_perm;              // [R_max, M], 16-byte aligned
   const void* prefetch;      // nullable: bytes to bring into L2 while the routing finishes
   int64_t prefetch_bytes;    // (the first expert GEMM's first weight tiles), multiple of 16
+  void* h_tail;              // nullable: h [R_max + 64, h_cols] bf16, rows R .. R + 63 zeroed
+  int h_cols;                //   (R = the kept rows; h_cols % 8 == 0)
 };
 int launch_route(const moe_config_t& c, int C, const float* logits, const float* u,
                  const moe_route_out_t& out, char* ws, const WsLayout& L, cudaStream_t st,
@@ -219,6 +216,13 @@ struct GemmDesc {
   // with out2: output rows are pairs of 128-row blocks (the interleaved SwiGLU order) that go
   // to out (first block) and out2 (second), each [groups * c1 / 2, N]
   void* out2 = nullptr;
+  // MN-major K-ragged mode: A [a_krows, c1] and B [b_krows, N] row-major, K along the rows;
+  // group g takes koffs[g+1] - koffs[g] rows from row aoffs[g] of A and boffs[g] of B (null:
+  // koffs[g]); rows past a tensor's end read as zeros
+  bool mn = false;
+  int64_t a_krows = 0, b_krows = 0;
+  const int32_t* aoffs = nullptr;
+  const int32_t* boffs = nullptr;
 };
 int launch_gemm_bf16(const GemmDesc& d, cudaStream_t st);
 // 2-D tensor map over a row-major bf16 [rows, K] matrix, boxes of 64 columns x box_rows rows,
@@ -238,6 +242,11 @@ int launch_ffn_down_f32(const moe_config_t& c, int H, const float* h, const int3
 // backward.cu
 int launch_pad_offsets(const int32_t* offsets, int groups, int dense_rows, int32_t* poff,
                        cudaStream_t st);
+// dst[p] = scale[r] * src[token_of[r]] over per-expert 64-padded segments (poff), zeros
+// in the padding; with tail, 64 rows of tail from row offsets[E] zeroed (bf16, cols % 8 == 0)
+int launch_pad_gather(const void* src, int cols, const int32_t* token_of, const float* scale,
+                      const int32_t* offsets, const int32_t* poff, int E, int S, int64_t rows_bound,
+                      void* out, void* tail, int tail_cols, unsigned* status, cudaStream_t st);
 int launch_seg_transpose(const void* in, int64_t ld_in, const int32_t* offsets, int groups,
                          int dense_rows, const int32_t* poff, int64_t rows_pad_max,
                          const int32_t* gather, int src_rows, const float* scale, int C, void* out,
@@ -248,14 +257,12 @@ int launch_pack_transposed(int mode, int swiglu, int groups, int N, int K, int M
 struct RouterBwdBufs {
   float* dlogits;  // [S][E] fp32
   void* dlb;       // [S][Ep] bf16, Ep = E rounded up to 64
-  void* dlT;       // [Ep][Sp] bf16
   void* wgT;       // [M][Ep] bf16
-  const void* xT;  // [M][Sp] bf16 (x transposed, the caller's)
   float* dx_r;     // [S][M] fp32
   int32_t* koff_e; int32_t* koff_s;  // [2] each
   int64_t Sp;
   int32_t* koff_split;  // [max_split + 1]: split-K ranges of dW_g
-  float* dwg_part;      // [max_split][E][M] partials of dW_g
+  float* dwg_part;      // [max_split][Ep][M] partials of dW_g
   int max_split;
 };
 int launch_router_backward(const moe_config_t& c, const float* logits, const moe_route_out_t& r,

@@ -27,6 +27,8 @@
 //      expert_offsets, the per-(group, expert) first rows and the two loss scalars.
 //   3. route_finalize_kernel  one thread per assignment: slot, keep/drop, row, inverse map.
 // Every integer output is a pure function of the logits and u: no atomic decides an order.
+#include <algorithm>
+
 #include "route_kernels.cuh"
 
 namespace moe {
@@ -377,7 +379,7 @@ constexpr int64_t kPrefetchPiece = 32768;
 __global__ void __launch_bounds__(256)
     route_finalize_dispatch_kernel(RouteArgs a, const uint4* __restrict__ x, int units,
                                    uint4* __restrict__ x_perm, const char* __restrict__ pf,
-                                   int64_t pf_bytes) {
+                                   int64_t pf_bytes, uint4* __restrict__ h_tail, int h_units) {
   if (pf_bytes > 0 && threadIdx.x == 0) {
     const int64_t pieces = (pf_bytes + kPrefetchPiece - 1) / kPrefetchPiece;
     const int nb = min(int(gridDim.x), kPrefetchCtas);
@@ -390,6 +392,12 @@ __global__ void __launch_bounds__(256)
   pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (h_tail && t < 64) {  // the 64 rows of h after the kept ones: zeros (h is written later)
+    int64_t R = a.offsets[a.E];
+    R = R < 0 ? 0 : (R > a.R_max ? a.R_max : R);
+    uint4* hr = h_tail + (R + t) * h_units;
+    for (int q = lane; q < h_units; q += 32) hr[q] = make_uint4(0u, 0u, 0u, 0u);
+  }
   if (t >= a.S) return;
   int row = -1;
   if (lane < a.k) row = finalize_assignment(a, t * a.k + lane);
@@ -464,10 +472,12 @@ int launch_scan_finalize(const moe_config_t& c, const RouteArgs& a, const Dispat
   if (rc != MOE_OK) return rc;
   if (d) {
     const int units = int(int64_t(c.M) * elem_bytes(c) / 16);
-    return launch_kernel(route_finalize_dispatch_kernel, dim3(unsigned((int64_t(c.S) * 32 + 255) / 256)),
+    const int64_t warps = std::max<int64_t>(c.S, d->h_tail ? 64 : 1);  // 64: h's tail rows
+    return launch_kernel(route_finalize_dispatch_kernel, dim3(unsigned((warps * 32 + 255) / 256)),
                          dim3(256), 0, st, a, static_cast<const uint4*>(d->x), units,
                          static_cast<uint4*>(d->x_perm), static_cast<const char*>(d->prefetch),
-                         d->prefetch ? (d->prefetch_bytes & ~int64_t(15)) : int64_t(0));
+                         d->prefetch ? (d->prefetch_bytes & ~int64_t(15)) : int64_t(0),
+                         static_cast<uint4*>(d->h_tail), d->h_tail ? d->h_cols / 8 : 0);
   }
   const int64_t n = int64_t(c.S) * c.k;
   return launch_kernel(route_finalize_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, st, a);
