@@ -113,3 +113,43 @@ def test_unused_experts_get_zero_weight_grads(run):
     counts = ref["route"]["counts"].sum(axis=0)
     for e in np.nonzero(counts == 0)[0]:
         assert not run["got"]["dW_in"][e].any() and not run["got"]["dW_out"][e].any()
+
+
+@pytest.mark.parametrize("name", ["relu_capacity_rr_bias", "shared_swiglu_capacity", "gates_none_k4"])
+def test_stale_workspace_bytes_are_never_read(name, native_lib):
+    """The weight-gradient GEMMs read 64-row blocks that run past each expert's rows (into
+    the next expert's, or into 64 rows after the last that the forward and the backward
+    zero). With every workspace byte past the status header set to 0xFF (NaN in bf16 and
+    fp32) and the unwritten rows of token_of / w_perm poisoned too, every gradient must come
+    out bit for bit as from zero-filled workspaces, and so must the forward's y."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    cfg, residual = CASES[name]
+    seed = zlib.crc32(name.encode()) % 10000
+    inp = make_inputs(cfg, seed=seed)
+    g = torch.Generator().manual_seed(seed)
+    dy = torch.randn((cfg["S"], cfg["M"]), generator=g).to(torch.bfloat16).cuda()
+    x = inp.host["x"].cuda()
+    u = inp.host["u"].cuda() if cfg["random_routing"] else None
+
+    def grads(poison):
+        layer = moe.MoeLayer(cfg, inp.host)
+        layer.enable_backward(inp.host)
+        if poison:
+            for ws in (layer.ws, layer.ws_bwd):
+                ws[256:].fill_(0xFF)  # past the status word and the scan's ticket
+            layer.route_out.token_of.fill_(-1)
+            layer.route_out.w_perm.fill_(float("nan"))
+        y = to_np(layer.forward(x, u, residual=x if residual else None))
+        out = layer.backward(x, dy, residual=residual, aux_coef=AUX, z_coef=Z)
+        assert moe.device_status(layer.ws) == 0 and moe.device_status(layer.ws_bwd) == 0
+        res = {f: to_np(getattr(out, f)) for f in ("dx", "dW_g", "dbias", "dW_in", "dW_up",
+                                                    "dW_out", "dWs_in", "dWs_up", "dWs_out")
+               if getattr(out, f) is not None}
+        res["y"] = y
+        return res
+
+    clean, dirty = grads(False), grads(True)
+    for f in clean:
+        assert np.isfinite(dirty[f]).all(), f"{name}: {f} not finite"
+        assert np.array_equal(clean[f], dirty[f]), f"{name}: {f} differs with a stale workspace"

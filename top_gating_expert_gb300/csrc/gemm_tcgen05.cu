@@ -631,11 +631,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = unit; t < total; t += units, ++i) {
       const int acc = i & 1;
       const uint32_t use = uint32_t(i >> 1) & 1u;
+      int g, m0, rows, nt;
+      decode(t, g, m0, rows, nt);
+      if constexpr (EPI == EPI_DGRAD2 || EPI == EPI_SWIGLU_BWD) {
+        // the tile's h (dh) row segment of this lane: into L2 while the MMAs run
+        const int r = int(rank) * BM + q * 32 + lane;
+        constexpr int kAuxCols = EPI == EPI_DGRAD2 ? BN : BN / 2;
+        if (r < rows)
+          prefetch_l2_bulk(static_cast<const __nv_bfloat16*>(p.aux) + (int64_t(m0) + r) * p.ld_aux +
+                               int64_t(nt) * kAuxCols,
+                           uint32_t(kAuxCols * 2));
+      }
       const bool ok = __all_sync(0xffffffffu, wait_bounded(tfull0 + 8 * acc, use, s_abort, p.status));
       if (!ok) break;
       tc_fence_after();
-      int g, m0, rows, nt;
-      decode(t, g, m0, rows, nt);
       const int r = int(rank) * BM + q * 32 + lane;  // row within the tile
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
       const bool zero = KRAG && s_koff[g + 1] == s_koff[g];  // no MMA ran for this tile
