@@ -1,8 +1,8 @@
 """GPU parity of moe_layer_backward against the backward oracle (itself pinned by finite
 differences): every gradient — dx, dW_g, dbias, the routed experts' and the shared experts'
 weights — element by element, on layers that span several GEMM tiles, with capacity drops,
-random routing, dropless top-3, shared SwiGLU experts, TopK(Softmax) and p-norm gates and a
-ragged token count. The oracle starts from the GPU's own logits, so both sides hold the same
+random routing, dropless top-3, shared SwiGLU experts, TopK(Softmax) and p-norm gates,
+group-limited top-k and a ragged token count. The oracle starts from the GPU's own logits, so both sides hold the same
 routing decisions.
 
 Tolerance: R14's bf16 form |g - r| <= 2e-2 (|r| + rms(row)): the GPU backward's operands are
@@ -40,6 +40,8 @@ CASES = {
                                 gate_norm="pnorm", gate_p=2.0), False),
     "pnorm_half_swiglu": (_cfg(S=1024, E=8, M=128, H=128, act="swiglu", gate_norm="pnorm",
                                gate_p=0.5), True),
+    "group_limited_k3": (_cfg(S=1024, E=32, M=128, H=256, k=3, capacity_factor=1.25, act="swiglu",
+                              n_expert_groups=8, topk_groups=3), False),
 }
 AUX, Z = 0.7, 0.3
 

@@ -13,11 +13,13 @@ EPS = 1e-6
 
 
 def _layer(seed, act, S=12, G=2, E=4, M=6, H=4, k=2, cf=1.0, rr=0, n_shared=0, bias=True,
-           norm="softmax_topk", p=1.0):
+           norm="softmax_topk", p=1.0, ng=0, tg=0):
     rng = np.random.default_rng(seed)
     cfg = dict(S=S, G=G, E=E, M=M, H=H, k=k, capacity_factor=cf, random_routing=rr,
                n_shared=n_shared, H_shared=3 if n_shared else 0, act=act, gate_norm=norm,
                gate_p=p)
+    if ng:
+        cfg.update(n_expert_groups=ng, topk_groups=tg)
     a = dict(x=rng.standard_normal((S, M)), W_g=rng.standard_normal((E, M)),
              W_in=rng.standard_normal((E, H, M)) * 0.5, W_up=rng.standard_normal((E, H, M)) * 0.5,
              W_out=rng.standard_normal((E, M, H)) * 0.5, u=rng.random(S, dtype=np.float32))
@@ -56,6 +58,8 @@ CASES = [
     dict(seed=6, act="swiglu", norm="none", G=3, S=15, E=6),            # TopK(Softmax) gates
     dict(seed=7, act="relu", norm="pnorm", p=2.0, k=3, E=6),            # p-norm gates
     dict(seed=8, act="swiglu", norm="pnorm", p=0.5, cf=0.75),           # p < 1, drops
+    dict(seed=9, act="relu", E=8, k=3, ng=4, tg=2),                     # group-limited top-k
+    dict(seed=10, act="swiglu", E=8, ng=4, tg=1, norm="none", cf=0.0),  # one group, dropless
 ]
 
 
