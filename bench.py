@@ -480,6 +480,17 @@ def run_ours(args, rank, world, local_rank):
             return 2.0 * rows * M * (2 * hidden + 2 * fh) + (4.0 * rows * M * hidden if f1 == 2 else 0.0)
         flops = ffn_bwd(Rb, H) + (ffn_bwd(S, Hc) if Hc else 0.0) + 4.0 * S * E * M
         grad_bytes = 4 * (E * (F + H) * M + ((f1 + 1) * Hc * M if Hc else 0) + E * M)
+        # algorithmic bytes: every input read once (dy, x, the logits, W_g, the transposed
+        # weight packs, the packed W_in again for the SwiGLU recompute, the stored h) and every
+        # output written once (the fp32 weight gradients, dx)
+        b2 = 2
+        in_bytes = (b2 * (2 * S * M + E * M + E * (F + H) * M + (E * F * M if f1 == 2 else 0)
+                          + Rb * H) + 4 * S * E)
+        if Hc:
+            in_bytes += b2 * ((f1 + 1) * Hc * M + (f1 * Hc * M if f1 == 2 else 0) + S * Hc)
+        bwd_bytes = in_bytes + grad_bytes + b2 * S * M
+        t_bytes = bwd_bytes / (P["hbm"] * 1e9) * 1e3
+        t_flops = flops / (P["tc_sustained"] * 1e12) * 1e3
         line["backward"] = {
             "what": "moe_layer_backward: gradients of sum(dy*y) + 0.01 aux + 0.001 z w.r.t. x, "
                     "W_g, every expert weight (fp32), routing fixed; forward = moe_layer_forward "
@@ -489,6 +500,12 @@ def run_ours(args, rank, world, local_rank):
             "algorithmic_flops": flops, "TFLOP/s": round(flops / (b_ms * 1e-3) / 1e12, 2),
             "tensor_frac_sustained": round(flops / (b_ms * 1e-3) / 1e12 / P["tc_sustained"], 4),
             "fp32_weight_grad_bytes": int(grad_bytes),
+            "algorithmic_bytes": int(bwd_bytes),
+            "hbm_frac": round(bwd_bytes / (b_ms * 1e-3) / 1e9 / P["hbm"], 4),
+            # the binding roofline: the larger of the byte time (measured HBM copy rate) and
+            # the flop time (sustained bf16), and the step's fraction of it
+            "bound": "hbm" if t_bytes >= t_flops else "tensor",
+            "roofline_frac": round(max(t_bytes, t_flops) / b_ms, 4),
         }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, n, inp)
