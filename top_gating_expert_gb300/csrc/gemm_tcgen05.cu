@@ -656,11 +656,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         epilogue_rows<BN, EPI>(p, tbase, r < rows, int64_t(m0) + r, nt, zero);
       }
+      // the accumulator is free: every lane has waited for its tensor-memory loads
+      // (tcgen05.wait::ld); a relaxed arrive, as nothing of the stores needs ordering here
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if constexpr (PAIR) mbar_arrive_cluster(tempty_leader + 8 * acc);
-        else mbar_arrive(tempty0 + 8 * acc);
+        if constexpr (PAIR) mbar_arrive_cluster_relaxed(tempty_leader + 8 * acc);
+        else mbar_arrive_relaxed(tempty0 + 8 * acc);
       }
     }
     // K-ragged: every TMA store has finished before the CTA's shared memory goes away
