@@ -174,6 +174,24 @@ def traffic_for(kernel: str, config: int):
 
 
 # ------------------------------------------------------------------ our arm
+def max_over_ranks(values, world: int, device=None) -> list:
+    """Each rank's timings (ms); returns the maximum over the ranks of each: with one replica
+    per GPU and a barrier on both sides of every timed region, the slowest replica bounds
+    the whole job."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(units_per_rank_step: int, steps: int, world: int, total_ms: float) -> float:
+    """Whole-job units/s: every replica processes its own units each step (weak scaling)."""
+    return units_per_rank_step * steps * world / (total_ms * 1e-3)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -294,11 +312,7 @@ def run_ours(args, rank, world, local_rank):
     rc = moe.device_status(ws)
     if rc != 0:
         raise RuntimeError(f"device status {rc} in the timed region")
-    total_ms = sum(a.elapsed_time(b) for a, b in head_ev)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, = max_over_ranks([sum(a.elapsed_time(b) for a, b in head_ev)], world, dev)
 
     # ---- per-kernel times: the same launches through the step-wise calls, an event between
     # consecutive calls (a second timed region of the same K steps)
@@ -332,11 +346,7 @@ def run_ours(args, rank, world, local_rank):
         pipe.submit(i, x_host, u_host, y_host, loss_host)
     e2e_end.record(pipe.d2h)
     barrier()
-    e2e_ms = e2e_start.elapsed_time(e2e_end)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms, = max_over_ranks([e2e_start.elapsed_time(e2e_end)], world, dev)
     rc = moe.device_status(ws)
     if rc != 0:
         raise RuntimeError(f"device status {rc} in the e2e region")
@@ -374,12 +384,9 @@ def run_ours(args, rank, world, local_rank):
         rc = moe.device_status(tl.ws_bwd)
         if rc != 0:
             raise RuntimeError(f"device status {rc} in the backward region")
-        f_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in tev)
-        b_ms = statistics.mean(b.elapsed_time(e) for _, b, e in tev)
-        if world > 1:
-            t = torch.tensor([f_ms, b_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            f_ms, b_ms = float(t[0]), float(t[1])
+        f_ms, b_ms = max_over_ranks([statistics.mean(a.elapsed_time(b) for a, b, _ in tev),
+                                     statistics.mean(b.elapsed_time(e) for _, b, e in tev)],
+                                    world, dev)
         bwd = (f_ms, b_ms, tl.route_out.expert_offsets[-1].item())
         del tl, dy
 
@@ -442,8 +449,7 @@ def run_ours(args, rank, world, local_rank):
                  "traffic": traffic_for(dom, n), "algorithmic_bytes": int(db),
                  "algorithmic_flops": dfl})
 
-    tokens = S * args.steps * world
-    value = tokens / (total_ms * 1e-3)
+    value = job_throughput(S, args.steps, world, total_ms)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -454,7 +460,7 @@ def run_ours(args, rank, world, local_rank):
                        rows=R, kept_fraction=round(R / (S * k), 4)),
         "roofline": roof,
         "kernels": kernels,
-        "e2e": {"value": round(S * args.steps * world / (e2e_ms * 1e-3), 1), "unit": UNIT,
+        "e2e": {"value": round(job_throughput(S, args.steps, world, e2e_ms), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": "HostPipeline.submit (pinned host in/out, 2 steps in flight) -> "
                        "moe_layer_forward (CUDA graph); L2 not flushed: inputs arrive from host"},
