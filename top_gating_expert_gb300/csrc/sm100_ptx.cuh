@@ -44,10 +44,9 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
-// Wait for the phase of parity `parity` to complete; false on abort or timeout.
-static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The bounded part of wait_bounded, out of line (the common case returns before it).
+static __device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity,
+                                                      volatile int* abort_flag, unsigned* status) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -60,6 +59,13 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
       }
     }
   }
+}
+
+// Wait for the phase of parity `parity` to complete; false on abort or timeout.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             unsigned* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bounded_slow(bar, parity, abort_flag, status);
 }
 
 // Wait that ignores the abort flag (used only to drain work already issued).
