@@ -324,8 +324,8 @@ __device__ __forceinline__ void epilogue_f32_tma(const KParams& p, const CUtenso
     __syncwarp();
     const int col = nt * BN + c0;
     if (nvr == 32) {
-      if (lane == 0 && col < p.n_valid) {
-        tma_store_2d(map, col, int(orow), smem_u32(buf));
+      if (lane == 0 && col < p.n_valid) {  // weight gradients: not read back by this step
+        tma_store_2d_evict_first(map, col, int(orow), smem_u32(buf), policy_evict_first());
         bulk_commit();
       }
     } else if (nvr > 0) {
