@@ -148,6 +148,7 @@ int down_proj(const moe_config_t& c, const void* h, int64_t a_rows, const int32_
   d.out = y; d.ldo = c.M;
   d.row_scale = row_scale;
   d.status = status;
+  d.reverse = offsets != nullptr;  // h's last rows (GEMM 1's last tiles) first
   return launch_gemm_bf16(d, st);
 }
 

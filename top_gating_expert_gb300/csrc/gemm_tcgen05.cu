@@ -101,6 +101,7 @@ struct KParams {
   // start at aoffs[g] in A and boffs[g] in B (null: koffs[g]), koffs giving the lengths
   const int32_t* aoffs;
   const int32_t* boffs;
+  int reverse;  // walk the tile schedule from its last tile (grouped rows only)
 };
 
 using namespace sm100;
@@ -418,8 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // m-tile per group when the rows are grouped), so it may be the wrong one, never one
     // outside B.
     const int mt = p.offsets ? 1 : (p.rows_dense + C::TILE_M - 1) / C::TILE_M;
-    const int g = p.offsets ? unit / p.n_tiles : 0;
-    const int nt = p.offsets ? unit % p.n_tiles : unit / (mt > 0 ? mt : 1);
+    const int ut = (p.offsets && p.reverse) ? G * p.n_tiles - 1 - unit : unit;
+    const int g = p.offsets ? ut / p.n_tiles : 0;
+    const int nt = p.offsets ? ut % p.n_tiles : unit / (mt > 0 ? mt : 1);
     if (g < G && nt < p.n_tiles) {
       const int64_t kb_bytes = int64_t(BN) * BK * 2;
       const int64_t tile_bytes = int64_t(p.K / BK) * kb_bytes;
@@ -481,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // tile t -> group g, first row m0, valid rows, n tile
   auto decode = [&](int t, int& g, int& m0, int& rows, int& nt) {
+    if (p.reverse) t = total - 1 - t;
     int lo = 0, hi = G;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -799,6 +802,7 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
   p.pf_bytes = int64_t(512) << 10;
   p.aoffs = d.aoffs;
   p.boffs = d.boffs;
+  p.reverse = (d.reverse && d.offsets && !KRAG) ? 1 : 0;
   auto kern = grouped_gemm_kernel<BN, EPI, PAIR, KRAG, MN>;
   MOE_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
   const int64_t m_tiles =

@@ -219,6 +219,9 @@ struct GemmDesc {
   // MN-major K-ragged mode: A [a_krows, c1] and B [b_krows, N] row-major, K along the rows;
   // group g takes koffs[g+1] - koffs[g] rows from row aoffs[g] of A and boffs[g] of B (null:
   // koffs[g]); rows past a tensor's end read as zeros
+  // grouped rows: walk the tiles from the last group's (GEMM 2 then starts on the rows of h
+  // that GEMM 1 wrote last, still in L2)
+  bool reverse = false;
   bool mn = false;
   int64_t a_krows = 0, b_krows = 0;
   const int32_t* aoffs = nullptr;
