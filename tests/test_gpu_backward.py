@@ -42,6 +42,9 @@ CASES = {
                                gate_p=0.5), True),
     "group_limited_k3": (_cfg(S=1024, E=32, M=128, H=256, k=3, capacity_factor=1.25, act="swiglu",
                               n_expert_groups=8, topk_groups=3), False),
+    # weight-gradient outputs whose last 256-wide N tile ends part-way (448 = 256 + 192,
+    # 320 = 256 + 64): the epilogue's chunks past N store nothing
+    "ragged_n_tiles": (_cfg(S=2048, E=8, M=320, H=448, k=2), False),
 }
 AUX, Z = 0.7, 0.3
 

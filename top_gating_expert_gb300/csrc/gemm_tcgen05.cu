@@ -324,12 +324,16 @@ __device__ __forceinline__ void epilogue_f32_tma(const KParams& p, const CUtenso
     fence_proxy_async_smem();
     __syncwarp();
     const int col = nt * BN + c0;
-    if (nvr == 32) {
-      if (lane == 0 && col < p.n_valid) {  // weight gradients: not read back by this step
+    if (lane == 0) {
+      if (nvr == 32 && col < p.n_valid)  // weight gradients: not read back by this step
         tma_store_2d_evict_first(map, col, int(orow), smem_u32(buf), policy_evict_first());
-        bulk_commit();
-      }
-    } else if (nvr > 0) {
+      // one bulk group per 32 columns, empty when nothing was stored: the wait above counts
+      // groups, so a buffer is rewritten only once the store that read it has (a chunk past
+      // N or a warp of plain stores that committed nothing would let it overwrite a buffer
+      // a TMA store is still reading)
+      bulk_commit();
+    }
+    if (nvr < 32 && nvr > 0) {
       const int cl = (lane & 7) * 4;
 #pragma unroll 1
       for (int pass = 0; pass < 8; ++pass) {
