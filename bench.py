@@ -53,8 +53,8 @@ def parse():
 
 
 def preset_for(args) -> dict:
-    from top_gating_expert_gb300.inputs import CONFIGS
-    cfg = dict(CONFIGS[args.config])
+    from top_gating_expert_gb300.inputs import PRESETS
+    cfg = dict(PRESETS[args.config])
     for kv in args.override:
         key, val = kv.split("=", 1)
         if key not in cfg:
@@ -197,7 +197,7 @@ def run_ours(args, rank, world, local_rank):
     import torch.distributed as dist
     from top_gating_expert_gb300 import _native as N
     from top_gating_expert_gb300 import moe
-    from top_gating_expert_gb300.inputs import CONFIGS, make_inputs
+    from top_gating_expert_gb300.inputs import PRESETS, make_inputs
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
@@ -560,7 +560,7 @@ def cpu_baseline(cfg, n, inp, target_flops=1.2e12):
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    from top_gating_expert_gb300.inputs import CONFIGS, make_inputs
+    from top_gating_expert_gb300.inputs import PRESETS, make_inputs
     n = args.config
     cfg = preset_for(args)
     inp = make_inputs(cfg, preset_number=n)

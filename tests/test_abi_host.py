@@ -7,7 +7,7 @@ import math
 import pytest
 
 from top_gating_expert_gb300 import _native as N
-from top_gating_expert_gb300.inputs import CONFIGS, preset
+from top_gating_expert_gb300.inputs import PRESETS, preset
 
 
 def test_exports_every_declared_symbol(native_lib):
@@ -28,7 +28,7 @@ def test_status_strings(native_lib):
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
 def test_presets_validate_and_capacity(native_lib, n):
     from top_gating_expert_gb300 import moe
-    cfg = CONFIGS[n]
+    cfg = PRESETS[n]
     assert moe.validate(cfg) == 0
     want_C = None if cfg["capacity_factor"] <= 0 else math.ceil(
         cfg["capacity_factor"] * cfg["k"] * (cfg["S"] // cfg["G"]) / cfg["E"])
@@ -45,10 +45,10 @@ def test_presets_validate_and_capacity(native_lib, n):
 
 def test_capacity_values(native_lib):
     from top_gating_expert_gb300 import moe
-    assert moe.capacity(CONFIGS[1]) == 64
-    assert moe.capacity(CONFIGS[2]) == 16
-    assert moe.capacity(CONFIGS[5]) == 2560
-    assert moe.capacity(CONFIGS[3]) is None
+    assert moe.capacity(PRESETS[1]) == 64
+    assert moe.capacity(PRESETS[2]) == 16
+    assert moe.capacity(PRESETS[5]) == 2560
+    assert moe.capacity(PRESETS[3]) is None
 
 
 BAD = [
@@ -92,7 +92,7 @@ def test_unsupported_shapes(native_lib, over):
 def test_compute_entry_points_check_arguments_on_host(native_lib):
     """Null pointers and short workspaces fail before any launch (no GPU needed)."""
     from top_gating_expert_gb300 import moe
-    c = moe.make_config(CONFIGS[2])
+    c = moe.make_config(PRESETS[2])
     L = native_lib
     out = N.MoeRouteOut()
     assert L.moe_route(ctypes.byref(c), None, None, ctypes.byref(out), None, 0, None) == -1
@@ -117,7 +117,7 @@ def test_compute_entry_points_check_arguments_on_host(native_lib):
                               need, None) == -1  # random routing needs u
     assert L.moe_router_route(ctypes.byref(c), fake, fake, None, fake, None, ctypes.byref(out2), fake,
                               16, None) == -3
-    c32 = moe.make_config(CONFIGS[1])
+    c32 = moe.make_config(PRESETS[1])
     assert L.moe_router_route(ctypes.byref(c32), fake, fake, None, fake, None, ctypes.byref(out2),
                               fake, moe.workspace_bytes(c32, N.MOE_WS_STEP), None) == -1  # fp32 needs logits_out
     assert L.moe_get_device_status(None, None) == -1
@@ -129,7 +129,7 @@ def test_backward_host_checks(native_lib):
     """The backward's workspace kind and its argument checks, before any launch."""
     from top_gating_expert_gb300 import moe
     L = native_lib
-    c = moe.make_config(CONFIGS[2])
+    c = moe.make_config(PRESETS[2])
     step = moe.workspace_bytes(c, N.MOE_WS_STEP)
     bwd = moe.workspace_bytes(c, N.MOE_WS_BACKWARD)
     assert bwd > step
@@ -149,7 +149,7 @@ def test_backward_host_checks(native_lib):
     assert L.moe_layer_backward(ctypes.byref(c), *args(), *tail(fwd_bytes=16)) == -3
     g0 = N.MoeGrads(**{f: (1 << 20) for f in N.GRAD_FIELDS}); g0.dW_in = None
     assert L.moe_layer_backward(ctypes.byref(c), *args(), *tail(grads=g0)) == -1
-    c32 = moe.make_config(CONFIGS[1])
+    c32 = moe.make_config(PRESETS[1])
     assert L.moe_layer_backward(ctypes.byref(c32), *args(), *tail()) == -2   # bf16 only
     cu = moe.make_config(preset(2, uniform_assignment=1, random_routing=0))
     assert L.moe_layer_backward(ctypes.byref(cu), *args(), *tail()) == -2    # forward-only ids

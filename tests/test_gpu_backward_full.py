@@ -20,7 +20,7 @@ from oracle import moe_backward as B
 from oracle import moe_oracle as O
 from gpu_util import RTOL, assert_close, oracle_cfg, to_np
 from top_gating_expert_gb300 import moe
-from top_gating_expert_gb300.inputs import CONFIGS, make_inputs
+from top_gating_expert_gb300.inputs import PRESETS, make_inputs
 
 pytestmark = pytest.mark.gpu
 AUX, Z = 0.7, 0.3
@@ -42,7 +42,7 @@ def _expert_backward(x_rows, a, e, act, do, mask):
 def test_backward_full_size_sampled(n, native_lib):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    cfg = CONFIGS[n]
+    cfg = PRESETS[n]
     inp = make_inputs(cfg, preset_number=n)
     layer = moe.MoeLayer(cfg, inp.host)
     layer.enable_backward(inp.host)

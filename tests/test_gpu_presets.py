@@ -11,7 +11,7 @@ from oracle import moe_oracle as O
 from gpu_util import (LOGIT_RTOL, RTOL, assert_close, compare_route, near_tie_tokens, oracle_cfg,
                       route_np, to_np)
 from top_gating_expert_gb300 import moe
-from top_gating_expert_gb300.inputs import CONFIGS, make_inputs
+from top_gating_expert_gb300.inputs import PRESETS, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 def test_preset_full_size(n, native_lib):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    cfg = CONFIGS[n]
+    cfg = PRESETS[n]
     inp = make_inputs(cfg, preset_number=n)
     layer = moe.MoeLayer(cfg, inp.host)
     dev = layer.device

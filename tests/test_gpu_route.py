@@ -8,7 +8,7 @@ import torch
 from oracle import moe_oracle as O
 from gpu_util import compare_route, gpu_route, oracle_cfg, route_np
 from top_gating_expert_gb300 import moe
-from top_gating_expert_gb300.inputs import CONFIGS, make_inputs
+from top_gating_expert_gb300.inputs import PRESETS, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -66,7 +66,7 @@ def test_route_parity_cases(name):
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
 def test_route_parity_presets_full_size(n):
     """Full-size routing on the preset's own logits (oracle router, rounded to fp32)."""
-    cfg = CONFIGS[n]
+    cfg = PRESETS[n]
     inp = make_inputs(cfg, preset_number=n, names=("x", "W_g", "u", "bias"))
     logits = O.router_logits(inp.np["x"], inp.np["W_g"], inp.np.get("bias")).astype(np.float32)
     out, status = gpu_route(cfg, logits, inp.np["u"] if cfg["random_routing"] else None)

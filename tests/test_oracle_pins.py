@@ -11,7 +11,7 @@ import torch
 
 from oracle import moe_oracle as O
 from bruteforce import bf_route, bf_layer, bf_capacity
-from top_gating_expert_gb300.inputs import CONFIGS, make_inputs, preset
+from top_gating_expert_gb300.inputs import PRESETS, make_inputs, preset
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -107,7 +107,7 @@ def test_layer_matches_brute_force(act, cf, rr, n_shared):
 @pytest.mark.parametrize("n", [1, 2, 5])
 def test_capacity_is_2N_over_GE(n):
     """cf = 1, k = 2 reproduces GShard's 2N/(G*E); cf = 1.25 scales it."""
-    c = CONFIGS[n]
+    c = PRESETS[n]
     C = O.capacity(c["S"], c["G"], c["E"], c["k"], c["capacity_factor"])
     want = {1: 2 * 256 // (1 * 8), 2: 2 * 16384 // (16 * 128), 5: int(1.25 * 2 * 65536 // 64)}[n]
     assert C == want == bf_capacity(c["S"], c["G"], c["E"], c["k"], c["capacity_factor"])
@@ -257,7 +257,7 @@ def test_two_shared_experts_equal_one_with_concatenated_hidden():
 # ---------------------------------------------------------------- invariants on the presets
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
 def test_route_invariants_on_presets(n):
-    cfg = CONFIGS[n]
+    cfg = PRESETS[n]
     inp = make_inputs(cfg, preset_number=n, names=("x", "W_g", "u", "bias"))
     logits = O.router_logits(inp.np["x"], inp.np["W_g"], inp.np.get("bias")).astype(np.float32)
     r = O.route(logits, cfg, inp.np["u"])

@@ -35,7 +35,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 # Workload presets. capacity_factor <= 0 means dropless.
-CONFIGS = {
+PRESETS = {
     1: dict(name="tiny_gshard_top2_fp32", S=256, G=1, E=8, M=64, H=128, k=2,
             capacity_factor=1.0, random_routing=1, n_shared=0, H_shared=0,
             act="relu", dtype="f32", bias=False),
@@ -60,7 +60,7 @@ _BIAS_LAMBDA = 0.33
 
 def preset(n: int, **overrides) -> dict:
     """Return a copy of preset ``n`` with fields overridden (e.g. a smaller S)."""
-    cfg = dict(CONFIGS[n])
+    cfg = dict(PRESETS[n])
     cfg.update(overrides)
     return cfg
 
