@@ -36,6 +36,10 @@ CASES = {
     # shared experts (dense segment) + routed SwiGLU, k = 6
     "shared_swiglu_k6": _cfg(S=2048, E=16, M=256, H=256, k=6, act="swiglu", n_shared=2,
                              H_shared=192),
+    # the fused router with E = 64, k = 2 over 24 chunks (2 groups of 1500 tokens, the last
+    # chunk of each group ragged), random routing and capacity
+    "relu_E64_router_pairs": _cfg(S=3000, G=2, E=64, M=512, H=512, capacity_factor=1.0,
+                                  random_routing=1),
     # the fp32 path (plain FMA), tiny GShard top-2 with random routing
     "f32_tiny": preset(1),
     "f32_swiglu_shared": _cfg(S=200, G=2, E=4, M=32, H=128, k=2, capacity_factor=1.0,
