@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ut = (p.offsets && p.reverse) ? G * p.n_tiles - 1 - unit : unit;
     const int g = p.offsets ? ut / p.n_tiles : 0;
     const int nt = p.offsets ? ut % p.n_tiles : unit / (mt > 0 ? mt : 1);
-    if (g < G && nt < p.n_tiles) {
+    if (ut >= 0 && g < G && nt < p.n_tiles) {  // (reversed: no guess past the first tile)
       const int64_t kb_bytes = int64_t(BN) * BK * 2;
       const int64_t tile_bytes = int64_t(p.K / BK) * kb_bytes;
       const char* base = p.pfB + (int64_t(g) * p.n_tiles + nt) * tile_bytes;
