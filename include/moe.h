@@ -328,7 +328,12 @@ int moe_combine(const moe_config_t* cfg, const void* y_perm, const moe_route_out
  * (when n_shared > 0) and moe_combine, with the intermediates carved from ws
  * (MOE_WS_LAYER bytes). logits_out (float [S, E]) receives the router logits when
  * non-null. W_*_packed / Ws_*_packed come from the pack calls above; bias, u, residual
- * and the shared weights may be NULL when unused.
+ * and the shared weights may be NULL when unused. Results are those of the separate calls
+ * bit for bit; the launches differ: the routing's last kernel also does the dispatch
+ * gather (and brings GEMM 1's first weight tiles into L2), and the 64 rows of h after the
+ * kept ones are zeroed in ws for moe_layer_backward. Only the first 256 bytes of ws (the
+ * status word and a ticket) must be zero when it is first used; nothing else in it is read
+ * before it is written.
  */
 int moe_layer_forward(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
                       const void* W_in_packed, const void* W_out_packed, const void* Ws_in_packed,
