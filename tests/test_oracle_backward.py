@@ -178,3 +178,24 @@ def _z_sign_flipped(logits, r, dgate, cfg, aux_coef, z_coef):
 def test_planted_router_mistake_is_caught(name, fn, monkeypatch):
     monkeypatch.setattr(B, "router_logit_grad", fn)
     assert not _pins_ok(), name
+
+
+def _pnorm_power_dropped(logits, r, dgate, cfg, aux_coef, z_coef):
+    """p-norm gates with g_j in place of g_j^p in the Jacobian's second term."""
+    if cfg.get("gate_norm") != "pnorm":
+        return _orig_router(logits, r, dgate, cfg, aux_coef, z_coef)
+    dl = _orig_router(logits, r, np.zeros_like(dgate), cfg, aux_coef, z_coef)  # aux and z only
+    ids = r["expert_id"]
+    g = O.normalised_gates(logits, ids, "pnorm", float(cfg["gate_p"]))
+    inner = np.sum(g * dgate, axis=1, keepdims=True)
+    np.add.at(dl, (np.repeat(np.arange(cfg["S"]), cfg["k"]), ids.ravel()),
+              (g * dgate - g * inner).ravel())
+    return dl
+
+
+def test_planted_pnorm_mistake_is_caught(monkeypatch):
+    case = next(c for c in CASES if c.get("norm") == "pnorm" and c.get("p") == 2.0)
+    check_all(case)  # the pin holds for the oracle as written
+    monkeypatch.setattr(B, "router_logit_grad", _pnorm_power_dropped)
+    with pytest.raises(AssertionError):
+        check_all(case)
