@@ -328,11 +328,13 @@ class MoeLayer:
         self.y = torch.empty((self.cfg.S, self.cfg.M), dtype=dt, device=dev)
         self.device = dev
 
-    def forward(self, x, u=None, residual=None, stream=None, out=None):
+    def forward(self, x, u=None, residual=None, stream=None, out=None, route_out=None):
+        """y (self.y unless `out` is given); the routing outputs go to self.route_out unless
+        `route_out` (a RouteOutputs of this config) is given."""
         y = self.y if out is None else out
         layer_forward(self.cfg, x, self.W_g, self.bias, self.W_in_packed, self.W_out_packed,
                       self.Ws_in_packed, self.Ws_out_packed, u, residual, y, self.logits,
-                      self.route_out, self.ws, stream)
+                      self.route_out if route_out is None else route_out, self.ws, stream)
         return y
 
     def enable_backward(self, weights: dict):
@@ -406,7 +408,9 @@ class HostPipeline:
     buffer set) on the compute stream, and copies y and the two losses device->host on a
     second copy stream, so step i's input copy and step i-1's output copy overlap the
     compute of the steps around them. Buffer set i % depth is reused only after step
-    i - depth's output copy has finished."""
+    i - depth's output copy has finished. Each buffer set has its own routing outputs
+    (``route[i % depth]`` holds step i's), so the output copy reads the two losses from
+    them directly."""
 
     def __init__(self, layer: MoeLayer, has_u: bool, depth: int = 2):
         dev = layer.device
@@ -417,7 +421,7 @@ class HostPipeline:
         self.u = [torch.empty(c.S, dtype=torch.float32, device=dev) if has_u else None
                   for _ in range(depth)]
         self.y = [torch.empty((c.S, c.M), dtype=dt, device=dev) for _ in range(depth)]
-        self.loss = [torch.empty(2, dtype=torch.float32, device=dev) for _ in range(depth)]
+        self.route = [RouteOutputs.allocate(c, dev) for _ in range(depth)]
         self.compute = torch.cuda.current_stream(dev)
         self.h2d = torch.cuda.Stream(device=dev)
         self.d2h = torch.cuda.Stream(device=dev)
@@ -432,13 +436,11 @@ class HostPipeline:
             side = torch.cuda.Stream(device=dev)
             side.wait_stream(self.compute)
             with torch.cuda.stream(side):
-                layer.forward(self.x[b], self.u[b], out=self.y[b])
+                layer.forward(self.x[b], self.u[b], out=self.y[b], route_out=self.route[b])
             self.compute.wait_stream(side)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                layer.forward(self.x[b], self.u[b], out=self.y[b])
-                self.loss[b][0:1].copy_(layer.route_out.aux_loss)
-                self.loss[b][1:2].copy_(layer.route_out.z_loss)
+                layer.forward(self.x[b], self.u[b], out=self.y[b], route_out=self.route[b])
             self.graphs.append(g)
         torch.cuda.synchronize(dev)
 
@@ -458,5 +460,6 @@ class HostPipeline:
             if y_host is not None:
                 y_host.copy_(self.y[b], non_blocking=True)
             if loss_host is not None:
-                loss_host.copy_(self.loss[b], non_blocking=True)
+                loss_host[0:1].copy_(self.route[b].aux_loss, non_blocking=True)
+                loss_host[1:2].copy_(self.route[b].z_loss, non_blocking=True)
             self.ev_free[b].record(self.d2h)
