@@ -128,6 +128,7 @@ int up_proj(const moe_config_t& c, const void* A, int64_t a_rows, const int32_t*
   d.offsets = offsets; d.groups = groups; d.rows_dense = rows_dense;
   d.out = h; d.ldo = H;
   d.status = status;
+  d.out_keep = true;  // GEMM 2 reads h next
   return launch_gemm_bf16(d, st);
 }
 
@@ -149,6 +150,7 @@ int down_proj(const moe_config_t& c, const void* h, int64_t a_rows, const int32_
   d.row_scale = row_scale;
   d.status = status;
   d.reverse = offsets != nullptr;  // h's last rows (GEMM 1's last tiles) first
+  d.out_keep = true;               // the combine reads y_perm next
   return launch_gemm_bf16(d, st);
 }
 

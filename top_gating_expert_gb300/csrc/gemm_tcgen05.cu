@@ -102,6 +102,7 @@ struct KParams {
   const int32_t* aoffs;
   const int32_t* boffs;
   int reverse;  // walk the tile schedule from its last tile (grouped rows only)
+  int out_keep; // bf16 output read by the next kernel: stores marked evict-last in L2
 };
 
 using namespace sm100;
@@ -275,8 +276,14 @@ __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, 
           pk0[j] = pack_bf16x2(a0, a1);
           pk1[j] = pack_bf16x2(b0, b1);
         }
-        store_bf16x16(out + c0, pk0);
-        store_bf16x16(out + c0 + 16, pk1);
+        if (p.out_keep) {
+          const uint64_t q = policy_evict_last();
+          store_bf16x16_hint(out + c0, pk0, q);
+          store_bf16x16_hint(out + c0 + 16, pk1, q);
+        } else {
+          store_bf16x16(out + c0, pk0);
+          store_bf16x16(out + c0 + 16, pk1);
+        }
       }
     }
   }
@@ -807,6 +814,7 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
   p.aoffs = d.aoffs;
   p.boffs = d.boffs;
   p.reverse = (d.reverse && d.offsets && !KRAG) ? 1 : 0;
+  p.out_keep = (d.out_keep && d.offsets && !KRAG && d.a_rows <= int64_t(d.groups) * C::TILE_M) ? 1 : 0;
   auto kern = grouped_gemm_kernel<BN, EPI, PAIR, KRAG, MN>;
   MOE_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
   const int64_t m_tiles =

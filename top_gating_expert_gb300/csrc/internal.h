@@ -222,6 +222,9 @@ struct GemmDesc {
   // grouped rows: walk the tiles from the last group's (GEMM 2 then starts on the rows of h
   // that GEMM 1 wrote last, still in L2)
   bool reverse = false;
+  // the output is read by the next kernel (GEMM 1's h by GEMM 2): with about one m-tile a
+  // group, its stores are marked evict-last in L2
+  bool out_keep = false;
   bool mn = false;
   int64_t a_krows = 0, b_krows = 0;
   const int32_t* aoffs = nullptr;

@@ -276,6 +276,21 @@ __device__ __forceinline__ void store_bf16x16(void* dst, const uint32_t (&p)[8])
   d[0] = make_uint4(p[0], p[1], p[2], p[3]);
   d[1] = make_uint4(p[4], p[5], p[6], p[7]);
 }
+// The same with an L2 cache policy (evict-last: output the next kernel reads soon).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t q;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(q));
+  return q;
+}
+__device__ __forceinline__ void store_bf16x16_hint(void* dst, const uint32_t (&p)[8], uint64_t q) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "r"(p[0]),
+               "r"(p[1]), "r"(p[2]), "r"(p[3]), "l"(q)
+               : "memory");
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(
+                   static_cast<char*>(dst) + 16),
+               "r"(p[4]), "r"(p[5]), "r"(p[6]), "r"(p[7]), "l"(q)
+               : "memory");
+}
 
 
 }  // namespace sm100
