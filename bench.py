@@ -47,6 +47,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-backward", action="store_true",
                    help="skip the training-step (forward + backward) measurement")
+    p.add_argument("--no-variants", action="store_true",
+                   help="skip the routing-variant measurement")
     p.add_argument("--override", action="append", default=[], metavar="KEY=VALUE",
                    help="change a field of the preset (smaller cases for profiler captures)")
     return p.parse_args()
@@ -404,6 +406,11 @@ def run_ours(args, rank, world, local_rank):
         bwd = (f_ms, b_ms, tl.route_out.expert_offsets[-1].item())
         del tl, dy
 
+    variants = None
+    if fused and not args.no_variants:
+        variants = time_variants(args, cfg, c, x, layer, bias, u, flush, barrier, world, dev,
+                                 per_kernel["router_route"])
+
     if rank != 0:
         return None
 
@@ -531,9 +538,86 @@ def run_ours(args, rank, world, local_rank):
             "bound": "hbm" if t_bytes >= t_flops else "tensor",
             "roofline_frac": round(max(t_bytes, t_flops) / b_ms, 4),
         }
+    if variants is not None:
+        line["variants"] = variants
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, n, inp)
     return line
+
+
+# ------------------------------------------------------------------ routing variants
+# Each entry: the preset's fields it changes. Group-limited routing and the gate
+# normalisations: Lec16 "DeepSeek V3 MoE" (8 expert groups, 4 kept, TopK(Softmax) gates),
+# MegaBlocks router chapter §2 (p-norm of the top-k weights, the uniform-assignment switch).
+VARIANTS = {
+    "group_limited_8x4": dict(n_expert_groups=8, topk_groups=4),
+    "gates_unnormalised": dict(gate_norm="none"),
+    "gates_pnorm2": dict(gate_norm="pnorm", gate_p=2.0),
+    "uniform_assignment": dict(uniform_assignment=1, random_routing=0),
+    "top4": dict(k=4, random_routing=0),
+    # DeepSeek-V3's routing over the preset's tokens: 256 experts in 8 groups, 4 kept, top-8,
+    # un-normalised gates, no capacity (a seeded random router of 256 rows)
+    "deepseek_v3_routing": dict(E=256, k=8, n_expert_groups=8, topk_groups=4, gate_norm="none",
+                                capacity_factor=0.0, random_routing=0, G=1),
+}
+
+
+def time_variants(args, cfg, c, x, layer, bias, u, flush, barrier, world, dev, default_ms):
+    """moe_router_route under each routing variant on the preset's tokens (x and, where E is
+    unchanged, W_g), L2 flushed before each call, CUDA events around it; bytes as for the
+    default routing (x and W_g in, per-assignment outputs, the inverse map)."""
+    import torch
+    from top_gating_expert_gb300 import moe
+
+    P = peaks()
+    res = {"what": "moe_router_route (router GEMM + softmax + variant top-k + slots + rows), "
+                   "L2 flushed before each call; default routing for comparison",
+           "default_ms": round(default_ms, 5)}
+    for name, kw in VARIANTS.items():
+        vc = dict(cfg, **kw)
+        if vc["S"] % vc["G"] or vc["E"] % vc.get("n_expert_groups", 1) or vc["k"] > vc["E"]:
+            continue
+        cv = moe.make_config(vc)
+        if moe.validate(cv) != 0:
+            res[name] = {"skipped": "configuration not valid for this preset"}
+            continue
+        if vc["E"] != cfg["E"]:
+            g = torch.Generator().manual_seed(31)
+            W_g = (torch.randn((vc["E"], vc["M"]), generator=g) / vc["M"] ** 0.5).to(x.dtype).to(dev)
+            b = None
+        else:
+            W_g, b = layer.W_g, bias
+        uv = u if vc["random_routing"] else None
+        outv = moe.RouteOutputs.allocate(cv, dev)
+        wsv = moe.workspace(cv, moe.N.MOE_WS_STEP, device=dev)
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            moe.router_route(cv, x, W_g, b, uv, None, outv, wsv)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        barrier()
+        for s in range(args.steps):
+            flush.zero_()
+            evs[s][0].record()
+            moe.router_route(cv, x, W_g, b, uv, None, outv, wsv)
+            evs[s][1].record()
+        barrier()
+        rc = moe.device_status(wsv)
+        if rc != 0:
+            raise RuntimeError(f"device status {rc} in the {name} variant")
+        ms, = max_over_ranks([sum(a.elapsed_time(e) for a, e in evs) / args.steps], world, dev)
+        R = int(outv.expert_offsets[-1].item())
+        S, E, M, k = vc["S"], vc["E"], vc["M"], vc["k"]
+        nb = (S * M * 2 + E * M * 2 + (E * 4 if b is not None else 0) + (S * 4 if uv is not None else 0)
+              + S * k * (4 + 4 + 4 + 1 + 4) + R * 8)
+        gbs = nb / (ms * 1e-3) / 1e9
+        res[name] = {"fields": {kk: vv for kk, vv in kw.items()}, "ms": round(ms, 5),
+                     "vs_default": round(ms / default_ms, 3), "rows": R,
+                     "kept_fraction": round(R / (S * k), 4), "bytes": int(nb),
+                     "GB/s": round(gbs, 1), "hbm_frac": round(gbs / P["hbm"], 4),
+                     "TFLOP/s": round(2.0 * S * M * E / (ms * 1e-3) / 1e12, 2)}
+        del outv, wsv
+    return res
 
 
 # ------------------------------------------------------------------ the oracle on the host

@@ -83,6 +83,27 @@ def test_valid_variant_configs(native_lib):
         assert moe.validate(preset(2, **over)) == 0, over
 
 
+@pytest.mark.parametrize("n", [2, 3, 4, 5])
+def test_bench_routing_variants_validate(native_lib, n):
+    """Every routing variant the benchmark times is a valid configuration of each bf16 preset."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    from top_gating_expert_gb300 import moe
+    for name, over in bench.VARIANTS.items():
+        assert moe.validate(preset(n, **over)) == 0, (n, name)
+
+
+def test_group_index_by_multiply_shift():
+    """The variant top-k filter finds an expert's group as (e * ceil(2^24 / gsz)) >> 24 in
+    32-bit arithmetic; exact for every expert index and group size up to 256."""
+    for gsz in range(1, 257):
+        m = ((1 << 24) + gsz - 1) // gsz
+        for e in range(256):
+            assert ((e * m) & 0xFFFFFFFF) >> 24 == e // gsz
+
+
 @pytest.mark.parametrize("over", [dict(M=1000), dict(H=4000), dict(act="swiglu", H=4160)])
 def test_unsupported_shapes(native_lib, over):
     from top_gating_expert_gb300 import moe

@@ -104,34 +104,51 @@ __device__ __forceinline__ bool ranks_before(float v, int i, float w, int j) {
 // Group-limited routing (one call per token lane, all TPT lanes of a token together): the
 // token's best logit in each of the ng contiguous expert groups of gsz (non-finite logits
 // count as -inf), then the bit mask of the tg groups ranked first, ties to the lower
-// group.
+// group. Lane sub takes groups sub, sub + TPT, ... (it reads a group's logits from a
+// rotated start, so the lanes of a warp fall on different banks), ranks each of them
+// against the ng maxima broadcast one by one, and the lanes' bits are OR-ed together.
 template <int TPT>
 __device__ __forceinline__ unsigned group_mask(const float* rowp, bool tok, int sub, unsigned tmask,
                                             int ng, int tg, int gsz) {
-  float gm[16];
+  constexpr int kSlots = (16 + TPT - 1) / TPT;  // ng <= 16
+  float gs[kSlots];
+  int before[kSlots];
+  const int rot = sub % gsz;
 #pragma unroll
-  for (int g = 0; g < 16; ++g) {
+  for (int s = 0; s < kSlots; ++s) {
+    const int g = sub + s * TPT;
     float lm = -INFINITY;
-    if (g < ng && tok) {
-      const int lo = g * gsz, hi = lo + gsz;
-      for (int e = lo + ((sub - lo) & (TPT - 1)); e < hi; e += TPT) {
-        const float v = rowp[e];
+    if (tok && g < ng) {
+      const float* gp = rowp + g * gsz;
+      int r = rot;
+      for (int q = 0; q < gsz; ++q) {
+        const float v = gp[r];
         if (isfinite(v)) lm = fmaxf(lm, v);
+        r = r + 1 == gsz ? 0 : r + 1;
       }
     }
+    gs[s] = lm;
+    before[s] = 0;
+  }
+  for (int h = 0; h < ng; ++h) {  // group h's maximum sits in lane h % TPT, slot h / TPT
+    const int hs = h / TPT;
+    float mine = gs[0];
 #pragma unroll
-    for (int off = TPT >> 1; off > 0; off >>= 1) lm = fmaxf(lm, __shfl_xor_sync(tmask, lm, off, TPT));
-    gm[g] = lm;
+    for (int s = 1; s < kSlots; ++s)
+      if (s == hs) mine = gs[s];
+    const float vh = __shfl_sync(tmask, mine, h % TPT, TPT);
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s)
+      if (vh > gs[s] || (vh == gs[s] && h < sub + s * TPT)) ++before[s];
   }
   unsigned mask = 0u;
 #pragma unroll
-  for (int g = 0; g < 16; ++g) {
-    int before = 0;
-#pragma unroll
-    for (int h = 0; h < 16; ++h)
-      if (h < ng && (gm[h] > gm[g] || (gm[h] == gm[g] && h < g))) ++before;
-    if (g < ng && before < tg) mask |= 1u << g;
+  for (int s = 0; s < kSlots; ++s) {
+    const int g = sub + s * TPT;
+    if (g < ng && before[s] < tg) mask |= 1u << g;
   }
+#pragma unroll
+  for (int off = TPT >> 1; off > 0; off >>= 1) mask |= __shfl_xor_sync(tmask, mask, off, TPT);
   return mask;
 }
 
@@ -201,6 +218,10 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
     // group-limited routing: the groups this token may take experts from
     const unsigned gmask = (VAR && a.ng > 1) ? group_mask<TPT>(rowp, tok, sub, tmask, a.ng, a.tg, a.gsz)
                                              : 0xffffffffu;
+    // an expert's group e / gsz as (e * gm24) >> 24 with gm24 = ceil(2^24 / gsz): exact for
+    // e, gsz <= 256 (the error term e * (gm24 * gsz - 2^24) stays below 2^24); 0 (group 0,
+    // whose bit is set) when the routing is not group-limited
+    const unsigned gm24 = (VAR && a.ng > 1) ? ((1u << 24) + unsigned(a.gsz) - 1u) / unsigned(a.gsz) : 0u;
     float m = -INFINITY;
     bool bad = false;
     if (tok) {
@@ -214,7 +235,7 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
         m = fmaxf(m, v);
         // local sorted list; experts arrive in increasing index, so an equal logit ranks
         // after the ones already held. Once placed, the rest shift down one slot.
-        if ((!VAR || a.ng <= 1 || ((gmask >> (e / a.gsz)) & 1u)) &&
+        if ((!VAR || ((gmask >> ((unsigned(e) * gm24) >> 24)) & 1u)) &&
             ranks_before(v, e, top[K - 1], id[K - 1])) {
           float cv = v;
           int ci = e;
