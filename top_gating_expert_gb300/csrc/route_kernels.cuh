@@ -191,7 +191,7 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
   __shared__ float s_inv[kThreads], s_pp[kT];
   __shared__ uint8_t s_id[kThreads * kMaxK];
   __shared__ uint8_t s_cand[kThreads];
-  __shared__ int s_wc[kWarps][kMaxE];
+  __shared__ uint8_t s_rk[kThreads * kMaxK];  // rank within the warp of each candidate
   __shared__ int s_route[kMaxE];
   __shared__ float s_z[kT / 32];
 
@@ -372,42 +372,56 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
   }
 
   // rank of each candidate among the chunk's earlier candidates of the same (j, e); the
-  // first kThreads threads hold one token each
+  // first kThreads threads hold one token each. All K choice ranks at once: per (j, warp,
+  // e) counts in shared memory (over the staged logits, which nothing reads any more), one
+  // scan over the warps per (j, e), then each token's K ranks -- three barriers for any K.
+  int* s_cnt = reinterpret_cast<int*>(s_log);  // [K][kWarps][E] (16 K E <= 512 (E + TPT) bytes)
+  for (int x = tid; x < K * kWarps * E; x += kT) s_cnt[x] = 0;
+  __syncthreads();
   const bool valid = tid < nt;
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int j = 0; j < K; ++j) {
-    for (int x = tid; x < kWarps * E; x += kT) s_wc[x / E][x % E] = 0;
-    __syncthreads();
-    int e = -1, rk = 0;
-    if (tid < kThreads) {
+  if (tid < kThreads) {
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
       const bool cnd = valid && ((s_cand[tid] >> j) & 1u);
-      e = cnd ? int(s_id[tid * kMaxK + j]) : -1;
+      const int e = cnd ? int(s_id[tid * kMaxK + j]) : -1;
       const int key = cnd ? e : (1024 + lane);
       const unsigned peers = __match_any_sync(0xffffffffu, key);
-      rk = __popc(peers & lt_mask);
-      if (cnd && rk == 0) s_wc[warp][e] = __popc(peers);
+      const int rk = __popc(peers & lt_mask);
+      s_rk[tid * kMaxK + j] = uint8_t(rk);  // < 32
+      if (cnd && rk == 0) s_cnt[(j * kWarps + warp) * E + e] = __popc(peers);
     }
-    __syncthreads();
-    for (int e2 = tid; e2 < E; e2 += kT) {
-      int run = 0;
+  }
+  __syncthreads();
+  for (int x = tid; x < K * E; x += kT) {
+    const int j = x / E, e2 = x - j * E;
+    int run = 0;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const int v = s_wc[w][e2];
-        s_wc[w][e2] = run;
-        run += v;
-      }
-      a.hist[(size_t(c) * K + j) * E + e2] = run;
+    for (int w = 0; w < kWarps; ++w) {
+      int* cw = s_cnt + (j * kWarps + w) * E + e2;
+      const int v = *cw;
+      *cw = run;
+      run += v;
     }
-    __syncthreads();
-    if (valid) a.rank[size_t(t0 + tid) * K + j] = e >= 0 ? s_wc[warp][e] + rk : -1;
-    __syncthreads();
+    a.hist[(size_t(c) * K + j) * E + e2] = run;
+  }
+  __syncthreads();
+  if (valid) {
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      const bool cnd = (s_cand[tid] >> j) & 1u;
+      const int e = int(s_id[tid * kMaxK + j]);
+      a.rank[size_t(t0 + tid) * K + j] =
+          cnd ? s_cnt[(j * kWarps + warp) * E + e] + int(s_rk[tid * kMaxK + j]) : -1;
+    }
   }
 }
 
 // One CTA per chunk: stage the chunk's logits (contiguous rows t0..t0+nt-1, coalesced) into
-// padded shared memory, then topk_chunk.
+// padded shared memory, then topk_chunk. With 8 lanes a token and k <= 3 two CTAs share an
+// SM (32 registers a thread).
 template <int K, int TPT, bool VAR>
-__global__ void __launch_bounds__(kThreads * TPT) route_topk_kernel(RouteArgs a) {
+__global__ void __launch_bounds__(kThreads * TPT, (TPT == 8 && K <= 3) ? 2 : 1) route_topk_kernel(RouteArgs a) {
   constexpr int kT = kThreads * TPT;
   extern __shared__ float s_log[];  // [kThreads][E + TPT] (padded: conflict-free lanes)
   const int c = blockIdx.x;
