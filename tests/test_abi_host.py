@@ -53,6 +53,7 @@ def test_capacity_values(native_lib):
 
 BAD = [
     dict(S=100, G=3),             # S % G != 0
+    dict(S=0, G=1),               # no tokens: an empty batch is rejected, not launched
     dict(E=0), dict(E=300),       # expert count
     dict(k=0), dict(k=9),         # k range
     dict(k=3, random_routing=1),  # random routing needs k == 2
