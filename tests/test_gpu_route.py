@@ -36,6 +36,11 @@ CASES = {
     "E128_k2_groups_rr": _case(8192, 8, 128, 2, 1.0, 1),
     "E64_k6_dropless": _case(5000, 1, 64, 6, 0.0, 0),
     "E48_k4_cap": _case(3000, 2, 48, 4, 2.0, 0),
+    # 4 <= k <= lanes a token: the selection keeps only logits at or above the smallest lane
+    # maximum; with ties at that bound, all-equal rows and a dominant expert
+    "coarse_ties_E128_k6": _case(1500, 3, 128, 6, 1.0, 0, kind="coarse"),
+    "all_equal_E200_k8": _case(640, 1, 200, 8, 0.0, 0, kind="equal"),
+    "skew_E96_k5": _case(1200, 1, 96, 5, 1.5, 0, kind="skew"),
 }
 
 

@@ -47,6 +47,8 @@ CASES = {
     # the fp32 path with groups and TopK(Softmax) gates
     "f32_groups_none": _cfg(S=300, E=12, k=3, M=32, H=64, dtype="f32", n_expert_groups=3,
                             topk_groups=2, gate_norm="none", capacity_factor=1.0),
+    # no variant, top-6 of 128 (the selection's threshold pass) through both entry points
+    "plain_top6_E128": _cfg(S=900, G=3, E=128, k=6, capacity_factor=1.0),
     # 16 single-expert groups (E = 16): group-limited = plain top-k over the kept groups
     "sixteen_groups": _cfg(S=640, E=16, k=4, n_expert_groups=16, topk_groups=5, bias=True),
 }

@@ -224,37 +224,77 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
     const unsigned gm24 = (VAR && a.ng > 1) ? ((1u << 24) + unsigned(a.gsz) - 1u) / unsigned(a.gsz) : 0u;
     float m = -INFINITY;
     bool bad = false;
-    if (tok) {
-      for (int e = sub; e < E; e += TPT) {
-        float v = rowp[e];
-        if (!isfinite(v)) {
-          bad = true;
-          v = -INFINITY;
-          rowp[e] = v;
-        }
-        m = fmaxf(m, v);
-        // local sorted list; experts arrive in increasing index, so an equal logit ranks
-        // after the ones already held. Once placed, the rest shift down one slot.
-        if ((!VAR || ((gmask >> ((unsigned(e) * gm24) >> 24)) & 1u)) &&
-            ranks_before(v, e, top[K - 1], id[K - 1])) {
-          float cv = v;
-          int ci = e;
-          bool placed = false;
+    // may this token select expert e (group-limited routing)
+    auto selectable = [&](int e) { return !VAR || ((gmask >> ((unsigned(e) * gm24) >> 24)) & 1u); };
+    // local sorted list; experts arrive in increasing index, so an equal logit ranks after
+    // the ones already held. Once placed, the rest shift down one slot.
+    auto insert = [&](float v, int e) {
+      if (!ranks_before(v, e, top[K - 1], id[K - 1])) return;
+      float cv = v;
+      int ci = e;
+      bool placed = false;
 #pragma unroll
-          for (int j = 0; j < K; ++j) {
-            if (placed || ranks_before(cv, ci, top[j], id[j])) {
-              const float tv = top[j];
-              const int ti = id[j];
-              top[j] = cv;
-              id[j] = ci;
-              cv = tv;
-              ci = ti;
-              placed = true;
-            }
-          }
+      for (int j = 0; j < K; ++j) {
+        if (placed || ranks_before(cv, ci, top[j], id[j])) {
+          const float tv = top[j];
+          const int ti = id[j];
+          top[j] = cv;
+          id[j] = ci;
+          cv = tv;
+          ci = ti;
+          placed = true;
         }
       }
-      if (bad) atomicOr(a.status, kStatusNonfinite);
+    };
+    if constexpr (K >= 4 && K <= TPT) {
+      // pass 1: the maxima (non-finite logits flagged and set to -inf)
+      float la = -INFINITY;  // this lane's largest selectable logit
+      if (tok) {
+        for (int e = sub; e < E; e += TPT) {
+          float v = rowp[e];
+          if (!isfinite(v)) {
+            bad = true;
+            v = -INFINITY;
+            rowp[e] = v;
+          }
+          m = fmaxf(m, v);
+          if (selectable(e)) la = fmaxf(la, v);
+        }
+        if (bad) atomicOr(a.status, kStatusNonfinite);
+      }
+      // the TPT lane maxima are TPT >= K selectable logits of the token, so its K-th largest
+      // is at least the smallest of them, tau: no logit below tau is selected
+      float tau = la;
+#pragma unroll
+      for (int off = TPT >> 1; off > 0; off >>= 1) tau = fminf(tau, __shfl_xor_sync(tmask, tau, off, TPT));
+      // pass 2: the lane's selectable logits >= tau as a bit mask (bit q: expert sub + q TPT,
+      // E / TPT <= 32), inserted in increasing expert index -- a few per lane instead of all
+      unsigned cmask = 0u;
+      if (tok) {
+        int q = 0;
+        for (int e = sub; e < E; e += TPT, ++q)
+          if (selectable(e) && rowp[e] >= tau) cmask |= 1u << q;
+      }
+      while (cmask) {
+        const int q = __ffs(cmask) - 1;
+        cmask &= cmask - 1u;
+        const int e = sub + q * TPT;
+        insert(rowp[e], e);
+      }
+    } else {
+      if (tok) {
+        for (int e = sub; e < E; e += TPT) {
+          float v = rowp[e];
+          if (!isfinite(v)) {
+            bad = true;
+            v = -INFINITY;
+            rowp[e] = v;
+          }
+          m = fmaxf(m, v);
+          if (selectable(e)) insert(v, e);
+        }
+        if (bad) atomicOr(a.status, kStatusNonfinite);
+      }
     }
     // merge the TPT local lists: K rounds of a TPT-lane arg-best, the owner pops its head
     float bestv[K];
