@@ -246,9 +246,13 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
         }
       }
     };
-    if constexpr (K >= 4 && K <= TPT) {
-      // pass 1: the maxima (non-finite logits flagged and set to -inf)
-      float la = -INFINITY;  // this lane's largest selectable logit
+    if constexpr (K >= 4) {
+      // pass 1: the token's maximum (non-finite logits flagged and set to -inf) and this
+      // lane's RL = ceil(K / TPT) largest selectable logits
+      constexpr int RL = (K + TPT - 1) / TPT;
+      float lv[RL];
+#pragma unroll
+      for (int j = 0; j < RL; ++j) lv[j] = -INFINITY;
       if (tok) {
         for (int e = sub; e < E; e += TPT) {
           float v = rowp[e];
@@ -258,17 +262,23 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
             rowp[e] = v;
           }
           m = fmaxf(m, v);
-          if (selectable(e)) la = fmaxf(la, v);
+          if (selectable(e) && v > lv[RL - 1]) {
+#pragma unroll
+            for (int j = RL - 1; j > 0; --j) lv[j] = v > lv[j - 1] ? lv[j - 1] : (v > lv[j] ? v : lv[j]);
+            lv[0] = fmaxf(lv[0], v);
+          }
         }
         if (bad) atomicOr(a.status, kStatusNonfinite);
       }
-      // the TPT lane maxima are TPT >= K selectable logits of the token, so its K-th largest
-      // is at least the smallest of them, tau: no logit below tau is selected
-      float tau = la;
+      // every lane holds RL selectable logits >= its lv[RL - 1], RL * TPT >= K of them in
+      // all, so the token's K-th largest selectable logit is at least the smallest of the
+      // lanes' lv[RL - 1], tau: no logit below tau is selected
+      float tau = lv[RL - 1];
 #pragma unroll
       for (int off = TPT >> 1; off > 0; off >>= 1) tau = fminf(tau, __shfl_xor_sync(tmask, tau, off, TPT));
-      // pass 2: the lane's selectable logits >= tau as a bit mask (bit q: expert sub + q TPT,
-      // E / TPT <= 32), inserted in increasing expert index -- a few per lane instead of all
+      // pass 2: the lane's selectable logits >= tau as a bit mask (bit q: expert sub + q TPT;
+      // E / TPT <= 32 for every TPT the launch picks), inserted in increasing expert index
+      // -- a few per lane instead of all
       unsigned cmask = 0u;
       if (tok) {
         int q = 0;
