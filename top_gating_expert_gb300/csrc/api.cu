@@ -505,6 +505,7 @@ int ffn_backward_data(const moe_config_t& c, const FfnBwd& f, unsigned* status, 
   d.offsets = f.offsets; d.groups = f.groups; d.rows_dense = f.dense_rows;
   d.out = sw ? f.dh : f.dab; d.ldo = f.Hn;
   d.row_scale = f.w; d.aux = f.h; d.ld_aux = f.Hn; d.gpart = f.gpart; d.relu = sw ? 0 : 1;
+  d.out_keep = !sw;  // ReLU: GEMM 1's data gradient reads da next
   d.status = status;
   int rc = launch_gemm_bf16(d, st);
   if (rc != MOE_OK) return rc;

@@ -184,8 +184,14 @@ __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, 
           }
           pk[j] = pack_bf16x2(o0, o1);
         }
-        store_bf16x16(out + c0, *reinterpret_cast<const uint32_t(*)[8]>(pk));
-        store_bf16x16(out + c0 + 16, *reinterpret_cast<const uint32_t(*)[8]>(pk + 8));
+        if (p.out_keep) {
+          const uint64_t pol = policy_evict_last();
+          store_bf16x16_hint(out + c0, *reinterpret_cast<const uint32_t(*)[8]>(pk), pol);
+          store_bf16x16_hint(out + c0 + 16, *reinterpret_cast<const uint32_t(*)[8]>(pk + 8), pol);
+        } else {
+          store_bf16x16(out + c0, *reinterpret_cast<const uint32_t(*)[8]>(pk));
+          store_bf16x16(out + c0 + 16, *reinterpret_cast<const uint32_t(*)[8]>(pk + 8));
+        }
       }
     }
     if (valid && p.gpart) p.gpart[grow * p.n_tiles + nt] = gsum;
