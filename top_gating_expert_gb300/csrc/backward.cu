@@ -172,8 +172,9 @@ __global__ void __launch_bounds__(256)
 //   aux term    aux_coef * E / (G * S_g) * p_e (f_e - sum_e' f_e' p_e'), f = counts_routed of
 //               the token's group / (S_g k);
 //   z term      z_coef * 2 / S * lse * p_e.
-// dg_j (the gate's gradient) = sum over the GEMM's N tiles of gpart[row] for a kept
-// assignment, 0 for a dropped one (it adds nothing to y).
+// dg_j (the gate's gradient) = sum of the n_tiles partials of gpart[row] (the GEMM's N
+// tiles, two column halves each, in order) for a kept assignment, 0 for a dropped one (it
+// adds nothing to y).
 template <int KMAX>
 __global__ void __launch_bounds__(256)
     router_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ expert_id,

@@ -53,7 +53,6 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // bf16 elements per 128-byte swizzled row
-constexpr int kThreads = 192;
 constexpr int kMaxGroups = 256;
 
 template <int BN, bool PAIR, bool KRAG = false>
@@ -75,6 +74,15 @@ struct Cfg {
                               3 * (kMaxGroups + 1) * 4;
 };
 
+// Epilogue warps: four, one per 32 TMEM lanes. The data-gradient epilogues, whose
+// per-element work (the stored h or dh read back, the mask or the SwiGLU derivative, the
+// gate partials) can outlast a tile's MMAs, have eight: two per 32 lanes, each taking half
+// of the tile's columns.
+template <int EPI, bool KRAG>
+constexpr int epi_warps() {
+  return (!KRAG && (EPI == EPI_DGRAD2 || EPI == EPI_SWIGLU_BWD)) ? 8 : 4;
+}
+
 struct KParams {
   const int32_t* offsets;
   int b_tiled;  // B packed tile-major: box (g, nt, kb) is block (g * n_tiles + nt) * kblocks + kb
@@ -90,7 +98,8 @@ struct KParams {
   unsigned* status;
   const void* aux;  // EPI_DGRAD2: h; EPI_SWIGLU_BWD: dh (bf16)
   int64_t ld_aux;
-  float* gpart;     // EPI_DGRAD2: [rows][n_tiles] sums of D * h, nullable
+  float* gpart;     // EPI_DGRAD2: [rows][n_tiles][2] sums of D * h over each half of a
+                    // tile's columns, nullable
   int relu;
   const int32_t* koffs;  // K-ragged mode: per-group K range
   int c1;                // K-ragged mode: output rows per group
@@ -109,10 +118,11 @@ using namespace sm100;
 
 // ------------------------------------------------------------------ the epilogue
 // One warp drains 32 accumulator rows (TMEM lanes) x BN columns at `tbase`; the thread
-// holding tile row `grow` stores it if `valid`. nt: the tile's N index.
+// holding tile row `grow` stores it if `valid`. nt: the tile's N index. With eight
+// epilogue warps (the data-gradient epilogues) the warp takes half `part` of the columns.
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, bool valid,
-                                              int64_t grow, int nt, bool zero = false) {
+                                              int64_t grow, int nt, bool zero = false, int part = 0) {
   if constexpr (EPI == EPI_F32_BIAS) {
     float* out = static_cast<float*>(p.out) + grow * p.ldo;
     if (p.out2) {  // row j of group g in the interleaved SwiGLU order (128 gate, 128 up rows)
@@ -147,6 +157,9 @@ __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, 
   } else if constexpr (EPI == EPI_DGRAD2) {
     // D = dy_perm . W_out (unscaled); out = w_r * D (ReLU: where h > 0), gate partial
     // sum_c D * h over this tile's columns (h as the forward stored it, bf16)
+    // columns cb .. ce - 1 of the tile: half `part`
+    constexpr int kHalf = BN / 2;
+    const int cb = part * kHalf, ce = cb + kHalf;
     const float scale = (valid && p.row_scale) ? p.row_scale[grow] : 1.f;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + nt * BN;
     const __nv_bfloat16* hrow = static_cast<const __nv_bfloat16*>(p.aux) + grow * p.ld_aux + nt * BN;
@@ -155,13 +168,13 @@ __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, 
     uint4 hn[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      hn[q] = valid ? __ldg(reinterpret_cast<const uint4*>(hrow) + q) : make_uint4(0u, 0u, 0u, 0u);
+      hn[q] = valid ? __ldg(reinterpret_cast<const uint4*>(hrow + cb) + q) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
+    for (int c0 = cb; c0 < ce; c0 += 32) {
       uint4 hc[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) hc[q] = hn[q];
-      if (valid && c0 + 32 < BN) {
+      if (valid && c0 + 32 < ce) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) hn[q] = __ldg(reinterpret_cast<const uint4*>(hrow + c0 + 32) + q);
       }
@@ -194,21 +207,24 @@ __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, 
         }
       }
     }
-    if (valid && p.gpart) p.gpart[grow * p.n_tiles + nt] = gsum;
+    if (valid && p.gpart) p.gpart[(grow * p.n_tiles + nt) * 2 + part] = gsum;
   } else if constexpr (EPI == EPI_SWIGLU_BWD) {
     // D = (a | b): the tile's 128 gate and 128 up pre-activations of hidden units
     // 128 nt ..; with dh: da = dh * b * silu'(a), db = dh * silu(a), written to the same
     // interleaved column positions (out [rows, 2H])
+    // hidden units cb .. ce - 1 of the tile's BN / 2: half `part`
+    constexpr int kQuarter = BN / 4;
+    const int cb = part * kQuarter, ce = cb + kQuarter;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + nt * BN;
     const __nv_bfloat16* dhrow = static_cast<const __nv_bfloat16*>(p.aux) + grow * p.ld_aux + nt * (BN / 2);
     uint4 dn[2];  // the next step's dh, loaded before this step's math
 #pragma unroll
     for (int q = 0; q < 2; ++q)
-      dn[q] = valid ? __ldg(reinterpret_cast<const uint4*>(dhrow) + q) : make_uint4(0u, 0u, 0u, 0u);
+      dn[q] = valid ? __ldg(reinterpret_cast<const uint4*>(dhrow + cb) + q) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN / 2; c0 += 16) {
+    for (int c0 = cb; c0 < ce; c0 += 16) {
       const uint4 d0 = dn[0], d1 = dn[1];
-      if (valid && c0 + 16 < BN / 2) {
+      if (valid && c0 + 16 < ce) {
         dn[0] = __ldg(reinterpret_cast<const uint4*>(dhrow + c0 + 16));
         dn[1] = __ldg(reinterpret_cast<const uint4*>(dhrow + c0 + 16) + 1);
       }
@@ -378,7 +394,7 @@ __device__ __forceinline__ uint64_t mn_sw128_desc(uint32_t saddr) {
 
 // ------------------------------------------------------------------ the kernel
 template <int BN, int EPI, bool PAIR, bool KRAG, bool MN = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO,   // K-ragged: fp32 output
@@ -418,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 4 * C::CTAS);
+      mbar_init(tempty0 + 8 * a, epi_warps<EPI, KRAG>() * C::CTAS);
     }
     mbar_init(drain_bar, 1);
     *s_abort = 0;
@@ -643,8 +659,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
   } else {
-    // ---------------- epilogue warps 2..5
+    // ---------------- epilogue warps 2 .. 1 + epi_warps
     const int q = warp & 3;  // TMEM lanes 32q..32q+31 = this CTA's tile rows
+    const int part = (warp - 2) >> 2;  // eight epilogue warps: the half of the columns
     const uint32_t tempty_leader = PAIR ? cluster_addr(tempty0, 0) : tempty0;
     int stg_buf = 0;  // K-ragged: the staging buffer the next 32 columns go to
     int i = 0;
@@ -674,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         epilogue_f32_tma<BN>(p, &tmO, &tmO2, tbase, int64_t(m0) + r0, nvr, nt, zero,
                              sStg + q * 2 * 4096, lane, stg_buf);
       } else {
-        epilogue_rows<BN, EPI>(p, tbase, r < rows, int64_t(m0) + r, nt, zero);
+        epilogue_rows<BN, EPI>(p, tbase, r < rows, int64_t(m0) + r, nt, zero, part);
       }
       // the accumulator is free: every lane has waited for its tensor-memory loads
       // (tcgen05.wait::ld); a relaxed arrive, as nothing of the stores needs ordering here
@@ -829,7 +846,7 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
                        : (int64_t(d.rows_dense) + C::TILE_M - 1) / C::TILE_M;
   const int64_t tiles = m_tiles * p.n_tiles;
   cudaLaunchConfig_t lc = {};
-  lc.blockDim = dim3(kThreads);
+  lc.blockDim = dim3(64 + 32 * epi_warps<EPI, KRAG>());
   lc.dynamicSmemBytes = C::SMEM;
   lc.stream = st;
   cudaLaunchAttribute attr[2];

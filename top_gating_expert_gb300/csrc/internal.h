@@ -77,7 +77,7 @@ inline WsLayout ws_layout(const moe_config_t& c, int C) {
 // x gathered into them, zero rows between segments).
 struct WsLayoutBwd {
   int64_t Rp = 0, Sp = 0;
-  int n_tiles2 = 0;  // N tiles of the backward GEMM 2 (gate-partial stride)
+  int n_tiles2 = 0;  // gate partials a row of the backward GEMM 2: two per N tile
   size_t status = 0, dy_perm = 0, dh = 0, dab = 0, gpart = 0, dx_perm = 0, poff = 0, poff_s = 0,
          wdyP = 0, xP = 0, dlogits = 0, dx_r = 0, dlb = 0, wgT = 0, koff_e = 0, koff_split = 0,
          dwg_part = 0, dhs = 0, dabs = 0, dxs = 0;
@@ -120,7 +120,7 @@ inline WsLayoutBwd ws_layout_bwd(const moe_config_t& c, int C) {
   B.Rp = (R + 64 * int64_t(c.E) + 63) / 64 * 64;
   B.Sp = (int64_t(c.S) + 63) / 64 * 64;
   const int bn2 = gemm_bn(c.H, EPI_DGRAD2);
-  B.n_tiles2 = bn2 > 0 ? c.H / bn2 : 1;
+  B.n_tiles2 = bn2 > 0 ? 2 * (c.H / bn2) : 1;  // two column halves a tile
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t at = o; o = align256(o + bytes); return at; };
   B.status = take(256);
@@ -203,8 +203,9 @@ struct GemmDesc {
   const float* bias = nullptr;           // EPI_F32_BIAS: per-column bias (nullable)
   int n_valid = 0;                       // EPI_F32_BIAS: columns stored
   unsigned* status = nullptr;
-  // EPI_DGRAD2: aux = h [rows, N] bf16 (ld_aux elements a row), gpart = per-(row, N tile)
-  // sums of D * h (nullable), relu = mask by h > 0. EPI_SWIGLU_BWD: aux = dh [rows, N/2].
+  // EPI_DGRAD2: aux = h [rows, N] bf16 (ld_aux elements a row), gpart = per-(row, N tile,
+  // column half) sums of D * h, [rows][N / BN][2] (nullable), relu = mask by h > 0.
+  // EPI_SWIGLU_BWD: aux = dh [rows, N/2].
   const void* aux = nullptr; int64_t ld_aux = 0;
   float* gpart = nullptr;
   int relu = 0;
