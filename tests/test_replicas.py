@@ -72,3 +72,10 @@ def test_reference_arm_prints_from_rank_zero_only():
     assert bench.run_reference(args, rank=1, world=2) is None
     line = bench.run_reference(args, rank=0, world=2)
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    # the line's contract: the oracle on the host, same metric and unit as the GPU arm
+    assert line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["higher_is_better"] is True and line["dtype"] == "f64"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
