@@ -653,10 +653,19 @@ def cpu_baseline(cfg, n, inp, target_flops=1.2e12):
     t = time.perf_counter()
     _oracle_step(cfg, sc, inp.np)
     dt = time.perf_counter() - t
+    # the routing stage alone on the same sample (router projection, softmax, top-k, slots,
+    # rows, losses); the rest of the step is the experts' FFNs and the combine
+    from oracle import moe_oracle as O
+    a, S = inp.np, sc["S"]
+    t = time.perf_counter()
+    O.route(O.router_logits(a["x"][:S], a["W_g"], a.get("bias")), sc, a["u"][:S])
+    dt_route = time.perf_counter() - t
     return {"value": round(sc["S"] / dt, 2), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
             "kind": "oracle",
             "sample": f"{sc['S']} tokens ({sc['G']} group(s)) of preset {n}, one oracle layer "
-                      f"forward (numpy fp64), {dt:.2f} s"}
+                      f"forward (numpy fp64), {dt:.2f} s",
+            "stages_s": {"layer": round(dt, 3), "router_and_routing": round(dt_route, 3),
+                         "experts_and_combine": round(max(dt - dt_route, 0.0), 3)}}
 
 
 def run_reference(args, rank, world):
