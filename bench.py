@@ -562,6 +562,14 @@ VARIANTS = {
 }
 
 
+def variant_router_weights(E: int, M: int):
+    """The seeded router of a variant whose expert count differs from the preset's (fp32,
+    N(0, 1/M)); callers cast it to the layer's dtype."""
+    import torch
+    g = torch.Generator().manual_seed(31)
+    return torch.randn((E, M), generator=g) / M ** 0.5
+
+
 def time_variants(args, cfg, c, x, layer, bias, u, flush, barrier, world, dev, default_ms):
     """moe_router_route under each routing variant on the preset's tokens (x and, where E is
     unchanged, W_g), L2 flushed before each call, CUDA events around it; bytes as for the
@@ -582,8 +590,7 @@ def time_variants(args, cfg, c, x, layer, bias, u, flush, barrier, world, dev, d
             res[name] = {"skipped": "configuration not valid for this preset"}
             continue
         if vc["E"] != cfg["E"]:
-            g = torch.Generator().manual_seed(31)
-            W_g = (torch.randn((vc["E"], vc["M"]), generator=g) / vc["M"] ** 0.5).to(x.dtype).to(dev)
+            W_g = variant_router_weights(vc["E"], vc["M"]).to(x.dtype).to(dev)
             b = None
         else:
             W_g, b = layer.W_g, bias
