@@ -160,8 +160,8 @@ typedef struct {
 /* Human-readable name of a status code (static storage). */
 const char* moe_status_string(int status);
 
-/* ABI version of this library (major * 100 + minor): 101 (moe_config_t with the routing
- * variant fields). */
+/* ABI version of this library (major * 100 + minor): 102 (moe_config_t with the routing
+ * variant fields; moe_set_wait_limit). */
 int moe_abi_version(void);
 
 /* MOE_OK if the configuration is valid and built, else the reason. Host only. */
@@ -179,7 +179,8 @@ int moe_rows_max(const moe_config_t* cfg, int64_t* R_max);
  * moe_layer_backward needs. MOE_WS_LAYER: what
  * moe_layer_forward needs (the step workspace plus logits, x_perm, h, y_perm and the
  * shared-expert buffers). Workspaces must be 256-byte aligned and zero-filled once
- * before first use (the status word lives in their first bytes).
+ * before first use: their first 256 bytes are a header holding the status word (bytes
+ * 0..3), a ticket (4..7) and the wait limit (8..15, see moe_set_wait_limit).
  */
 int moe_workspace_bytes(const moe_config_t* cfg, int kind, size_t* bytes);
 
@@ -408,6 +409,21 @@ int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, c
  * MOE_ERR_DEVICE_DATA; MOE_ERR_CUDA if the synchronisation itself failed).
  */
 int moe_get_device_status(void* ws, moe_stream_t stream);
+
+/*
+ * Sets, in the header of workspace ws (DEVICE pointer, 256-byte aligned), how long a
+ * kernel launched with that workspace waits for an event of its own pipeline (a TMA load
+ * landing, an MMA finishing, an accumulator being freed) before it gives up: limit_ns
+ * nanoseconds, or the default of 2 s when limit_ns is 0 (a zero-filled header). A kernel
+ * that gives up stops issuing work, lets the loads and MMAs it already issued finish,
+ * frees its tensor memory and returns early; its outputs are then undefined and
+ * moe_get_device_status reports MOE_ERR_TIMEOUT. Waits for work already issued are not
+ * shortened. Not from the pages: a guard that keeps a stalled pipeline from holding the GPU
+ * (the 2 s default), and with a tiny limit a way to exercise that path.
+ * Stream-ordered: kernels enqueued on `stream` after this call see the new limit. Returns
+ * MOE_ERR_INVALID_ARG for a null or misaligned ws, MOE_ERR_CUDA if the copy fails.
+ */
+int moe_set_wait_limit(void* ws, uint64_t limit_ns, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -22,7 +22,7 @@ def test_exports_every_declared_symbol(native_lib):
 def test_status_strings(native_lib):
     for code, name in N.STATUS_NAMES.items():
         assert native_lib.moe_status_string(code).decode().startswith(name)
-    assert native_lib.moe_abi_version() == 101
+    assert native_lib.moe_abi_version() == 102
 
 
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5])

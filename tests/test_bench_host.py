@@ -22,17 +22,64 @@ def _args(*argv):
         sys.argv = old
 
 
-def test_defaults_are_one_gpu_preset_2():
+def test_defaults_are_one_gpu_headline_on_the_largest_preset():
     a = _args()
-    assert (a.gpus, a.config, a.impl) == (1, 2, "ours")
+    assert (a.gpus, a.config, a.impl) == (1, bench.HEADLINE, "ours")
     assert a.warmup >= 3 and a.steps >= 1
+    # the headline is the preset with the most expert-GEMM work
+    def work(c):
+        f = 3 if c["act"] == "swiglu" else 2
+        return 2 * f * c["S"] * c["k"] * c["M"] * c["H"] + \
+            2 * f * c["S"] * c["M"] * c["n_shared"] * c["H_shared"]
+    assert bench.HEADLINE == max(PRESETS, key=lambda n: work(PRESETS[n]))
+    # every other preset is measured into the line's "presets" object by default
+    assert bench.other_presets(a) == [n for n in sorted(PRESETS) if n != bench.HEADLINE]
+    assert bench.other_presets(_args("--presets", "none")) == []
+    assert bench.other_presets(_args("--config", "2", "--presets", "2,5")) == [5]
 
 
 def test_override_changes_fields_and_names_them():
-    cfg = bench.preset_for(_args("--override", "S=4096", "--override", "G=4", "--override", "E=32"))
+    a = _args("--config", "2", "--override", "S=4096", "--override", "G=4", "--override", "E=32")
+    cfg = bench.preset_for(a)
     assert (cfg["S"], cfg["G"], cfg["E"]) == (4096, 4, 32)
     assert isinstance(cfg["S"], int) and "S=4096" in cfg["name"]
     assert cfg["M"] == PRESETS[2]["M"]
+    # overrides apply to the headline preset only
+    assert bench.preset_for(a, 5) == PRESETS[5]
+
+
+def test_both_arms_print_the_same_config():
+    cfg = PRESETS[3]
+    c = bench.workload_config(cfg, 3)
+    assert c == bench.workload_config(dict(cfg), 3)
+    assert c["workload"].startswith("preset 3 ") and "l2" in c
+    assert "residual added" in bench.workload_config(PRESETS[5], 5)["workload"]
+
+
+def test_oracle_arrays_are_fp64_and_cut_to_the_sample():
+    import numpy as np
+    a = {"x": np.ones((10, 4), np.float32), "u": np.ones(10, np.float32),
+         "W_g": np.ones((3, 4), np.float32)}
+    o = bench.oracle_arrays(a, 6)
+    assert o["x"].shape == (6, 4) and o["u"].shape == (6,) and o["W_g"].shape == (3, 4)
+    assert all(v.dtype == np.float64 for v in o.values())
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_cpu_sample_is_bounded(n):
+    cfg = PRESETS[n]
+    t = bench.sample_tokens(cfg, bench.CPU_FLOPS_REFERENCE_STEP)
+    assert min(256, cfg["S"]) <= t <= cfg["S"]
+
+
+def test_roofline_picks_the_binding_bound():
+    P = {"hbm": 6000.0, "tc": 2000.0, "tc_sustained": 1800.0, "source": "test"}
+    algo = {"a": (6e9, 1e9), "b": (1e6, 1.8e12)}
+    ra = bench.roofline_of("a", 2.0, algo, P, 9)
+    assert ra["bound"] == "hbm" and ra["frac"] == pytest.approx(0.5)
+    rb = bench.roofline_of("b", 2.0, algo, P, 9)
+    assert rb["bound"] == "tensor" and rb["frac"] == pytest.approx(0.5)
+    assert rb["frac_of_burst_peak"] == pytest.approx(0.45)
 
 
 def test_override_rejects_unknown_fields():

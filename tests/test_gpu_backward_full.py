@@ -3,14 +3,25 @@ outputs the oracle can form one by one: the weight gradients of sampled experts 
 experts' rows alone) and dx of sampled tokens (their kept choices, the shared experts, the
 residual and the router's term through the token's own logits row). The oracle routes from
 the GPU's logits, so both sides hold the same routing decisions; dW_g and dbias need every
-token's gate gradient and are checked by the small layers of test_gpu_backward.
+token's gate gradient and are checked by the small layers of test_gpu_backward. Every
+expected value comes from the oracle (oracle/moe_backward.py's expert backward, its own
+fp64 ReLU mask); nothing the GPU computed enters the reference.
 
-Tolerance: R14's bf16 form, as in test_gpu_backward. The ReLU's mask is a decision that
-floating point takes: where a pre-activation lies within rounding of zero the GPU (fp32
-accumulation, the sign of its stored h) and an fp64 recomputation can disagree, and with
-millions of (row, hidden unit) pairs an expert at full size has a few such flips, each
-moving one of its K terms. So for ReLU the reference takes the mask from the GPU's own h
-(GEMM 1 of the step-wise calls, the layer's h bit for bit) and everything else in fp64."""
+Tolerance: R14's bf16 form, as in test_gpu_backward, widened only where the ReLU's mask is
+ambiguous. The mask is a decision that floating point takes: the GPU masks by the sign of
+its stored h, whose pre-activation it accumulated in fp32 over K = M products of exact bf16
+values, and the oracle by the sign of the fp64 pre-activation a. Recursive fp32 summation of
+K terms is off by at most (K - 1) u sum|terms| with u = 2^-24 (round to nearest), 2^-23 if
+the accumulator truncates; the bound used is
+
+    |a32 - a| <= 2 K 2^-24 sum_m |x_m| |w_m|,
+
+so the two masks can differ only at (row, unit) pairs whose |a| lies within it. Those pairs
+are counted and printed. Each one may move, by the size of its own term, the elements that
+it feeds: dW_in[j, :] by |dh[r, j]| |x[r, :]|, dx of its token by |dh[r, j]| |W_in[j, :]|,
+dW_out[:, j] by |do[r, :]| times its h (at most twice the bound), and dx's router term
+through the gate gradient, which takes h once more. The tolerance of exactly those elements
+is widened by the sum of those terms; every other element is compared at R14's tolerance."""
 
 import numpy as np
 import pytest
@@ -18,7 +29,7 @@ import torch
 
 from oracle import moe_backward as B
 from oracle import moe_oracle as O
-from gpu_util import RTOL, assert_close, oracle_cfg, to_np
+from gpu_util import RTOL, oracle_cfg, to_np
 from top_gating_expert_gb300 import moe
 from top_gating_expert_gb300.inputs import PRESETS, make_inputs
 
@@ -26,16 +37,32 @@ pytestmark = pytest.mark.gpu
 AUX, Z = 0.7, 0.3
 
 
-def _expert_backward(x_rows, a, e, act, do, mask):
-    """The oracle's expert backward with the ReLU mask given (None: its own, for SwiGLU)."""
-    if mask is None:
-        return B._ffn_backward(x_rows, a["W_in"][e], a["W_out"][e], act,
-                               a["W_up"][e] if act == "swiglu" else None, do)
-    xr = np.asarray(x_rows, np.float64)
-    W_in, W_out = np.asarray(a["W_in"][e], np.float64), np.asarray(a["W_out"][e], np.float64)
-    h = np.maximum(xr @ W_in.T, 0.0) * mask
-    da = (do @ W_out) * mask
-    return da @ W_in, da.T @ xr, None, do.T @ h, h @ W_out.T
+def relu_band(x_rows, W_in):
+    """(row, unit) pairs whose fp64 pre-activation lies within the fp32-accumulation bound
+    of zero, and that bound (module docstring)."""
+    xr, W = np.asarray(x_rows, np.float64), np.asarray(W_in, np.float64)
+    K = xr.shape[1]
+    a = xr @ W.T
+    bound = 2.0 * K * 2.0 ** -24 * (np.abs(xr) @ np.abs(W).T)
+    return np.abs(a) <= bound, bound
+
+
+def check_close(gpu, ref, rtol, dev, what):
+    """R14 (|g - r| <= rtol (|r| + rms(r row))) plus the widening `dev` (0 where no ambiguous
+    mask decision reaches the element). Returns how many elements the widening touched."""
+    g = np.asarray(gpu, np.float64)
+    r = np.asarray(ref, np.float64)
+    r2 = r.reshape(-1, r.shape[-1])
+    g2 = g.reshape(r2.shape)
+    d2 = np.broadcast_to(np.asarray(dev, np.float64), r.shape).reshape(r2.shape)
+    rms = np.sqrt(np.mean(r2 * r2, axis=1, keepdims=True))
+    err = np.abs(g2 - r2)
+    lim = rtol * (np.abs(r2) + rms)
+    bad = err > lim + d2
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements outside tolerance "
+                           f"(first at {np.argwhere(bad)[0].tolist()}, err "
+                           f"{err[bad][0]:.3e}, limit {lim[bad][0]:.3e} + {d2[bad][0]:.3e})")
+    return int(np.count_nonzero(d2 > 0))
 
 
 @pytest.mark.parametrize("n", [2, 4, 5])
@@ -56,19 +83,6 @@ def test_backward_full_size_sampled(n, native_lib):
     grads = layer.backward(x, dy_h.to(dev), residual=residual, aux_coef=AUX, z_coef=Z)
     assert moe.device_status(layer.ws_bwd) == 0
 
-    h_gpu = None
-    if cfg["act"] == "relu":  # GEMM 1's h through the step-wise calls: the mask's decisions
-        out = layer.route_out
-        R = moe.rows_max(cfg)
-        x_perm = torch.empty((R, cfg["M"]), dtype=torch.bfloat16, device=dev)
-        h_perm = torch.empty((R, cfg["H"]), dtype=torch.bfloat16, device=dev)
-        moe.dispatch(cfg, x, out, x_perm)
-        moe.expert_up(cfg, x_perm, out.expert_offsets, layer.W_in_packed, h_perm, layer.ws)
-        assert moe.device_status(layer.ws) == 0
-        h_gpu = to_np(h_perm) > 0
-        del x_perm, h_perm
-    rows_gpu = to_np(layer.route_out.row)
-
     a = inp.np
     ocfg = oracle_cfg(cfg)
     logits = to_np(layer.logits)
@@ -76,20 +90,33 @@ def test_backward_full_size_sampled(n, native_lib):
     dy = dy_h.float().numpy().astype(np.float64)
     act, k = cfg["act"], cfg["k"]
     ids, gate, pos = r["expert_id"], r["gate"], r["pos"]
-    swiglu = act == "swiglu"
+    relu = act == "relu"
+    rt = RTOL["bf16"]
+
+    def expert(e, t_idx, do):
+        W_up = a["W_up"][e] if not relu else None
+        return B._ffn_backward(a["x"][t_idx], a["W_in"][e], a["W_out"][e], act, W_up, do)
 
     # (i) weight gradients of two experts: the busiest and one near the median
     counts = np.bincount(ids[pos >= 0].ravel(), minlength=cfg["E"])
     order = np.argsort(counts)
+    n_band = n_pairs = 0
     for e in (int(order[-1]), int(order[len(order) // 2])):
         ti, tj = np.nonzero((ids == e) & (pos >= 0))
-        mask = None if h_gpu is None else h_gpu[rows_gpu[ti, tj]]
-        _, dWi, dWu, dWo, _ = _expert_backward(a["x"][ti], a, e, act,
-                                               gate[ti, tj][:, None] * dy[ti], mask)
-        assert_close(to_np(grads.dW_out[e]), dWo, RTOL["bf16"], f"preset {n} dW_out[{e}]")
-        assert_close(to_np(grads.dW_in[e]), dWi, RTOL["bf16"], f"preset {n} dW_in[{e}]")
-        if swiglu:
-            assert_close(to_np(grads.dW_up[e]), dWu, RTOL["bf16"], f"preset {n} dW_up[{e}]")
+        do = gate[ti, tj][:, None] * dy[ti]
+        _, dWi, dWu, dWo, _ = expert(e, ti, do)
+        dev_in = dev_out = 0.0
+        if relu:
+            band, bound = relu_band(a["x"][ti], a["W_in"][e])
+            n_band += int(band.sum())
+            n_pairs += band.size
+            dh = np.abs(do @ np.asarray(a["W_out"][e], np.float64))
+            dev_in = (band * dh).T @ np.abs(np.asarray(a["x"][ti], np.float64))
+            dev_out = np.abs(do).T @ (band * 2.0 * bound)
+        check_close(to_np(grads.dW_out[e]), dWo, rt, dev_out, f"preset {n} dW_out[{e}]")
+        check_close(to_np(grads.dW_in[e]), dWi, rt, dev_in, f"preset {n} dW_in[{e}]")
+        if not relu:
+            check_close(to_np(grads.dW_up[e]), dWu, rt, 0.0, f"preset {n} dW_up[{e}]")
 
     # (ii) dx of sampled tokens: kept choices, shared experts, residual, router term
     rng = np.random.default_rng(n)
@@ -99,22 +126,39 @@ def test_backward_full_size_sampled(n, native_lib):
         tokens = np.append(tokens, dropped[0])
     dgate = np.zeros((cfg["S"], k))
     ref = np.zeros((len(tokens), cfg["M"]))
+    dev_dx = np.zeros((len(tokens), cfg["M"]))
+    dev_dgate = np.zeros((len(tokens), k))
     for q, t in enumerate(tokens):
         for j in range(k):
             if pos[t, j] < 0:
                 continue
             e = ids[t, j]
-            mask = None if h_gpu is None else h_gpu[rows_gpu[t, j]][None]
-            dxe, _, _, _, o = _expert_backward(a["x"][t:t + 1], a, e, act,
-                                               gate[t, j] * dy[t:t + 1], mask)
+            do = gate[t, j] * dy[t:t + 1]
+            dxe, _, _, _, o = expert(e, [t], do)
             ref[q] += dxe[0]
             dgate[t, j] = float(np.dot(dy[t], o[0]))
+            if relu:
+                band, bound = relu_band(a["x"][t:t + 1], a["W_in"][e])
+                n_band += int(band.sum())
+                n_pairs += band.size
+                W_out = np.asarray(a["W_out"][e], np.float64)
+                dh = np.abs(do @ W_out)
+                dev_dx[q] += ((band * dh) @ np.abs(np.asarray(a["W_in"][e], np.float64)))[0]
+                # the expert output o, hence the gate gradient dy . o, through h
+                dev_dgate[q, j] = float(((band * 2.0 * bound) @ np.abs(W_out).T)[0] @ np.abs(dy[t]))
         for s in range(cfg.get("n_shared", 0)):
             dxs, _, _, _, _ = B._ffn_backward(a["x"][t:t + 1], a["Ws_in"][s], a["Ws_out"][s], act,
-                                              a["Ws_up"][s] if swiglu else None, dy[t:t + 1])
+                                              a["Ws_up"][s] if not relu else None, dy[t:t + 1])
             ref[q] += dxs[0]
         if residual:
             ref[q] += dy[t]
     dl = B.router_logit_grad(np.asarray(logits, np.float64), r, dgate, ocfg, AUX, Z)
-    ref += dl[tokens] @ np.asarray(a["W_g"], np.float64)
-    assert_close(to_np(grads.dx)[tokens], ref, RTOL["bf16"], f"preset {n} dx (sampled tokens)")
+    W_g = np.asarray(a["W_g"], np.float64)
+    ref += dl[tokens] @ W_g
+    # a gate gradient off by d moves the token's logit gradients by at most 2 d in all
+    # (gates <= 1), hence dx by 2 d max_e |W_g[e, m]|
+    dev_dx += 2.0 * dev_dgate.sum(axis=1, keepdims=True) * np.abs(W_g).max(axis=0)[None, :]
+    check_close(to_np(grads.dx)[tokens], ref, rt, dev_dx, f"preset {n} dx (sampled tokens)")
+    if relu:
+        print(f"preset {n}: {n_band} of {n_pairs} (row, unit) pairs of the checked rows lie "
+              f"within the fp32-accumulation bound of zero (their ReLU mask may differ)")

@@ -87,6 +87,7 @@ _PROTOTYPES = {
                            c_size_t, ctypes.c_int, c_float, c_float, _P(MoeGrads), c_void_p,
                            c_size_t, c_void_p],
     "moe_get_device_status": [c_void_p, c_void_p],
+    "moe_set_wait_limit": [c_void_p, ctypes.c_uint64, c_void_p],
 }
 _RESTYPES = {"moe_status_string": ctypes.c_char_p}
 

@@ -175,7 +175,7 @@ const char* moe_status_string(int status) {
   return "unknown status";
 }
 
-int moe_abi_version(void) { return 101; }
+int moe_abi_version(void) { return 102; }
 
 int moe_validate_config(const moe_config_t* cfg) {
   Prep p;
@@ -651,6 +651,17 @@ int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, c
   // dx = sum over kept choices of the rows' gradients (+ shared) (+ dy) + the router's
   return launch_combine(c, w + B.dx_perm, r->row, dxs, residual ? dy : nullptr, grads->dx, R,
                         stream, reinterpret_cast<const float*>(w + B.dx_r));
+}
+
+int moe_set_wait_limit(void* ws, uint64_t limit_ns, moe_stream_t stream) {
+  if (!ws || reinterpret_cast<uintptr_t>(ws) % 256 != 0) return MOE_ERR_INVALID_ARG;
+  // bytes 8..15 of the header (the bounded waits read them where they would give up);
+  // pageable source: the copy has taken the value by the time the call returns
+  const uint64_t v = limit_ns;
+  if (cudaMemcpyAsync(static_cast<char*>(ws) + kWaitLimitOffset, &v, sizeof(v),
+                      cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 int moe_get_device_status(void* ws, moe_stream_t stream) {

@@ -36,9 +36,10 @@
 // Tiles are ordered group by group, then by N tile, then by M tile, so the CTAs that run
 // at the same time share each weight tile through L2.
 //
-// Every wait is bounded: after kWaitLimitNs a waiting thread sets the status word's
-// timeout bit and a CTA-wide abort flag; every role then stops, the producer waits for its
-// loads in flight, the MMA thread for its MMAs, and TMEM is freed before the CTA exits.
+// Every wait is bounded: after the wait limit (2 s unless set in the workspace header) a
+// waiting thread sets the status word's timeout bit and a CTA-wide abort flag; every role
+// then stops and, after a CTA barrier, the producer waits for its loads in flight and the
+// MMA thread for its MMAs, whichever role gave up; TMEM is freed before the CTA exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -466,6 +467,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
   }
   pdl_wait();  // everything above is local setup; below, the first reads of the inputs
   pdl_trigger();
+  const uint64_t wlimit = wait_limit_ns(p.status);
   if (warp == 2) {
     // m-tile prefix over the groups, from the device row offsets
     bool bad = false;
@@ -532,10 +534,15 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
     rows = min(C::TILE_M, s_off[g + 1] - m0);
   };
 
+  // what each role has in flight, for the drain after an abort: the stages whose last load
+  // the producer issued (and that load's phase), whether the MMA thread issued MMAs and
+  // has already waited for them
+  uint32_t issued = 0, issued_par = 0;
+  bool mma_any = false, mma_drained = false;
   if (warp == 0) {
     // ---------------- TMA producer: the whole warp walks the schedule, lane 0 issues
     int stage = 0;
-    uint32_t phase = 0, issued = 0, issued_par = 0;
+    uint32_t phase = 0;
     bool ok = true;
     for (int t = unit; t < total && ok; t += units) {
       int g, m0, rows, nt;
@@ -548,7 +555,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
       const int abase = MN ? (p.aoffs ? __ldg(p.aoffs + g) : s_koff[g]) : 0;  // K rows of A
       const int bbase = MN ? (p.boffs ? __ldg(p.boffs + g) : s_koff[g]) : 0;  // K rows of B
       for (int kb = 0; kb < nkb; ++kb) {
-        ok = __all_sync(0xffffffffu, wait_bounded(empty0 + 8 * stage, phase ^ 1u, s_abort, p.status));
+        ok = __all_sync(0xffffffffu, wait_bounded(empty0 + 8 * stage, phase ^ 1u, s_abort, p.status, wlimit));
         if (!ok) break;
         if (lane == 0) {
           const uint32_t fb = full0 + 8 * stage;
@@ -590,12 +597,6 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
         }
       }
     }
-    // on abort, let every load in flight land before the CTA exits (the even CTA's full
-    // barriers also count the odd CTA's bytes)
-    if (!ok && leader && lane == 0) {
-      for (int s = 0; s < C::STAGES; ++s)
-        if ((issued >> s) & 1u) wait_drain(full0 + 8 * s, (issued_par >> s) & 1u);
-    }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer (the even CTA of a pair): the warp waits, lane 0 issues
@@ -604,12 +605,12 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
       constexpr uint32_t kIdesc = idesc_bf16(C::TILE_M, BN) | (MN ? (3u << 15) : 0u);
       int stage = 0;
       uint32_t phase = 0;
-      bool ok = true, any = false;
+      bool ok = true;
       int i = 0;
       for (int t = unit; t < total && ok; t += units, ++i) {
         const int acc = i & 1;
         const uint32_t use = uint32_t(i >> 1) & 1u;
-        ok = __all_sync(0xffffffffu, wait_bounded(tempty0 + 8 * acc, use ^ 1u, s_abort, p.status));
+        ok = __all_sync(0xffffffffu, wait_bounded(tempty0 + 8 * acc, use ^ 1u, s_abort, p.status, wlimit));
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem_base + uint32_t(acc * BN);
@@ -620,7 +621,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
           nkb = (s_koff[g + 1] - s_koff[g]) / BK;
         }
         for (int kb = 0; kb < nkb; ++kb) {
-          ok = __all_sync(0xffffffffu, wait_bounded(full0 + 8 * stage, phase, s_abort, p.status));
+          ok = __all_sync(0xffffffffu, wait_bounded(full0 + 8 * stage, phase, s_abort, p.status, wlimit));
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
@@ -639,7 +640,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
             else mma_commit(empty0 + 8 * stage);
           }
           __syncwarp();
-          any = true;
+          mma_any = true;
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -651,11 +652,12 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
         }
         __syncwarp();
       }
-      if (!ok && any && lane == 0) {  // every MMA issued must finish before TMEM is freed
+      if (!ok && mma_any && lane == 0) {  // every MMA issued must finish before TMEM is freed
         if constexpr (PAIR) mma_commit_pair(drain_bar, uint16_t(1));
         else mma_commit(drain_bar);
         wait_drain(drain_bar, 0u);
       }
+      mma_drained = !ok && mma_any;
       __syncwarp();
     }
   } else {
@@ -679,7 +681,7 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
                                int64_t(nt) * kAuxCols,
                            uint32_t(kAuxCols * 2));
       }
-      const bool ok = __all_sync(0xffffffffu, wait_bounded(tfull0 + 8 * acc, use, s_abort, p.status));
+      const bool ok = __all_sync(0xffffffffu, wait_bounded(tfull0 + 8 * acc, use, s_abort, p.status, wlimit));
       if (!ok) break;
       tc_fence_after();
       const int r = int(rank) * BM + q * 32 + lane;  // row within the tile
@@ -709,6 +711,23 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
 
   tc_fence_before();
   __syncthreads();
+  if (*s_abort) {
+    // A role may have finished its own loop before another gave up, with loads or MMAs still
+    // in flight: every load issued lands (the even CTA's full barriers also count the odd
+    // CTA's bytes) and every MMA issued finishes before shared and tensor memory go away.
+    // The flag is read after the barrier, so every thread of the CTA takes this branch.
+    if (warp == 0 && leader && lane == 0) {
+      for (int s = 0; s < C::STAGES; ++s)
+        if ((issued >> s) & 1u) wait_drain(full0 + 8 * s, (issued_par >> s) & 1u);
+    }
+    if (warp == 1 && leader && lane == 0 && mma_any && !mma_drained) {
+      if constexpr (PAIR) mma_commit_pair(drain_bar, uint16_t(1));
+      else mma_commit(drain_bar);
+      wait_drain(drain_bar, 0u);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if constexpr (PAIR) cluster_sync_all();  // both CTAs done with TMEM and each other's smem
   if (warp == 1) {
     tc_fence_after();

@@ -16,6 +16,10 @@ constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned kStatusNonfinite = 2u;
 constexpr unsigned kStatusDeviceData = 4u;
 
+// Byte offset, in every workspace header, of the wait limit in ns (uint64; 0 = 2 s) that
+// the kernels' bounded waits apply (moe_set_wait_limit).
+constexpr size_t kWaitLimitOffset = 8;
+
 // Tokens per routing chunk (one CTA of the routing kernels, one thread per token).
 constexpr int kRouteChunk = 128;
 

@@ -561,15 +561,19 @@ __global__ void __launch_bounds__(kThreads * TPT, 1)
   const uint32_t tmem = s_tmem;
   pdl_wait();
   pdl_trigger();
+  const uint64_t wlimit = wait_limit_ns(a.status);
   const float u_tok = token_u<K, TPT>(a, t0, nt);
 
+  // what each role has in flight, for the drain after an abort (see the end of the roles)
+  uint32_t issued = 0, issued_par = 0;
+  bool mma_any = false, mma_waited = false;
   if (warp == 0) {
     // ---------------- TMA producer
     int stage = 0;
-    uint32_t phase = 0, issued = 0, issued_par = 0;
+    uint32_t phase = 0;
     bool ok = true;
     for (int j = 0; j < kblocks; ++j) {
-      ok = __all_sync(0xffffffffu, wait_bounded(empty0 + 8 * stage, phase ^ 1u, &s_abort, a.status));
+      ok = __all_sync(0xffffffffu, wait_bounded(empty0 + 8 * stage, phase ^ 1u, &s_abort, a.status, wlimit));
       if (!ok) break;
       if (lane == 0) {
         const int kb = j;
@@ -586,18 +590,15 @@ __global__ void __launch_bounds__(kThreads * TPT, 1)
         phase ^= 1u;
       }
     }
-    if (!ok && lane == 0)
-      for (int s = 0; s < NS; ++s)
-        if ((issued >> s) & 1u) wait_drain(full0 + 8 * s, (issued_par >> s) & 1u);
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer: one 128 x BN tile
     const uint32_t idesc = idesc_bf16(128, BN);
     int stage = 0;
     uint32_t phase = 0;
-    bool ok = true, any = false;
+    bool ok = true;
     for (int j = 0; j < kblocks; ++j) {
-      ok = __all_sync(0xffffffffu, wait_bounded(full0 + 8 * stage, phase, &s_abort, a.status));
+      ok = __all_sync(0xffffffffu, wait_bounded(full0 + 8 * stage, phase, &s_abort, a.status, wlimit));
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
@@ -609,7 +610,7 @@ __global__ void __launch_bounds__(kThreads * TPT, 1)
         mma_commit(empty0 + 8 * stage);
       }
       __syncwarp();
-      any = true;
+      mma_any = true;
       if (++stage == NS) {
         stage = 0;
         phase ^= 1u;
@@ -617,14 +618,15 @@ __global__ void __launch_bounds__(kThreads * TPT, 1)
     }
     // done_bar completes once every MMA issued has finished (also after an abort, so that
     // shared and tensor memory are reused or freed only once nothing writes them)
-    if (lane == 0 && any) mma_commit(done_bar);
-    if (!ok && any && lane == 0) wait_drain(done_bar, 0u);
+    if (lane == 0 && mma_any) mma_commit(done_bar);
+    if (!ok && mma_any && lane == 0) wait_drain(done_bar, 0u);
+    mma_waited = !ok && mma_any;
     __syncwarp();
   } else if (warp >= 4 && warp < 8) {
     // ---------------- drain: token i = 32 q + lane owns TMEM lane i
     const int q = warp & 3, i = q * 32 + lane;
     const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
-    const bool ok = __all_sync(0xffffffffu, wait_bounded(done_bar, 0u, &s_abort, a.status));
+    const bool ok = __all_sync(0xffffffffu, wait_bounded(done_bar, 0u, &s_abort, a.status, wlimit));
     if (ok) {
       tc_fence_after();
       const bool store = f.logits_out != nullptr && i < nt;
@@ -665,6 +667,17 @@ __global__ void __launch_bounds__(kThreads * TPT, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (s_abort) {
+    // A role may have finished its own loop before another gave up, with loads or MMAs still
+    // in flight: every load issued lands and every MMA issued finishes before the ring is
+    // reused and tensor memory freed (the flag is read after the barrier: CTA-uniform).
+    if (warp == 0 && lane == 0)
+      for (int s = 0; s < NS; ++s)
+        if ((issued >> s) & 1u) wait_drain(full0 + 8 * s, (issued_par >> s) & 1u);
+    if (warp == 1 && lane == 0 && mma_any && !mma_waited) wait_drain(done_bar, 0u);
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, tcols);

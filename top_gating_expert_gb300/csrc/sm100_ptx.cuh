@@ -1,6 +1,6 @@
 // Inline-PTX wrappers for sm_100-family (sm_103a) kernels: mbarriers, TMA (cp.async.bulk.tensor),
 // tcgen05 tensor-memory allocation, MMA, commit and loads, cluster addressing. Shared by the
-// GEMM and routing translation units; every wait is bounded by kWaitLimitNs.
+// GEMM and routing translation units; every wait is bounded (wait_limit_ns, kWaitLimitNs).
 #pragma once
 
 #include <cuda.h>
@@ -13,6 +13,18 @@ namespace moe {
 namespace sm100 {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a bounded wait gives up after 2 s
+// Longest a waiting thread stays suspended in one mbarrier.try_wait before it looks at the
+// clock and the abort flag again (it resumes earlier when the phase completes).
+constexpr uint32_t kSuspendHintNs = 1000;
+
+// The limit the bounded waits of a kernel apply, read once per kernel (after its wait on
+// the previous kernel): bytes 8..15 of the workspace header that holds the status word (set
+// by moe_set_wait_limit), or kWaitLimitNs while that field is 0. Only waits for work that
+// may never come use it; draining work already issued does not.
+__device__ __forceinline__ uint64_t wait_limit_ns(const unsigned* status) {
+  const uint64_t v = *reinterpret_cast<const volatile uint64_t*>(status + 2);
+  return v ? v : kWaitLimitNs;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -27,14 +39,28 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Non-blocking test of the phase of parity `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Potentially blocking test: the thread may stay suspended until the phase completes or
+// about kSuspendHintNs have passed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -44,31 +70,34 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
-// The bounded part of wait_bounded, out of line (the common case returns before it).
+// The bounded part of wait_bounded, out of line (the common case returns before it): the
+// clock and the abort flag are checked after every suspension of at most kSuspendHintNs.
 static __device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity,
-                                                      volatile int* abort_flag, unsigned* status) {
+                                                      volatile int* abort_flag, unsigned* status,
+                                                      uint64_t limit) {
   const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0u) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        atomicOr(status, kStatusTimeout);
-        return false;
-      }
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > limit) {
+      *abort_flag = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
     }
   }
 }
 
-// Wait for the phase of parity `parity` to complete; false on abort or timeout.
+// Wait for the phase of parity `parity` to complete; false on abort or after `limit` ns
+// (wait_limit_ns).
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                             unsigned* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return wait_bounded_slow(bar, parity, abort_flag, status);
+                                             unsigned* status, uint64_t limit) {
+  if (mbar_test_wait(bar, parity)) return true;
+  return wait_bounded_slow(bar, parity, abort_flag, status, limit);
 }
 
-// Wait that ignores the abort flag (used only to drain work already issued).
+// Wait that ignores the abort flag and the settable limit (used only to drain work already
+// issued, which lands in bounded time: the CTA must not release shared or tensor memory
+// before it does).
 static __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity))

@@ -295,6 +295,13 @@ def device_status(ws, stream=None) -> int:
     return N.lib().moe_get_device_status(_ptr(ws), _stream(stream))
 
 
+def set_wait_limit(ws, limit_ns: int, stream=None):
+    """How long the kernels using workspace ws wait on their own pipeline before giving up
+    (0 = the default of 2 s)."""
+    _check(N.lib().moe_set_wait_limit(_ptr(ws), int(limit_ns), _stream(stream)),
+           "moe_set_wait_limit")
+
+
 # ------------------------------------------------------------------ a layer object
 class MoeLayer:
     """Weights resident on one GPU (packed once), a workspace and routing outputs.
@@ -412,7 +419,8 @@ class HostPipeline:
     (``route[i % depth]`` holds step i's), so the output copy reads the two losses from
     them directly."""
 
-    def __init__(self, layer: MoeLayer, has_u: bool, depth: int = 2):
+    def __init__(self, layer: MoeLayer, has_u: bool, depth: int = 2, residual: bool = False):
+        """residual: the layer adds its input x to the expert output (y = x + MoE(x))."""
         dev = layer.device
         c = layer.cfg
         dt = torch_dtype(c)
@@ -435,12 +443,13 @@ class HostPipeline:
                 self.u[b].fill_(0.5)
             side = torch.cuda.Stream(device=dev)
             side.wait_stream(self.compute)
+            res = self.x[b] if residual else None
             with torch.cuda.stream(side):
-                layer.forward(self.x[b], self.u[b], out=self.y[b], route_out=self.route[b])
+                layer.forward(self.x[b], self.u[b], res, out=self.y[b], route_out=self.route[b])
             self.compute.wait_stream(side)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                layer.forward(self.x[b], self.u[b], out=self.y[b], route_out=self.route[b])
+                layer.forward(self.x[b], self.u[b], res, out=self.y[b], route_out=self.route[b])
             self.graphs.append(g)
         torch.cuda.synchronize(dev)
 
