@@ -302,12 +302,29 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(RouteArgs a, i
   }
   // losses: aux = mean over groups of E * sum_e f_e P_e (f_e = routed_e / (Sg k),
   // P_e = psum_e / Sg); z = mean over tokens of logsumexp^2. Fixed-order sums.
+  // With many expert slices a group (X > 8: few groups, as in single-group layers) a warp
+  // sums a group's slices (lanes over slices, then a fixed shuffle tree) instead of one
+  // thread walking them: those loads would otherwise form one long dependent chain.
   float ga = 0.f, gzs = 0.f;
-  for (int gg = tid; gg < G; gg += kScanThreads) {
-    float tsum = 0.f;
-    for (int xx = 0; xx < X; ++xx) tsum += __ldcg(a.gaux + size_t(gg) * X + xx);
-    ga += float(double(tsum) * double(E) / (double(a.Sg) * a.k * double(a.Sg)));
-    gzs += __ldcg(a.gz + gg);
+  const double gscale = double(E) / (double(a.Sg) * a.k * double(a.Sg));
+  if (X > 8) {
+    for (int gg = warp; gg < G; gg += kScanThreads / 32) {
+      float tsum = 0.f;
+      for (int xx = lane; xx < X; xx += 32) tsum += __ldcg(a.gaux + size_t(gg) * X + xx);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, off);
+      if (lane == 0) {
+        ga += float(double(tsum) * gscale);
+        gzs += __ldcg(a.gz + gg);
+      }
+    }
+  } else {
+    for (int gg = tid; gg < G; gg += kScanThreads) {
+      float tsum = 0.f;
+      for (int xx = 0; xx < X; ++xx) tsum += __ldcg(a.gaux + size_t(gg) * X + xx);
+      ga += float(double(tsum) * gscale);
+      gzs += __ldcg(a.gz + gg);
+    }
   }
   ga = block_sum(ga, s_red);
   gzs = block_sum(gzs, s_red);

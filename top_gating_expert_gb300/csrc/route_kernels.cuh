@@ -179,12 +179,20 @@ __device__ __forceinline__ float token_u(const RouteArgs& a, int t0, int nt) {
   return (K == 2 && a.rr && int(threadIdx.x) % TPT == 0 && i < nt) ? __ldg(a.u + t0 + i) : 0.f;
 }
 
+// The barrier of the routing body: the whole CTA (NB = 0), or named barrier 1 over the
+// first NB threads when the CTA also runs warps of other roles.
+template <int NB>
+__device__ __forceinline__ void body_sync() {
+  if constexpr (NB == 0) __syncthreads();
+  else asm volatile("bar.sync 1, %0;" ::"n"(NB) : "memory");
+}
+
 // The per-chunk routing work on a chunk's logits staged in shared memory (s_log: nt rows of
 // E logits, row stride ld = E + TPT). TPT threads per token (consecutive lanes), each owning
 // experts sub, sub + TPT, ...; the CTA has kThreads * TPT threads, all of which call this.
 // Non-finite logits count as -inf (and are flagged); each staged logit is overwritten by
-// exp(logit - max of its token).
-template <int K, int TPT, bool VAR>
+// exp(logit - max of its token). NB: see body_sync (the body threads are 0 .. NB - 1).
+template <int K, int TPT, bool VAR, int NB = 0>
 __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int c, int t0, int nt,
                                            float u_tok) {
   constexpr int kT = kThreads * TPT;
@@ -197,9 +205,16 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, ld = E + TPT;
+  // The persistent router's body (NB != 0) with k <= 3 and at most 16 experts a lane (TPT
+  // 2 or 4): the lane's logits stay in registers through the selection, the exponentials
+  // and the sum, and the row then receives the probabilities themselves. (With one chunk a
+  // CTA, where the body does not overlap the loads, that form measured slower: 63 -> 76 us
+  // for the routing of 65536 tokens over 64 experts.)
+  constexpr bool kRegs = NB != 0 && K < 4 && TPT <= 4;
+  constexpr int NPL = kRegs ? 16 : 1;
   if (c == 0 && tid == 0) *a.done = 0u;  // ticket counter of route_scan_kernel
   for (int e = tid; e < E; e += kT) s_route[e] = 0;
-  __syncthreads();
+  body_sync<NB>();
 
   // token i = tid / TPT; this thread's experts: sub, sub + TPT, ...
   const int i = tid / TPT, sub = tid % TPT;
@@ -246,6 +261,7 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
         }
       }
     };
+    float lreg[NPL];
     if constexpr (K >= 4) {
       // pass 1: the token's maximum (non-finite logits flagged and set to -inf) and this
       // lane's RL = ceil(K / TPT) largest selectable logits
@@ -291,6 +307,44 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
         const int e = sub + q * TPT;
         insert(rowp[e], e);
       }
+    } else if constexpr (kRegs) {
+      // the lane's experts arrive in increasing index, so a held logit equal to v already
+      // ranks first and a strict comparison keeps the order: the insertion is a fixed
+      // sequence of selects (a branch per element diverged across the warp's lanes)
+#pragma unroll
+      for (int q = 0; q < NPL; ++q) {
+        if (q * TPT >= E) break;  // no lane of the warp has an expert left
+        const int e = sub + q * TPT;
+        const bool own = tok && e < E;
+        float v = own ? rowp[e] : -INFINITY;
+        const bool fin = isfinite(v);
+        bad |= own && !fin;
+        v = fin ? v : -INFINITY;
+        lreg[q] = v;
+        m = fmaxf(m, v);
+        if (own && selectable(e)) {
+          // the new list, slot by slot from the old one: slot j takes the old slot j - 1
+          // when v ranks above it, else v when v ranks above the old slot j (written into
+          // temporaries: the same selects updating the list in place, from the last slot
+          // down, gave lists holding one expert twice when built for the GPU, while the
+          // host build of the same code was right)
+          float nt[K];
+          int ni[K];
+#pragma unroll
+          for (int j = 0; j < K; ++j) {
+            const bool above = v > top[j];
+            const bool above_prev = j > 0 && v > top[j > 0 ? j - 1 : 0];
+            nt[j] = above_prev ? top[j > 0 ? j - 1 : 0] : (above ? v : top[j]);
+            ni[j] = above_prev ? id[j > 0 ? j - 1 : 0] : (above ? e : id[j]);
+          }
+#pragma unroll
+          for (int j = 0; j < K; ++j) {
+            top[j] = nt[j];
+            id[j] = ni[j];
+          }
+        }
+      }
+      if (tok && bad) atomicOr(a.status, kStatusNonfinite);
     } else {
       if (tok) {
         for (int e = sub; e < E; e += TPT) {
@@ -338,16 +392,41 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
     for (int off = TPT >> 1; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(tmask, m, off, TPT));
     if (m == -INFINITY) m = 0.f;  // only when every logit was non-finite (already flagged)
     // sum of exp(l - m); each exp(l - m) replaces its logit in the row (the probability
-    // sums below reuse it; the top-k logits are held in registers)
+    // sums below reuse it; the top-k logits are held in registers). In the register form
+    // the default routing takes the fast exponential here: these terms feed only the
+    // softmax sum (the z-loss's logsumexp) and the probabilities of the aux loss, each
+    // term within a few ulp (the gates are computed apart, with expf); the variants keep
+    // expf, as their un-normalised gates are these probabilities.
     float s = 0.f;
-    if (tok)
+    if constexpr (kRegs) {
+#pragma unroll
+      for (int q = 0; q < NPL; ++q) {
+        if (q * TPT >= E) break;
+        const int e = sub + q * TPT;
+        float v = 0.f;
+        if (tok && e < E) v = VAR ? expf(lreg[q] - m) : __expf(lreg[q] - m);
+        lreg[q] = v;
+        s += v;
+      }
+    } else if (tok) {
       for (int e = sub; e < E; e += TPT) {
         const float v = expf(rowp[e] - m);
         rowp[e] = v;
         s += v;
       }
+    }
 #pragma unroll
     for (int off = TPT >> 1; off > 0; off >>= 1) s += __shfl_xor_sync(tmask, s, off, TPT);
+    if constexpr (kRegs) {
+      // the probabilities, the products the sums below would otherwise form
+      const float inv = s > 0.f ? 1.f / s : 0.f;
+#pragma unroll
+      for (int q = 0; q < NPL; ++q) {
+        if (q * TPT >= E) break;
+        const int e = sub + q * TPT;
+        if (tok && e < E) rowp[e] = lreg[q] * inv;
+      }
+    }
 
     if (tok && sub == 0) {
       const int t = t0 + i;
@@ -391,7 +470,7 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
   }
   for (int off = 16; off > 0; off >>= 1) zacc += __shfl_xor_sync(0xffffffffu, zacc, off);
   if (lane == 0) s_z[warp] = zacc;
-  __syncthreads();
+  body_sync<NB>();
 
   // per-expert softmax-probability sums over the chunk: tpe threads per expert, each a
   // strided subset of tokens, partials added in a fixed order
@@ -402,17 +481,22 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
       const int x = base + tid;
       const int e = x / tpe, sb = x % tpe;
       float acc = 0.f;
-      if (e < E)
-        for (int t = sb; t < nt; t += tpe) acc += s_log[t * ld + e] * s_inv[t];
+      if (e < E) {
+        if constexpr (kRegs) {  // the row holds the probabilities
+          for (int t = sb; t < nt; t += tpe) acc += s_log[t * ld + e];
+        } else {
+          for (int t = sb; t < nt; t += tpe) acc += s_log[t * ld + e] * s_inv[t];
+        }
+      }
       s_pp[tid] = acc;
-      __syncthreads();
+      body_sync<NB>();
       if (e < E && sb == 0) {
         float sum = 0.f;
         for (int q = 0; q < tpe; ++q) sum += s_pp[tid + q];
         a.ppart[size_t(c) * E + e] = sum;
         a.hroute[size_t(c) * E + e] = s_route[e];
       }
-      __syncthreads();
+      body_sync<NB>();
     }
   }
   if (tid == 0) {
@@ -427,7 +511,7 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
   // scan over the warps per (j, e), then each token's K ranks -- three barriers for any K.
   int* s_cnt = reinterpret_cast<int*>(s_log);  // [K][kWarps][E] (16 K E <= 512 (E + TPT) bytes)
   for (int x = tid; x < K * kWarps * E; x += kT) s_cnt[x] = 0;
-  __syncthreads();
+  body_sync<NB>();
   const bool valid = tid < nt;
   const unsigned lt_mask = (1u << lane) - 1u;
   if (tid < kThreads) {
@@ -442,7 +526,7 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
       if (cnd && rk == 0) s_cnt[(j * kWarps + warp) * E + e] = __popc(peers);
     }
   }
-  __syncthreads();
+  body_sync<NB>();
   for (int x = tid; x < K * E; x += kT) {
     const int j = x / E, e2 = x - j * E;
     int run = 0;
@@ -455,7 +539,7 @@ __device__ __forceinline__ void topk_chunk(const RouteArgs& a, float* s_log, int
     }
     a.hist[(size_t(c) * K + j) * E + e2] = run;
   }
-  __syncthreads();
+  body_sync<NB>();
   if (valid) {
 #pragma unroll
     for (int j = 0; j < K; ++j) {
@@ -687,6 +771,228 @@ __global__ void __launch_bounds__(kThreads * TPT, 1)
   topk_chunk<K, TPT, VAR>(a, s_log, c, t0, nt, u_tok);
 }
 
+// ------------------------------------------------------------------ persistent fused router
+// router_topk_kernel's work for layers with more chunks than SMs: one CTA per SM walks the
+// chunks blockIdx.x, blockIdx.x + gridDim.x, ... Warps 0 .. kBody / 32 - 1 run the routing
+// body, warp kBody / 32 streams the chunks' x rows and W_g through a TMA ring that does not
+// drain between chunks, and warp kBody / 32 + 1 issues each chunk's MMAs into one of two
+// TMEM accumulators. So the next chunk's loads and MMAs run while the body routes the
+// current one; router_topk_kernel, one chunk a CTA, runs its body only after its own loads,
+// in waves that leave DRAM idle meanwhile. The MMA sequence (64-wide k-blocks in order,
+// four K = 16 steps each) and the bias addition are router_topk_kernel's, so the logits
+// equal moe_router's bit for bit. Lec16 Systems for MoE Models, "MoE Kernel 优化": the
+// gating function as one fused kernel.
+template <int K, int TPT, bool VAR>
+__global__ void __launch_bounds__(kThreads * TPT + 64, 1)
+    router_topk_persistent_kernel(const __grid_constant__ CUtensorMap tmX,
+                                  const __grid_constant__ CUtensorMap tmW, RouteArgs a,
+                                  FusedRouterArgs f) {
+  using namespace sm100;
+  constexpr int kBody = kThreads * TPT;             // the routing body's threads
+  constexpr int kPW = kBody / 32, kMW = kPW + 1;    // producer and MMA warps
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bars[2 * 8 + 5];
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int BN = f.BN, NS = f.stages;
+  const int A_BYTES = 128 * 64 * 2, B_BYTES = BN * 64 * 2;
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + NS * A_BYTES;
+  float* s_log = reinterpret_cast<float*>(sB + NS * B_BYTES);  // its own buffer
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * 8, tfull0 = empty0 + 8 * 8;
+  const uint32_t tempty0 = tfull0 + 16, drain_bar = tempty0 + 16;
+  const int tcols = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators (BN a power of 2)
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = a.E, ld = E + TPT;
+  const int kblocks = f.Mdim / 64;
+  const int n_chunks = a.G * a.n_cpg;
+  const int nch = blockIdx.x < unsigned(n_chunks)
+                      ? (n_chunks - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x) : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(tfull0 + 8 * q, 1);
+      mbar_init(tempty0 + 8 * q, 1);
+    }
+    mbar_init(drain_bar, 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_map(&tmX);
+    tma_prefetch_map(&tmW);
+  }
+  if (warp == kMW) tmem_alloc(smem_u32(&s_tmem), tcols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  pdl_wait();
+  pdl_trigger();
+  const uint64_t wlimit = wait_limit_ns(a.status);
+
+  // chunk i of this CTA: its group, first token and token count
+  auto chunk = [&](int i, int& c, int& t0, int& nt) {
+    c = int(blockIdx.x) + i * int(gridDim.x);
+    const int g = c / a.n_cpg, cc = c % a.n_cpg;
+    t0 = g * a.Sg + cc * kThreads;
+    nt = min(kThreads, a.Sg - cc * kThreads);
+  };
+  // what each role has in flight, for the drain after an abort
+  uint32_t issued = 0, issued_par = 0;
+  bool mma_any = false, mma_drained = false;
+
+  if (warp == kPW) {
+    // ---------------- TMA producer: every k-block of every chunk, the ring never drains
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int i = 0; i < nch && ok; ++i) {
+      int c, t0, nt;
+      chunk(i, c, t0, nt);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        ok = __all_sync(0xffffffffu, wait_bounded(empty0 + 8 * stage, phase ^ 1u, &s_abort, a.status, wlimit));
+        if (!ok) break;
+        if (lane == 0) {
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_expect_tx(fb, A_BYTES + B_BYTES);
+          tma_load_2d(smem_u32(sA + stage * A_BYTES), &tmX, kb * 64, t0, fb);
+          tma_load_2d(smem_u32(sB + stage * B_BYTES), &tmW, kb * 64, 0, fb);
+        }
+        __syncwarp();
+        issued |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == NS) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == kMW) {
+    // ---------------- MMA issuer: one 128 x BN tile a chunk, accumulators alternating
+    const uint32_t idesc = idesc_bf16(128, BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int i = 0; i < nch && ok; ++i) {
+      const int acc = i & 1;
+      const uint32_t use = uint32_t(i >> 1) & 1u;
+      ok = __all_sync(0xffffffffu, wait_bounded(tempty0 + 8 * acc, use ^ 1u, &s_abort, a.status, wlimit));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d = tmem + uint32_t(acc * BN);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        ok = __all_sync(0xffffffffu, wait_bounded(full0 + 8 * stage, phase, &s_abort, a.status, wlimit));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = smem_u32(sA + stage * A_BYTES), b0 = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                     (kb | kk) != 0 ? 1u : 0u);
+          mma_commit(empty0 + 8 * stage);
+        }
+        __syncwarp();
+        mma_any = true;
+        if (++stage == NS) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok && lane == 0) mma_commit(tfull0 + 8 * acc);
+      __syncwarp();
+    }
+    if (!ok && mma_any && lane == 0) {  // every MMA issued finishes before TMEM is freed
+      mma_commit(drain_bar);
+      wait_drain(drain_bar, 0u);
+    }
+    mma_drained = !ok && mma_any;
+    __syncwarp();
+  } else {
+    // ---------------- the routing body, chunk after chunk
+    // drain: warp w reads TMEM lanes 32 (w % 4) .. (its 32 tokens) and the 16-column blocks
+    // part, part + TPT, ... of the accumulator (part = w / 4), adding the bias
+    const int q = warp & 3, part = warp >> 2, r = q * 32 + lane;
+    for (int i = 0; i < nch; ++i) {
+      int c, t0, nt;
+      chunk(i, c, t0, nt);
+      const int acc = i & 1;
+      const uint32_t use = uint32_t(i >> 1) & 1u;
+      const float u_tok = token_u<K, TPT>(a, t0, nt);
+      const bool ok = __all_sync(0xffffffffu, wait_bounded(tfull0 + 8 * acc, use, &s_abort, a.status, wlimit));
+      if (ok) {  // after a timeout the body below runs, in bounds, on the stale buffer
+        tc_fence_after();
+        const uint32_t trow = tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
+        const bool store = f.logits_out != nullptr && r < nt;
+        float* dst = store ? f.logits_out + size_t(t0 + r) * E : nullptr;
+        float* row = s_log + r * ld;
+        for (int c0 = part * 16; c0 < BN; c0 += TPT * 16) {
+          uint32_t v[16];
+          tmem_ld16(trow + c0, v);
+          tmem_ld_wait();
+          float l[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            l[jj] = __uint_as_float(v[jj]) + ((f.bias && c0 + jj < E) ? f.bias[c0 + jj] : 0.f);
+          if ((ld & 3) == 0 && c0 + 16 <= E) {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+              reinterpret_cast<float4*>(row + c0)[jj] =
+                  make_float4(l[4 * jj], l[4 * jj + 1], l[4 * jj + 2], l[4 * jj + 3]);
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              if (c0 + jj < E) row[c0 + jj] = l[jj];
+          }
+          if (store) {
+            if ((E & 3) == 0 && c0 + 16 <= E) {
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj)
+                reinterpret_cast<float4*>(dst + c0)[jj] =
+                    make_float4(l[4 * jj], l[4 * jj + 1], l[4 * jj + 2], l[4 * jj + 3]);
+            } else {
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj)
+                if (c0 + jj < E) dst[c0 + jj] = l[jj];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      body_sync<kBody>();  // the chunk's logits are staged; its accumulator is free again
+      if (threadIdx.x == 0 && ok) mbar_arrive(tempty0 + 8 * acc);
+      topk_chunk<K, TPT, VAR, kBody>(a, s_log, c, t0, nt, u_tok);
+      body_sync<kBody>();  // the body's last reads of s_log are done before the next drain
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (s_abort) {
+    // as in the expert GEMM: whichever role gave up, every load issued lands and every MMA
+    // issued finishes before shared and tensor memory are released
+    if (warp == kPW && lane == 0)
+      for (int s = 0; s < NS; ++s)
+        if ((issued >> s) & 1u) wait_drain(full0 + 8 * s, (issued_par >> s) & 1u);
+    if (warp == kMW && lane == 0 && mma_any && !mma_drained) {
+      mma_commit(drain_bar);
+      wait_drain(drain_bar, 0u);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+  if (warp == kMW) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tcols);
+  }
+}
+
 template <bool VAR, int K, int TPT>
 int launch_topk_t(const RouteArgs& a, int n_chunks, cudaStream_t st) {
   const size_t smem = size_t(kThreads) * (a.E + TPT) * sizeof(float);
@@ -724,10 +1030,50 @@ int launch_router_topk_t(const CUtensorMap& tx, const CUtensorMap& tw, const Rou
                        tx, tw, a, f);
 }
 
-// as launch_topk, with at least two threads per token (the roles need eight warps)
+// The persistent form: one CTA per SM (at most one per chunk), a ring of up to 8 stages in
+// what shared memory the staged logits leave. Returns MOE_ERR_UNSUPPORTED when it does
+// not fit, so that the caller falls back to router_topk_kernel.
+template <bool VAR, int K, int TPT>
+int launch_router_topk_persistent_t(const CUtensorMap& tx, const CUtensorMap& tw,
+                                    const RouteArgs& a, FusedRouterArgs f, int n_chunks,
+                                    cudaStream_t st) {
+  auto kern = router_topk_persistent_kernel<K, TPT, VAR>;
+  static const int64_t static_smem = [&] {
+    cudaFuncAttributes fa;
+    return cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? int64_t(fa.sharedSizeBytes)
+                                                           : int64_t(1) << 30;
+  }();
+  const int stage_bytes = 128 * 64 * 2 + f.BN * 64 * 2;
+  const int64_t stage_log = int64_t(kThreads) * (a.E + TPT) * int64_t(sizeof(float));
+  const int64_t budget = int64_t(227 * 1024) - static_smem - 1024 - stage_log;
+  int stages = budget > 0 ? int(budget / stage_bytes) : 0;
+  if (stages > 8) stages = 8;
+  if (stages > f.Mdim / 64) stages = f.Mdim / 64;
+  if (stages < 2) return MOE_ERR_UNSUPPORTED;
+  f.stages = stages;
+  const size_t smem = size_t(stages) * stage_bytes + stage_log + 1024;
+  MOE_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+  int per_sm = 0;
+  MOE_CUDA_CHECK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads * TPT + 64, smem));
+  if (per_sm < 1) return MOE_ERR_UNSUPPORTED;
+  const int grid = n_chunks < num_sms() ? n_chunks : num_sms();
+  return launch_kernel(kern, dim3(grid), dim3(kThreads * TPT + 64), smem, st, tx, tw, a, f);
+}
+
+// as launch_topk, with at least two threads per token (the roles need eight warps); with
+// more chunks than SMs and at most 64 experts (a body of at most 512 threads, beside which
+// the persistent form's two role warps fit) the persistent form
 template <bool VAR, int K>
 int launch_router_topk(const CUtensorMap& tx, const CUtensorMap& tw, const RouteArgs& a,
                        const FusedRouterArgs& f, int n_chunks, cudaStream_t st) {
+  if constexpr (!VAR) {
+    if (n_chunks > num_sms() && a.E <= 64) {
+      const int rc = a.E <= 32
+                         ? launch_router_topk_persistent_t<VAR, K, 2>(tx, tw, a, f, n_chunks, st)
+                         : launch_router_topk_persistent_t<VAR, K, 4>(tx, tw, a, f, n_chunks, st);
+      if (rc != MOE_ERR_UNSUPPORTED) return rc;
+    }
+  }
   if (a.E <= 32) return launch_router_topk_t<VAR, K, 2>(tx, tw, a, f, n_chunks, st);
   if (a.E <= 64) return launch_router_topk_t<VAR, K, 4>(tx, tw, a, f, n_chunks, st);
   return launch_router_topk_t<VAR, K, 8>(tx, tw, a, f, n_chunks, st);
