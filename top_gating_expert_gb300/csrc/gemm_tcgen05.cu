@@ -56,7 +56,14 @@ constexpr int BM = 128;
 constexpr int BK = 64;  // bf16 elements per 128-byte swizzled row
 constexpr int kMaxGroups = 256;
 
-template <int BN, bool PAIR, bool KRAG = false>
+// The bf16 epilogues whose output goes out through shared memory and TMA stores (see
+// epilogue_bf16_tma): activation (GEMM 1) and gate scaling (GEMM 2).
+template <int EPI, bool KRAG>
+constexpr bool tma_epilogue() {
+  return !KRAG && (EPI == EPI_RELU || EPI == EPI_SWIGLU || EPI == EPI_SCALE);
+}
+
+template <int BN, bool PAIR, bool KRAG = false, bool TEPI = false>
 struct Cfg {
   static constexpr int CTAS = PAIR ? 2 : 1;
   static constexpr int TILE_M = BM * CTAS;  // rows of one output tile
@@ -65,10 +72,13 @@ struct Cfg {
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // K-ragged mode: each epilogue warp stages 32 x 32 fp32 outputs in two 4 KB buffers that
-  // TMA stores to global memory
-  static constexpr int STG_BYTES = KRAG ? 4 * 2 * 4096 : 0;
-  static constexpr int STAGES = ((196608 - STG_BYTES) / STAGE_BYTES) > 8
-                                    ? 8 : ((196608 - STG_BYTES) / STAGE_BYTES);
+  // TMA stores to global memory; the bf16 TMA epilogue, 32 rows x 64 bf16 in one 4 KB buffer
+  static constexpr int STG_BYTES = KRAG ? 4 * 2 * 4096 : (TEPI ? 4 * 4096 : 0);
+  // shared memory a CTA may take (227 KB) less the alignment slack, the barriers (for up to
+  // 8 stages), the TMEM address and flags, and the group tables
+  static constexpr int FIXED = 1024 + (2 * 8 + 5) * 8 + 16 + 3 * (kMaxGroups + 1) * 4;
+  static constexpr int RING = 232448 - FIXED - STG_BYTES;
+  static constexpr int STAGES = (RING / STAGE_BYTES) > 8 ? 8 : (RING / STAGE_BYTES);
   static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + STG_BYTES + BAR_BYTES + 16 +
@@ -312,6 +322,96 @@ __device__ __forceinline__ void epilogue_rows(const KParams& p, uint32_t tbase, 
   }
 }
 
+// The bf16 epilogues (activation, gate scale) of one warp through shared memory: rows
+// grow0 .. grow0 + 31 of the output (the first nvr valid), 64 output columns at a time. The
+// warp reads its accumulator rows from TMEM, applies the epilogue, and, when all 32 rows
+// are valid, writes them as bf16 into a 128-byte-swizzled 32 x 64 box in shared memory
+// (conflict-free) that lane 0 stores with one TMA tensor store; the box is rewritten once
+// that store has read it, a wait that the next columns' TMEM loads and math overlap. A
+// warp whose rows end inside it (the last rows of an expert's segment) stores its valid
+// rows from registers instead, so that no row of the next segment is written. Storing each
+// lane's row directly made every warp store touch 32 lines: with a wide output (GEMM 1's h,
+// d_ff wide) that kept L1 at 70 % of its throughput and the tensor pipe at 77 %.
+template <int BN, int EPI>
+__device__ __forceinline__ void epilogue_bf16_tma(const KParams& p, const CUtensorMap* tmO,
+                                                  uint32_t tbase, int64_t grow0, int nvr, int nt,
+                                                  uint8_t* buf, int lane) {
+  constexpr int OUT_COLS = EPI == EPI_SWIGLU ? BN / 2 : BN;  // output columns of a tile
+  const int64_t ocol0 = int64_t(nt) * OUT_COLS;
+  float scale = 1.f;
+  if (EPI == EPI_SCALE && lane < nvr && p.row_scale) scale = p.row_scale[grow0 + lane];
+  const bool full = nvr == 32;
+  const uint64_t pol = p.out_keep ? policy_evict_last() : 0ull;
+#pragma unroll 1
+  for (int c0 = 0; c0 < OUT_COLS; c0 += 64) {
+    uint32_t pk[32];  // this lane's row: 64 bf16 of the chunk
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // 32 output columns at a time
+      const int c = c0 + 32 * h;
+      if constexpr (EPI == EPI_SWIGLU) {
+        uint32_t g0[16], g1[16], u0[16], u1[16];
+        tmem_ld16(tbase + c, g0);
+        tmem_ld16(tbase + c + 16, g1);
+        tmem_ld16(tbase + BN / 2 + c, u0);
+        tmem_ld16(tbase + BN / 2 + c + 16, u1);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t* gv = j < 8 ? g0 : g1;
+          const uint32_t* uv = j < 8 ? u0 : u1;
+          const int jj = 2 * (j & 7);
+          const float a0 = __uint_as_float(gv[jj]), a1 = __uint_as_float(gv[jj + 1]);
+          const float h0 = a0 / (1.f + __expf(-a0)) * __uint_as_float(uv[jj]);
+          const float h1 = a1 / (1.f + __expf(-a1)) * __uint_as_float(uv[jj + 1]);
+          pk[16 * h + j] = pack_bf16x2(h0, h1);
+        }
+      } else {
+        uint32_t v0[16], v1[16];
+        tmem_ld16(tbase + c, v0);
+        tmem_ld16(tbase + c + 16, v1);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t* v = j < 8 ? v0 : v1;
+          const int jj = 2 * (j & 7);
+          float a0 = __uint_as_float(v[jj]), a1 = __uint_as_float(v[jj + 1]);
+          if (EPI == EPI_RELU) {
+            a0 = fmaxf(a0, 0.f);
+            a1 = fmaxf(a1, 0.f);
+          } else {
+            a0 *= scale;
+            a1 *= scale;
+          }
+          pk[16 * h + j] = pack_bf16x2(a0, a1);
+        }
+      }
+    }
+    if (full) {
+      if (lane == 0) bulk_wait_read<0>();  // the previous box's store has read the buffer
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(buf + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (p.out_keep) tma_store_2d_hint(tmO, int(ocol0 + c0), int(grow0), smem_u32(buf), pol);
+        else tma_store_2d(tmO, int(ocol0 + c0), int(grow0), smem_u32(buf));
+        bulk_commit();
+      }
+    } else if (lane < nvr) {
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (grow0 + lane) * p.ldo + ocol0 + c0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t(&pq)[8] = *reinterpret_cast<const uint32_t(*)[8]>(pk + 8 * q);
+        if (p.out_keep) store_bf16x16_hint(out + 16 * q, pq, pol);
+        else store_bf16x16(out + 16 * q, pq);
+      }
+    }
+  }
+}
+
 // K-ragged mode's fp32 epilogue for one warp: rows grow0 .. grow0 + 31 (the first nvr valid),
 // 32 columns at a time: lanes write their row into a 128-byte-swizzled 32 x 32 staging
 // buffer (conflict-free), fence it for the async proxy, and lane 0 stores it with one TMA
@@ -356,7 +456,7 @@ __device__ __forceinline__ void epilogue_f32_tma(const KParams& p, const CUtenso
     const int col = nt * BN + c0;
     if (lane == 0) {
       if (nvr == 32 && col < p.n_valid)  // weight gradients: not read back by this step
-        tma_store_2d_evict_first(map, col, int(orow), smem_u32(buf), policy_evict_first());
+        tma_store_2d_hint(map, col, int(orow), smem_u32(buf), policy_evict_first());
       // one bulk group per 32 columns, empty when nothing was stored: the wait above counts
       // groups, so a buffer is rewritten only once the store that read it has (a chunk past
       // N or a warp of plain stores that committed nothing would let it overwrite a buffer
@@ -401,13 +501,15 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
                         const __grid_constant__ CUtensorMap tmO,   // K-ragged: fp32 output
                         const __grid_constant__ CUtensorMap tmO2,  // K-ragged: second output
                         const KParams p) {
-  using C = Cfg<BN, PAIR, KRAG>;
+  constexpr bool TEPI = tma_epilogue<EPI, KRAG>();
+  using C = Cfg<BN, PAIR, KRAG, TEPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + C::STAGES * C::A_BYTES;
-  uint8_t* sStg = sB + C::STAGES * C::B_BYTES;  // K-ragged: [4 warps][2][32 rows][128 B], swizzled
+  // output staging: K-ragged [4 warps][2][32 rows][128 B]; bf16 TMA epilogue [4 warps][32][128 B]
+  uint8_t* sStg = sB + C::STAGES * C::B_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + C::STG_BYTES);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
@@ -692,6 +794,11 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
         const int nvr = rows - r0 < 0 ? 0 : (rows - r0 > 32 ? 32 : rows - r0);
         epilogue_f32_tma<BN>(p, &tmO, &tmO2, tbase, int64_t(m0) + r0, nvr, nt, zero,
                              sStg + q * 2 * 4096, lane, stg_buf);
+      } else if constexpr (TEPI) {
+        const int r0 = int(rank) * BM + q * 32;
+        const int nvr = rows - r0 < 0 ? 0 : (rows - r0 > 32 ? 32 : rows - r0);
+        epilogue_bf16_tma<BN, EPI>(p, &tmO, tbase, int64_t(m0) + r0, nvr, nt, sStg + q * 4096,
+                                   lane);
       } else {
         epilogue_rows<BN, EPI>(p, tbase, r < rows, int64_t(m0) + r, nt, zero, part);
       }
@@ -704,8 +811,8 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
         else mbar_arrive_relaxed(tempty0 + 8 * acc);
       }
     }
-    // K-ragged: every TMA store has finished before the CTA's shared memory goes away
-    if constexpr (KRAG && EPI == EPI_F32_BIAS)
+    // every TMA store has finished before the CTA's shared memory goes away
+    if constexpr ((KRAG && EPI == EPI_F32_BIAS) || TEPI)
       if (lane == 0) bulk_wait_all();
   }
 
@@ -782,6 +889,24 @@ int make_map_f32_out(CUtensorMap* m, void* base, int64_t rows, int N) {
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// 2-D bf16 tensor map over a row-major [rows, cols] output with row stride ld elements,
+// 32-row x 64-column boxes, 128-byte swizzle (the bf16 TMA epilogue's stores).
+int make_map_bf16_out(CUtensorMap* m, void* base, int64_t rows, int cols, int64_t ld) {
+  auto fn = encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || (ld * 2) % 16 != 0 || cols < 64 || ld < cols ||
+      rows < 1)
+    return MOE_ERR_INVALID_ARG;
+  cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(ld) * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
 // 3-D bf16 tensor map over a tile-major packed matrix: `blocks` contiguous [block_rows][64]
 // blocks; a box is box_rows rows (all of a block, or half of it for a CTA pair).
 int make_map_tiled(CUtensorMap* m, const void* base, int64_t blocks, int block_rows, int box_rows) {
@@ -800,7 +925,8 @@ int make_map_tiled(CUtensorMap* m, const void* base, int64_t blocks, int block_r
 
 template <int BN, int EPI, bool PAIR, bool KRAG = false, bool MN = false>
 int run_gemm(const GemmDesc& d, cudaStream_t st) {
-  using C = Cfg<BN, PAIR, KRAG>;
+  constexpr bool TEPI = tma_epilogue<EPI, KRAG>();
+  using C = Cfg<BN, PAIR, KRAG, TEPI>;
   CUtensorMap ta, tb;
   if (KRAG && (!d.koffs || d.c1 < 1 || d.b_tiled || d.groups < 1)) return MOE_ERR_INVALID_ARG;
   int rc;
@@ -828,6 +954,11 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
     const int64_t out_rows = int64_t(d.groups) * d.c1 / (d.out2 ? 2 : 1);
     if ((rc = make_map_f32_out(&to, d.out, out_rows, d.N)) != MOE_OK) return rc;
     if (d.out2 && (rc = make_map_f32_out(&to2, d.out2, out_rows, d.N)) != MOE_OK) return rc;
+  }
+  if constexpr (TEPI) {  // the bf16 output [rows, columns] (row stride ldo), 32 x 64 boxes
+    const int64_t out_rows = d.offsets ? d.a_rows : int64_t(d.rows_dense);
+    const int out_cols = EPI == EPI_SWIGLU ? d.N / 2 : d.N;
+    if ((rc = make_map_bf16_out(&to, d.out, out_rows, out_cols, d.ldo)) != MOE_OK) return rc;
   }
   KParams p;
   p.b_tiled = d.b_tiled ? 1 : 0;

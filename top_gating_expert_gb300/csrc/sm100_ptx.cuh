@@ -263,8 +263,9 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
-__device__ __forceinline__ void tma_store_2d_evict_first(const CUtensorMap* map, int x, int y,
-                                                         uint32_t src, uint64_t policy) {
+// TMA tensor store with an L2 cache policy (createpolicy)
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, int x, int y, uint32_t src,
+                                                  uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(map),
       "r"(x), "r"(y), "r"(src), "l"(policy)
