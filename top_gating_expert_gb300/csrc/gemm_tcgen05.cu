@@ -60,7 +60,14 @@ constexpr int kMaxGroups = 256;
 // epilogue_bf16_tma): activation (GEMM 1) and gate scaling (GEMM 2).
 template <int EPI, bool KRAG>
 constexpr bool tma_epilogue() {
-  return !KRAG && (EPI == EPI_RELU || EPI == EPI_SWIGLU || EPI == EPI_SCALE);
+  return !KRAG && (EPI == EPI_RELU || EPI == EPI_SWIGLU || EPI == EPI_SCALE || EPI == EPI_DGRAD2 ||
+                   EPI == EPI_SWIGLU_BWD);
+}
+// its boxes: 32 rows x 64 bf16 (128-byte swizzle, 4 KB) for the four-warp epilogues, 32 rows
+// x 32 bf16 (64-byte swizzle, 2 KB) for the eight-warp data-gradient epilogues: 16 KB a CTA
+template <int EPI>
+constexpr bool tma_box32() {
+  return EPI == EPI_DGRAD2 || EPI == EPI_SWIGLU_BWD;
 }
 
 template <int BN, bool PAIR, bool KRAG = false, bool TEPI = false>
@@ -72,7 +79,8 @@ struct Cfg {
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // K-ragged mode: each epilogue warp stages 32 x 32 fp32 outputs in two 4 KB buffers that
-  // TMA stores to global memory; the bf16 TMA epilogue, 32 rows x 64 bf16 in one 4 KB buffer
+  // TMA stores to global memory; the bf16 TMA epilogue, 16 KB (one box a warp, see
+  // tma_box32)
   static constexpr int STG_BYTES = KRAG ? 4 * 2 * 4096 : (TEPI ? 4 * 4096 : 0);
   // shared memory a CTA may take (227 KB) less the alignment slack, the barriers (for up to
   // 8 stages), the TMEM address and flags, and the group tables
@@ -408,6 +416,142 @@ __device__ __forceinline__ void epilogue_bf16_tma(const KParams& p, const CUtens
         if (p.out_keep) store_bf16x16_hint(out + 16 * q, pq, pol);
         else store_bf16x16(out + 16 * q, pq);
       }
+    }
+  }
+}
+
+// A warp's 32 rows x 32 bf16 columns (pk: this lane's row) at output column col: with all
+// 32 rows valid, through a 64-byte-swizzled 2 KB box in shared memory (16-byte chunk q of
+// row r at r * 64 + ((q ^ ((r >> 1) & 3)) << 4), conflict-free) and one TMA store, once the
+// box's previous store has read it; else each valid row directly.
+__device__ __forceinline__ void store_box32(const KParams& p, const CUtensorMap* tmO, uint8_t* buf,
+                                            const uint32_t (&pk)[16], int64_t col, int64_t grow0,
+                                            int nvr, int lane, uint64_t pol) {
+  if (nvr == 32) {
+    if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(buf + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) =
+          make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (p.out_keep) tma_store_2d_hint(tmO, int(col), int(grow0), smem_u32(buf), pol);
+      else tma_store_2d(tmO, int(col), int(grow0), smem_u32(buf));
+      bulk_commit();
+    }
+  } else if (lane < nvr) {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (grow0 + lane) * p.ldo + col;
+    const uint32_t(&p0)[8] = *reinterpret_cast<const uint32_t(*)[8]>(pk);
+    const uint32_t(&p1)[8] = *reinterpret_cast<const uint32_t(*)[8]>(pk + 8);
+    if (p.out_keep) {
+      store_bf16x16_hint(out, p0, pol);
+      store_bf16x16_hint(out + 16, p1, pol);
+    } else {
+      store_bf16x16(out, p0);
+      store_bf16x16(out + 16, p1);
+    }
+  }
+}
+
+// The data-gradient epilogues of one warp (rows grow0 .., the first nvr valid; half or
+// quarter `part` of the tile's columns), as epilogue_rows computes them, their bf16 output
+// stored 32 columns at a time with store_box32.
+//   EPI_DGRAD2: D = dy_perm . W_out (unscaled); out = w_r * D (ReLU: where h > 0), and the
+//     gate partial sum_c D * h over the half (h as the forward stored it).
+//   EPI_SWIGLU_BWD: D = (a | b), the tile's 128 gate and 128 up pre-activations; with dh:
+//     da = dh * b * silu'(a), db = dh * silu(a), at the same interleaved columns.
+template <int BN, int EPI>
+__device__ __forceinline__ void epilogue_dgrad_tma(const KParams& p, const CUtensorMap* tmO,
+                                                   uint32_t tbase, int64_t grow0, int nvr, int nt,
+                                                   int part, uint8_t* buf, int lane) {
+  const bool valid = lane < nvr;
+  const int64_t grow = grow0 + lane;
+  const uint64_t pol = p.out_keep ? policy_evict_last() : 0ull;
+  if constexpr (EPI == EPI_DGRAD2) {
+    constexpr int kHalf = BN / 2;
+    const int cb = part * kHalf, ce = cb + kHalf;
+    const float scale = (valid && p.row_scale) ? p.row_scale[grow] : 1.f;
+    const __nv_bfloat16* hrow = static_cast<const __nv_bfloat16*>(p.aux) + grow * p.ld_aux + nt * BN;
+    float gsum = 0.f;
+    uint4 hn[4];  // h of the next 32 columns, loaded before this step's math
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      hn[q] = valid ? __ldg(reinterpret_cast<const uint4*>(hrow + cb) + q) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+    for (int c0 = cb; c0 < ce; c0 += 32) {
+      uint4 hc[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) hc[q] = hn[q];
+      if (valid && c0 + 32 < ce) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) hn[q] = __ldg(reinterpret_cast<const uint4*>(hrow + c0 + 32) + q);
+      }
+      uint32_t v[32];
+      tmem_ld16(tbase + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+      tmem_ld16(tbase + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+      tmem_ld_wait();
+      const uint32_t* hw = reinterpret_cast<const uint32_t*>(hc);
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float2 hv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[j]));
+        const float d0 = __uint_as_float(v[2 * j]), d1 = __uint_as_float(v[2 * j + 1]);
+        gsum += d0 * hv.x + d1 * hv.y;
+        float o0 = d0 * scale, o1 = d1 * scale;
+        if (p.relu) {
+          o0 = hv.x > 0.f ? o0 : 0.f;
+          o1 = hv.y > 0.f ? o1 : 0.f;
+        }
+        pk[j] = pack_bf16x2(o0, o1);
+      }
+      store_box32(p, tmO, buf, pk, int64_t(nt) * BN + c0, grow0, nvr, lane, pol);
+    }
+    if (valid && p.gpart) p.gpart[(grow * p.n_tiles + nt) * 2 + part] = gsum;
+  } else {
+    constexpr int kQuarter = BN / 4;
+    const int cb = part * kQuarter, ce = cb + kQuarter;
+    const __nv_bfloat16* dhrow =
+        static_cast<const __nv_bfloat16*>(p.aux) + grow * p.ld_aux + nt * (BN / 2);
+    uint4 dn[4];  // the next 32 hidden units' dh, loaded before this step's math
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      dn[q] = valid ? __ldg(reinterpret_cast<const uint4*>(dhrow + cb) + q) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+    for (int c0 = cb; c0 < ce; c0 += 32) {
+      uint4 dc[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dc[q] = dn[q];
+      if (valid && c0 + 32 < ce) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dn[q] = __ldg(reinterpret_cast<const uint4*>(dhrow + c0 + 32) + q);
+      }
+      uint32_t av[32], bv[32];
+      tmem_ld16(tbase + c0, *reinterpret_cast<uint32_t(*)[16]>(av));
+      tmem_ld16(tbase + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(av + 16));
+      tmem_ld16(tbase + BN / 2 + c0, *reinterpret_cast<uint32_t(*)[16]>(bv));
+      tmem_ld16(tbase + BN / 2 + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(bv + 16));
+      tmem_ld_wait();
+      const uint32_t* dw = reinterpret_cast<const uint32_t*>(dc);
+      uint32_t pa[16], pb[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float2 dh = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[j]));
+        float da[2], db[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float a = __uint_as_float(av[2 * j + q]), b = __uint_as_float(bv[2 * j + q]);
+          const float sg = 1.f / (1.f + __expf(-a));
+          const float d = q ? dh.y : dh.x;
+          da[q] = d * b * sg * (1.f + a * (1.f - sg));
+          db[q] = d * a * sg;
+        }
+        pa[j] = pack_bf16x2(da[0], da[1]);
+        pb[j] = pack_bf16x2(db[0], db[1]);
+      }
+      store_box32(p, tmO, buf, pa, int64_t(nt) * BN + c0, grow0, nvr, lane, pol);
+      store_box32(p, tmO, buf, pb, int64_t(nt) * BN + BN / 2 + c0, grow0, nvr, lane, pol);
     }
   }
 }
@@ -794,6 +938,11 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
         const int nvr = rows - r0 < 0 ? 0 : (rows - r0 > 32 ? 32 : rows - r0);
         epilogue_f32_tma<BN>(p, &tmO, &tmO2, tbase, int64_t(m0) + r0, nvr, nt, zero,
                              sStg + q * 2 * 4096, lane, stg_buf);
+      } else if constexpr (TEPI && tma_box32<EPI>()) {
+        const int r0 = int(rank) * BM + q * 32;
+        const int nvr = rows - r0 < 0 ? 0 : (rows - r0 > 32 ? 32 : rows - r0);
+        epilogue_dgrad_tma<BN, EPI>(p, &tmO, tbase, int64_t(m0) + r0, nvr, nt, part,
+                                    sStg + (warp - 2) * 2048, lane);
       } else if constexpr (TEPI) {
         const int r0 = int(rank) * BM + q * 32;
         const int nvr = rows - r0 < 0 ? 0 : (rows - r0 > 32 ? 32 : rows - r0);
@@ -890,19 +1039,21 @@ int make_map_f32_out(CUtensorMap* m, void* base, int64_t rows, int N) {
 }
 
 // 2-D bf16 tensor map over a row-major [rows, cols] output with row stride ld elements,
-// 32-row x 64-column boxes, 128-byte swizzle (the bf16 TMA epilogue's stores).
-int make_map_bf16_out(CUtensorMap* m, void* base, int64_t rows, int cols, int64_t ld) {
+// boxes of 32 rows x box_cols columns: 64 with the 128-byte swizzle, 32 with the 64-byte
+// swizzle (the bf16 TMA epilogues' stores).
+int make_map_bf16_out(CUtensorMap* m, void* base, int64_t rows, int cols, int64_t ld, int box_cols) {
   auto fn = encode_fn();
   if (!fn) return MOE_ERR_CUDA;
-  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || (ld * 2) % 16 != 0 || cols < 64 || ld < cols ||
-      rows < 1)
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || (ld * 2) % 16 != 0 || cols < box_cols ||
+      ld < cols || rows < 1 || (box_cols != 64 && box_cols != 32))
     return MOE_ERR_INVALID_ARG;
   cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
   cuuint64_t strides[1] = {cuuint64_t(ld) * 2};
-  cuuint32_t box[2] = {64, 32};
+  cuuint32_t box[2] = {cuuint32_t(box_cols), 32};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -955,10 +1106,12 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
     if ((rc = make_map_f32_out(&to, d.out, out_rows, d.N)) != MOE_OK) return rc;
     if (d.out2 && (rc = make_map_f32_out(&to2, d.out2, out_rows, d.N)) != MOE_OK) return rc;
   }
-  if constexpr (TEPI) {  // the bf16 output [rows, columns] (row stride ldo), 32 x 64 boxes
+  if constexpr (TEPI) {  // the bf16 output [rows, columns] (row stride ldo)
     const int64_t out_rows = d.offsets ? d.a_rows : int64_t(d.rows_dense);
     const int out_cols = EPI == EPI_SWIGLU ? d.N / 2 : d.N;
-    if ((rc = make_map_bf16_out(&to, d.out, out_rows, out_cols, d.ldo)) != MOE_OK) return rc;
+    if ((rc = make_map_bf16_out(&to, d.out, out_rows, out_cols, d.ldo, tma_box32<EPI>() ? 32 : 64)) !=
+        MOE_OK)
+      return rc;
   }
   KParams p;
   p.b_tiled = d.b_tiled ? 1 : 0;
