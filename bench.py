@@ -22,10 +22,12 @@ each step one bounded sample of the same workload; under torchrun only rank 0 ru
 from __future__ import annotations
 
 import argparse
+import faulthandler
 import hashlib
 import json
 import os
 import platform
+import signal
 import statistics
 import subprocess
 import sys
@@ -48,6 +50,14 @@ L2_POLICY = ("GPU: L2 flushed before every timed step, outside its events (256 M
 CPU_FLOPS_HEADLINE = 6.0e12
 CPU_FLOPS_PRESET = 1.2e12
 CPU_FLOPS_REFERENCE_STEP = 0.8e12
+
+
+_T0 = time.perf_counter()
+
+
+def log(msg: str):
+    """A progress line on stderr (the JSON line alone goes to stdout)."""
+    print(f"[bench {time.perf_counter() - _T0:7.1f} s] {msg}", file=sys.stderr, flush=True)
 
 
 def parse(argv=None):
@@ -400,9 +410,11 @@ def run_preset(args, n, cfg, rank, world, dev, flush, barrier, *, headline: bool
     from top_gating_expert_gb300 import moe
     from top_gating_expert_gb300.inputs import make_inputs
 
+    log(f"preset {n}: drawing inputs")
     inp = make_inputs(cfg, preset_number=n)
     # the layer's step output is y and the losses: the bf16 path never writes the logits
     layer = moe.MoeLayer(cfg, inp.host, device=dev, keep_logits=False)
+    log(f"preset {n}: weights packed")
     c = layer.cfg
     x = inp.host["x"].to(dev)
     u = inp.host["u"].to(dev) if cfg["random_routing"] else None
@@ -460,6 +472,7 @@ def run_preset(args, n, cfg, rank, world, dev, flush, barrier, *, headline: bool
     check("after warm-up")
 
     # ---- the whole forward (moe_layer_forward) captured once as a CUDA graph
+    log(f"preset {n}: step-wise warm-up done; capturing the forward")
     graph_ok = True
     try:
         layer.capture(x, u, residual)
@@ -506,6 +519,7 @@ def run_preset(args, n, cfg, rank, world, dev, flush, barrier, *, headline: bool
 
     # ---- per-kernel times: the same launches through the step-wise calls, an event between
     # consecutive calls (a second timed region of the same K steps)
+    log(f"preset {n}: graph timed; per-kernel timing")
     nev = len(names) + 1
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
     barrier()
@@ -521,6 +535,7 @@ def run_preset(args, n, cfg, rank, world, dev, flush, barrier, *, headline: bool
 
     # ---- e2e through the public API: pinned host buffers in and out, every step copying its
     # own inputs to the device and its result back (HostPipeline: two steps in flight)
+    log(f"preset {n}: host-to-host timing")
     x_host = inp.host["x"].pin_memory()
     u_host = inp.host["u"].pin_memory() if u is not None else None
     y_host = torch.empty((c.S, c.M), dtype=dt).pin_memory()
@@ -545,6 +560,7 @@ def run_preset(args, n, cfg, rank, world, dev, flush, barrier, *, headline: bool
     # moe_layer_backward on the same inputs, L2 flushed before each step
     bwd = None
     if cfg["dtype"] == "bf16" and not args.no_backward:
+        log(f"preset {n}: backward")
         del x_perm, h_perm, y_perm
         tl = moe.MoeLayer(cfg, inp.host, device=dev)
         tl.enable_backward(inp.host)
@@ -580,6 +596,7 @@ def run_preset(args, n, cfg, rank, world, dev, flush, barrier, *, headline: bool
 
     var = None
     if variants and fused and not args.no_variants:
+        log(f"preset {n}: routing variants")
         var = time_variants(args, cfg, c, x, layer, bias, u, flush, barrier, world, dev,
                             per_kernel["router_route"])
         var["preset"] = n
@@ -628,8 +645,10 @@ def run_preset(args, n, cfg, rank, world, dev, flush, barrier, *, headline: bool
     if var is not None:
         res["variants"] = var
     if world == 1 and not args.no_cpu_baseline:
+        log(f"preset {n}: oracle on the host")
         res["cpu_baseline"] = cpu_baseline(cfg, n, inp,
                                            CPU_FLOPS_HEADLINE if headline else CPU_FLOPS_PRESET)
+    log(f"preset {n}: done")
     return res
 
 
@@ -879,6 +898,11 @@ def run_reference(args, rank, world):
 
 def main():
     args = parse()
+    # a run that should take minutes: after 15 minutes, every thread's Python stack goes to
+    # stderr (every 5 minutes), so that a stalled phase can be located afterwards
+    faulthandler.dump_traceback_later(900, repeat=True, file=sys.stderr)
+    if hasattr(signal, "SIGUSR1"):  # and on demand (kill -USR1)
+        faulthandler.register(signal.SIGUSR1, file=sys.stderr, all_threads=True)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
