@@ -143,6 +143,9 @@ def test_compute_entry_points_check_arguments_on_host(native_lib):
     assert L.moe_router_route(ctypes.byref(c32), fake, fake, None, fake, None, ctypes.byref(out2),
                               fake, moe.workspace_bytes(c32, N.MOE_WS_STEP), None) == -1  # fp32 needs logits_out
     assert L.moe_get_device_status(None, None) == -1
+    # the wait limit lives in a workspace header: null or misaligned workspaces are refused
+    assert L.moe_set_wait_limit(None, 1000, None) == -1
+    assert L.moe_set_wait_limit(ctypes.c_void_p((1 << 20) + 8), 1000, None) == -1
     # shared-expert calls need shared experts
     assert L.moe_shared_ffn(ctypes.byref(c), fake, fake, fake, fake, fake, fake, need, None) == -1
 
