@@ -78,10 +78,15 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  // K-ragged mode: each epilogue warp stages 32 x 32 fp32 outputs in two 4 KB buffers that
-  // TMA stores to global memory; the bf16 TMA epilogue, 16 KB (one box a warp, see
-  // tma_box32)
-  static constexpr int STG_BYTES = KRAG ? 4 * 2 * 4096 : (TEPI ? 4 * 4096 : 0);
+  // K-ragged mode: each epilogue warp stages fp32 outputs in boxes of 32 rows x F32_BOX
+  // columns that TMA stores to global memory: 32 columns (128-byte rows, 4 KB, two buffers a
+  // warp) for single-CTA tiles; 16 columns (64-byte rows, 2 KB, three buffers) for CTA pairs,
+  // whose 32 KB k-blocks then get a sixth ring stage. (Single-CTA 256-wide tiles would get a
+  // fourth 48 KB stage the same way, but there the twice as many, half-size stores cost more
+  // than the stage gains.) The bf16 TMA epilogue: 16 KB (one box a warp, see tma_box32).
+  static constexpr int F32_BOX = PAIR ? 16 : 32;
+  static constexpr int F32_BUFS = PAIR ? 3 : 2;
+  static constexpr int STG_BYTES = KRAG ? 4 * F32_BUFS * 32 * F32_BOX * 4 : (TEPI ? 4 * 4096 : 0);
   // shared memory a CTA may take (227 KB) less the alignment slack, the barriers (for up to
   // 8 stages), the TMEM address and flags, and the group tables
   static constexpr int FIXED = 1024 + (2 * 8 + 5) * 8 + 16 + 3 * (kMaxGroups + 1) * 4;
@@ -557,16 +562,24 @@ __device__ __forceinline__ void epilogue_dgrad_tma(const KParams& p, const CUten
 }
 
 // K-ragged mode's fp32 epilogue for one warp: rows grow0 .. grow0 + 31 (the first nvr valid),
-// 32 columns at a time: lanes write their row into a 128-byte-swizzled 32 x 32 staging
-// buffer (conflict-free), fence it for the async proxy, and lane 0 stores it with one TMA
-// tensor store (two buffers alternate; a buffer is rewritten once its earlier store has
-// read it). A warp whose rows end inside it (the last rows of a one-group output) stores
-// its valid rows from the buffer with plain stores instead.
-template <int BN>
+// BOX (32 or 16) columns at a time: lanes write their row into a swizzled 32 x BOX staging
+// buffer (128- or 64-byte swizzle, conflict-free), fence it for the async proxy, and lane 0
+// stores it with one TMA tensor store (NBUF buffers in turn; a buffer is rewritten once the
+// store that last read it has finished reading). A warp whose rows end inside it (the last
+// rows of a one-group output) stores its valid rows from the buffer with plain stores
+// instead.
+template <int BN, int BOX, int NBUF>
 __device__ __forceinline__ void epilogue_f32_tma(const KParams& p, const CUtensorMap* tmO,
                                                  const CUtensorMap* tmO2, uint32_t tbase,
                                                  int64_t grow0, int nvr, int nt, bool zero,
                                                  uint8_t* bufs, int lane, int& nb) {
+  static_assert(BOX == 32 || BOX == 16, "fp32 staging boxes are 32 or 16 columns");
+  constexpr int kRowBytes = BOX * 4;           // one staged row
+  constexpr int kBufBytes = 32 * kRowBytes;
+  constexpr int kLanesPerRow = BOX / 4;        // plain-store path: 16 bytes a lane
+  // the 16-byte chunk c of row r sits at chunk c ^ (r & 7) (128-byte swizzle) or
+  // c ^ ((r >> 1) & 3) (64-byte swizzle)
+  auto chunk = [](int c, int r) { return BOX == 32 ? (c ^ (r & 7)) : (c ^ ((r >> 1) & 3)); };
   const CUtensorMap* map = tmO;
   int64_t orow = grow0;
   float* out0 = static_cast<float*>(p.out);
@@ -579,21 +592,20 @@ __device__ __forceinline__ void epilogue_f32_tma(const KParams& p, const CUtenso
     }
   }
 #pragma unroll 1
-  for (int c0 = 0; c0 < BN; c0 += 32) {
-    uint32_t v0[16], v1[16];
-    tmem_ld16(tbase + c0, v0);
-    tmem_ld16(tbase + c0 + 16, v1);
+  for (int c0 = 0; c0 < BN; c0 += BOX) {
+    uint32_t v[BOX];
+    tmem_ld16(tbase + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+    if constexpr (BOX == 32) tmem_ld16(tbase + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
     tmem_ld_wait();
-    uint8_t* buf = bufs + nb * 4096;
-    if (lane == 0) bulk_wait_read<1>();
+    uint8_t* buf = bufs + nb * kBufBytes;
+    if (lane == 0) bulk_wait_read<NBUF - 1>();
     __syncwarp();
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t* v = c < 4 ? v0 + 4 * c : v1 + 4 * (c - 4);
+    for (int c = 0; c < BOX / 4; ++c) {
       const float4 f = zero ? make_float4(0.f, 0.f, 0.f, 0.f)
-                            : make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]),
-                                          __uint_as_float(v[2]), __uint_as_float(v[3]));
-      *reinterpret_cast<float4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) = f;
+                            : make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                                          __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+      *reinterpret_cast<float4*>(buf + lane * kRowBytes + (chunk(c, lane) << 4)) = f;
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -601,26 +613,26 @@ __device__ __forceinline__ void epilogue_f32_tma(const KParams& p, const CUtenso
     if (lane == 0) {
       if (nvr == 32 && col < p.n_valid)  // weight gradients: not read back by this step
         tma_store_2d_hint(map, col, int(orow), smem_u32(buf), policy_evict_first());
-      // one bulk group per 32 columns, empty when nothing was stored: the wait above counts
+      // one bulk group per box, empty when nothing was stored: the wait above counts
       // groups, so a buffer is rewritten only once the store that read it has (a chunk past
       // N or a warp of plain stores that committed nothing would let it overwrite a buffer
       // a TMA store is still reading)
       bulk_commit();
     }
     if (nvr < 32 && nvr > 0) {
-      const int cl = (lane & 7) * 4;
+      const int cl = (lane % kLanesPerRow) * 4;
 #pragma unroll 1
-      for (int pass = 0; pass < 8; ++pass) {
-        const int rr = pass * 4 + (lane >> 3);
+      for (int pass = 0; pass < kLanesPerRow; ++pass) {
+        const int rr = pass * (32 / kLanesPerRow) + lane / kLanesPerRow;
         if (rr < nvr && col + cl < p.n_valid) {
-          const float* sv = reinterpret_cast<const float*>(buf + rr * 128 + (((cl >> 2) ^ (rr & 7)) << 4));
+          const float* sv = reinterpret_cast<const float*>(buf + rr * kRowBytes + (chunk(cl >> 2, rr) << 4));
           float* out = out0 + (orow + rr) * p.ldo + col + cl;
           for (int i = 0; i < 4 && col + cl + i < p.n_valid; ++i) out[i] = sv[i];
         }
       }
     }
     __syncwarp();
-    nb ^= 1;
+    nb = nb + 1 == NBUF ? 0 : nb + 1;
   }
 }
 
@@ -936,8 +948,9 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
       if constexpr (KRAG && EPI == EPI_F32_BIAS) {
         const int r0 = int(rank) * BM + q * 32;  // this warp's first row in the tile
         const int nvr = rows - r0 < 0 ? 0 : (rows - r0 > 32 ? 32 : rows - r0);
-        epilogue_f32_tma<BN>(p, &tmO, &tmO2, tbase, int64_t(m0) + r0, nvr, nt, zero,
-                             sStg + q * 2 * 4096, lane, stg_buf);
+        epilogue_f32_tma<BN, C::F32_BOX, C::F32_BUFS>(p, &tmO, &tmO2, tbase, int64_t(m0) + r0, nvr,
+                                                      nt, zero, sStg + q * (C::STG_BYTES / 4),
+                                                      lane, stg_buf);
       } else if constexpr (TEPI && tma_box32<EPI>()) {
         const int r0 = int(rank) * BM + q * 32;
         const int nvr = rows - r0 < 0 ? 0 : (rows - r0 > 32 ? 32 : rows - r0);
@@ -1022,18 +1035,19 @@ int make_map(CUtensorMap* m, const void* base, int64_t rows, int K, int box_rows
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
-// 2-D fp32 tensor map over a row-major [rows, N] output, 32 x 32 boxes, 128-byte swizzle
-// (the K-ragged epilogue's TMA stores).
-int make_map_f32_out(CUtensorMap* m, void* base, int64_t rows, int N) {
+// 2-D fp32 tensor map over a row-major [rows, N] output, boxes of 32 rows x box_cols columns:
+// 32 with the 128-byte swizzle, 16 with the 64-byte one (the K-ragged epilogue's TMA stores).
+int make_map_f32_out(CUtensorMap* m, void* base, int64_t rows, int N, int box_cols) {
   auto fn = encode_fn();
   if (!fn) return MOE_ERR_CUDA;
   if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || (int64_t(N) * 4) % 16 != 0) return MOE_ERR_INVALID_ARG;
   cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(rows)};
   cuuint64_t strides[1] = {cuuint64_t(N) * 4};
-  cuuint32_t box[2] = {32, 32};
+  cuuint32_t box[2] = {cuuint32_t(box_cols), 32};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -1103,8 +1117,9 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
   if constexpr (KRAG) {
     if (d.epi != EPI_F32_BIAS || d.ldo != d.N) return MOE_ERR_UNSUPPORTED;
     const int64_t out_rows = int64_t(d.groups) * d.c1 / (d.out2 ? 2 : 1);
-    if ((rc = make_map_f32_out(&to, d.out, out_rows, d.N)) != MOE_OK) return rc;
-    if (d.out2 && (rc = make_map_f32_out(&to2, d.out2, out_rows, d.N)) != MOE_OK) return rc;
+    if ((rc = make_map_f32_out(&to, d.out, out_rows, d.N, C::F32_BOX)) != MOE_OK) return rc;
+    if (d.out2 && (rc = make_map_f32_out(&to2, d.out2, out_rows, d.N, C::F32_BOX)) != MOE_OK)
+      return rc;
   }
   if constexpr (TEPI) {  // the bf16 output [rows, columns] (row stride ldo)
     const int64_t out_rows = d.offsets ? d.a_rows : int64_t(d.rows_dense);
