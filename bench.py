@@ -42,6 +42,11 @@ UNIT = "tokens/s"
 FLUSH_BYTES = 256 << 20
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.md")
 HEADLINE = 3  # the largest preset by work
+# steps in flight in the host-to-host leg: with two, a 134 MB input copy, the layer and the
+# 134 MB output copy of one buffer set (≈ 0.65 + 1.1 + 0.7 ms at the ≈ 200 GB/s a pinned copy
+# reaches over the host link, preset 5) bound a step at half their sum; three measured 11 %
+# faster there (50.3 -> 55.7 M tokens/s), four no faster
+E2E_DEPTH = 3
 L2_POLICY = ("GPU: L2 flushed before every timed step, outside its events (256 MiB write, "
              "then 256 MiB read, so dirty lines are written back outside the step); "
              "host-to-host e2e: not flushed, inputs arrive from host memory")
@@ -534,13 +539,16 @@ def run_preset(args, n, cfg, rank, world, dev, flush, barrier, *, headline: bool
     per_kernel = dict(zip(names, max_over_ranks(pk, world, dev)))
 
     # ---- e2e through the public API: pinned host buffers in and out, every step copying its
-    # own inputs to the device and its result back (HostPipeline: two steps in flight)
+    # own inputs to the device and its result back (HostPipeline: E2E_DEPTH steps in flight,
+    # so that a buffer set's input copy, layer and output copy together may take up to that
+    # many steps' time)
     log(f"preset {n}: host-to-host timing")
     x_host = inp.host["x"].pin_memory()
     u_host = inp.host["u"].pin_memory() if u is not None else None
     y_host = torch.empty((c.S, c.M), dtype=dt).pin_memory()
     loss_host = torch.empty(2, dtype=torch.float32).pin_memory()
-    pipe = moe.HostPipeline(layer, has_u=u is not None, residual=residual is not None)
+    pipe = moe.HostPipeline(layer, has_u=u is not None, residual=residual is not None,
+                            depth=E2E_DEPTH)
     for i in range(args.warmup):
         pipe.submit(i, x_host, u_host, y_host, loss_host)
     barrier()
@@ -623,7 +631,7 @@ def run_preset(args, n, cfg, rank, world, dev, flush, barrier, *, headline: bool
         "kernels": kernel_table(names, per_kernel, algo, P),
         "e2e": {"value": round(job_throughput(S, args.steps, world, e2e_ms), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "api": "HostPipeline.submit (pinned host in/out, 2 steps in flight) -> "
+                "api": f"HostPipeline.submit (pinned host in/out, {E2E_DEPTH} steps in flight) -> "
                        "moe_layer_forward (CUDA graph); L2 not flushed: inputs arrive from host"},
         # moe_layer_forward runs the routing's last kernel and the dispatch as one launch
         "launches_per_step": sum(LAUNCHES[nm] for nm in names) - 1,

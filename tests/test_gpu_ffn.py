@@ -274,23 +274,26 @@ def test_graph_replay_equals_eager(run):
     assert np.array_equal(to_np(y), run["y"])
 
 
-def test_host_pipeline_matches_eager(run):
-    """HostPipeline (pinned host in/out, two steps in flight) returns, step by step, the bits
-    of the eager forward on the same inputs."""
+@pytest.mark.parametrize("depth", [2, 3])
+def test_host_pipeline_matches_eager(run, depth):
+    """HostPipeline (pinned host in/out, two or three steps in flight) returns, step by step,
+    the bits of the eager forward on the same inputs; five steps, so that every buffer set
+    is reused."""
     cfg = run["cfg"]
     layer = moe.MoeLayer(cfg, {k: run["inp"].host[k] for k in run["inp"].host})
     rr = bool(cfg["random_routing"])
-    pipe = moe.HostPipeline(layer, has_u=rr)
+    pipe = moe.HostPipeline(layer, has_u=rr, depth=depth)
     x0 = run["inp"].host["x"]
-    xs = [(x0 * (1.0 + 0.25 * i)).to(x0.dtype).pin_memory() for i in range(3)]
+    n = 5
+    xs = [(x0 * (1.0 + 0.25 * i)).to(x0.dtype).pin_memory() for i in range(n)]
     u_host = run["inp"].host["u"].pin_memory() if rr else None
-    ys = [torch.empty_like(x0).pin_memory() for _ in range(3)]
-    losses = [torch.empty(2, dtype=torch.float32).pin_memory() for _ in range(3)]
-    for i in range(3):
+    ys = [torch.empty_like(x0).pin_memory() for _ in range(n)]
+    losses = [torch.empty(2, dtype=torch.float32).pin_memory() for _ in range(n)]
+    for i in range(n):
         pipe.submit(i, xs[i], u_host, ys[i], losses[i])
     torch.cuda.synchronize()
     assert moe.device_status(layer.ws) == 0
-    for i in range(3):
+    for i in range(n):
         y = layer.forward(xs[i].cuda(), u_host.cuda() if rr else None)
         torch.cuda.synchronize()
         assert torch.equal(ys[i], y.cpu()), i
