@@ -45,6 +45,14 @@ CASES = {
     # weight-gradient outputs whose last 256-wide N tile ends part-way (448 = 256 + 192,
     # 320 = 256 + 64): the epilogue's chunks past N store nothing
     "ragged_n_tiles": (_cfg(S=2048, E=8, M=320, H=448, k=2), False),
+    # grouped routing with a capacity bounding every expert's rows by groups x capacity
+    # <= 256: both routed weight gradients run the resident-B kernel. 8 x 32 = 256 rows (four
+    # 64-row k-blocks) at most, ragged per expert, with random routing
+    "grouped_short_k_rr": (_cfg(S=2048, G=8, E=16, capacity_factor=1.0, random_routing=1), False),
+    # 4 x 48 = 192 (three k-blocks); SwiGLU (dW_in's rows split between dW_in and dW_up),
+    # dW_out's last N tile ending part-way (384 = 256 + 128)
+    "grouped_short_k_swiglu": (_cfg(S=1024, G=4, E=8, H=384, capacity_factor=0.75,
+                                    act="swiglu"), True),
 }
 AUX, Z = 0.7, 0.3
 

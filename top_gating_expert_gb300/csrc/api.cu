@@ -532,10 +532,12 @@ int ffn_backward_data(const moe_config_t& c, const FfnBwd& f, unsigned* status, 
 // dW[g] (fp32 [c1][N]) = A_g . B_g^T over group g's padded K segment (A [c1][Kp], B [N][Kp]).
 // dW[g] = A_g^T . B_g over K-row ranges, both operands row-major and read in place (MN-major
 // tcgen05 operands): A [a_krows, c1], B [b_krows, N]; group g takes koffs[g+1] - koffs[g]
-// rows (a multiple of 64) from row aoffs[g] of A and boffs[g] of B (null: koffs[g]).
+// rows (a multiple of 64) from row aoffs[g] of A and boffs[g] of B (null: koffs[g]). k_max:
+// a bound on every group's range known to the caller (0: none).
 int weight_grad_mn(const void* A, int64_t a_krows, const int32_t* aoffs, int c1, const void* B,
                    int64_t b_krows, const int32_t* boffs, int N, int64_t Kp, const int32_t* koffs,
-                   int groups, float* out, float* out2, unsigned* status, cudaStream_t st) {
+                   int groups, float* out, float* out2, unsigned* status, cudaStream_t st,
+                   int k_max = 0) {
   GemmDesc d;
   d.epi = EPI_F32_BIAS;
   d.mn = true;
@@ -544,6 +546,7 @@ int weight_grad_mn(const void* A, int64_t a_krows, const int32_t* aoffs, int c1,
   d.koffs = koffs; d.c1 = c1; d.groups = groups;
   d.out = out; d.ldo = N; d.n_valid = N; d.out2 = out2;
   d.status = status;
+  d.k_max = k_max;
   return launch_gemm_bf16(d, st);
 }
 
@@ -605,13 +608,17 @@ int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, c
   if ((rc = launch_pad_gather(x, c.M, r->token_of, nullptr, r->expert_offsets, poff, c.E, c.S,
                               B.Rp, w + B.xP, w + B.dab, F, status, stream)) != MOE_OK)
     return rc;
+  // with a capacity, an expert keeps at most C rows of each of the G groups: its padded K
+  // range is at most G C rounded up to 64
+  const int64_t kcap = p.C > 0 ? (int64_t(c.G) * p.C + 63) / 64 * 64 : 0;
+  const int k_max = kcap <= INT32_MAX ? int(kcap) : 0;
   if ((rc = weight_grad_mn(w + B.wdyP, B.Rp, nullptr, c.M, fw + p.L.h_perm, R + 64,
                            r->expert_offsets, c.H, B.Rp, poff, c.E, grads->dW_out, nullptr, status,
-                           stream)) != MOE_OK)
+                           stream, k_max)) != MOE_OK)
     return rc;
   if ((rc = weight_grad_mn(w + B.dab, R + 64, r->expert_offsets, F, w + B.xP, B.Rp, nullptr, c.M,
                            B.Rp, poff, c.E, grads->dW_in, sw ? grads->dW_up : nullptr, status,
-                           stream)) != MOE_OK)
+                           stream, k_max)) != MOE_OK)
     return rc;
   // K = all S tokens (padded to 64) for the router's dW_g and the shared experts: the tensors
   // end at row S, so the padding reads as zeros

@@ -1005,6 +1005,302 @@ __global__ void __launch_bounds__(64 + 32 * epi_warps<EPI, KRAG>(), 1)
   }
 }
 
+// ------------------------------------------------------------------ short-K weight gradients
+// K-ragged, MN-major weight gradients (dW[g] = A_g^T . B_g over group g's K rows) when every
+// group's K range is at most kResKB k-blocks: the GShard grouped layer's experts, whose rows
+// are at most (groups x capacity) = 256. A tile (128 output rows x 256 columns) then takes
+// only 4 k-blocks, and the tiles of one (group, N tile) all read the same 256 columns of B.
+// The work goes in runs: (group, chunk of kRunM m-tiles, N tile), N tile innermost, the CTAs
+// taking runs grid-strided, so that the runs in flight at one time share their A rows and
+// the B of their group through L2. A CTA keeps its run's B k-blocks resident in kResKB fixed
+// slots (32 KB each), loaded once per run, while A streams through its own ring. Such a
+// GEMM is bound by its fp32 epilogue, which stores at about the rate HBM absorbs writes
+// from every SM; what the B reuse buys is an MMA that keeps the accumulators ready.
+// Measured on the GShard grouped layer's backward (two such GEMMs, 2.15 GB of fp32 each):
+// runs of 2 m-tiles 1.387 ms, of 1, 3, 4 or 8: 1.474, 1.437, 1.437, 1.437 ms, against
+// 1.428 ms for the streamed-B kernel (longer runs leave the CTAs' last runs uneven). Roles as in grouped_gemm_kernel: warp 0 the
+// TMA producer, warp 1 the MMA issuer (two TMEM accumulators), warps 2..5 the fp32 TMA-store
+// epilogue. Slot kb's barriers: b_full completes once per run that loads it, b_empty once
+// per run that used it (the MMA thread commits it after the run's last tile), so neither
+// can run two phases ahead of its waiter.
+constexpr int kResKB = 4;
+constexpr int kRunM = 2;  // m-tiles a run (the group's last may hold one)
+
+struct ResCfg {
+  static constexpr int BN = 256;
+  static constexpr int A_BYTES = BM * BK * 2;  // 64 K rows x 128 output rows: two 64-column boxes
+  static constexpr int B_BYTES = BN * BK * 2;  // 64 K rows x 256 columns: four boxes
+  static constexpr int STG_BYTES = 4 * 2 * 4096;                  // fp32 staging, 32 x 32 boxes
+  static constexpr int NBARS = 2 * 8 + 2 * kResKB + 5;            // A ring, B slots, TMEM, drain
+  static constexpr int TABLE_BYTES = (kMaxGroups + 1) * 4;        // K offsets
+  static constexpr int FIXED = 1024 + NBARS * 8 + 16 + TABLE_BYTES;
+  static constexpr int A_RAW = (232448 - FIXED - kResKB * B_BYTES - STG_BYTES) / A_BYTES;
+  static constexpr int A_STAGES = A_RAW > 8 ? 8 : A_RAW;
+  static constexpr int SMEM = FIXED + kResKB * B_BYTES + A_STAGES * A_BYTES + STG_BYTES;
+};
+static_assert(ResCfg::A_STAGES >= 2, "the A ring needs two stages");
+
+__global__ void __launch_bounds__(192, 1)
+    wgrad_resident_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmO,
+                          const __grid_constant__ CUtensorMap tmO2, const KParams p) {
+  using R = ResCfg;
+  constexpr int BN = R::BN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sB = smem;                             // [kResKB] resident B k-blocks
+  uint8_t* sA = sB + kResKB * R::B_BYTES;         // [A_STAGES] A ring
+  uint8_t* sStg = sA + R::A_STAGES * R::A_BYTES;  // [4 warps][2][32 rows][128 B]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + R::STG_BYTES);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + R::NBARS);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int* s_total = reinterpret_cast<int*>(s_tmem + 2);
+  int* s_koff = reinterpret_cast<int*>(s_tmem + 4);  // [groups + 1]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t afull0 = smem_u32(bars), aempty0 = afull0 + 8 * 8;
+  const uint32_t bfull0 = aempty0 + 8 * 8, bempty0 = bfull0 + 8 * kResKB;
+  const uint32_t tfull0 = bempty0 + 8 * kResKB, tempty0 = tfull0 + 16, drain_bar = tempty0 + 16;
+  const int G = p.groups;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < R::A_STAGES; ++s) {
+      mbar_init(afull0 + 8 * s, 1);
+      mbar_init(aempty0 + 8 * s, 1);
+    }
+    for (int kb = 0; kb < kResKB; ++kb) {
+      mbar_init(bfull0 + 8 * kb, 1);
+      mbar_init(bempty0 + 8 * kb, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 4);
+    }
+    mbar_init(drain_bar, 1);
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(s_tmem), 2 * BN);
+  pdl_wait();  // everything above is local setup; below, the first reads of the inputs
+  pdl_trigger();
+  const uint64_t wlimit = wait_limit_ns(p.status);
+  const int mt = (p.c1 + BM - 1) / BM;  // m tiles a group
+  const int n_mc = (mt + kRunM - 1) / kRunM;  // m-tile chunks a group
+  if (warp == 2) {
+    // the groups' K offsets: multiples of 64, in order, each range at most kResKB k-blocks
+    bool bad = false;
+    for (int g = lane; g <= G; g += 32) {
+      const int k = p.koffs[g];
+      s_koff[g] = k;
+      if (k < 0 || k > p.K || k % BK) bad = true;
+      if (g > 0) {
+        const int kp = p.koffs[g - 1];
+        if (k < kp || k - kp > kResKB * BK) bad = true;
+      }
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      *s_total = bad ? 0 : G * n_mc * p.n_tiles;  // runs
+      if (bad) atomicOr(p.status, kStatusDeviceData);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int n_runs = *s_total;
+  // run r -> group g, N tile nt, m-tiles mb .. me - 1 of the group
+  auto run_of = [&](int r, int& g, int& nt, int& mb, int& me) {
+    const int per_g = n_mc * p.n_tiles;
+    g = r / per_g;
+    const int local = r - g * per_g;
+    const int mc = local / p.n_tiles;
+    nt = local - mc * p.n_tiles;
+    mb = mc * kRunM;
+    me = min(mt, mb + kRunM);
+  };
+
+  // in flight, for the drain after an abort: the producer's last load into each A stage and
+  // each B slot (and the phase it completes); whether the MMA thread issued MMAs
+  uint32_t a_issued = 0, a_par = 0, b_issued = 0, b_par = 0;
+  bool mma_any = false, mma_drained = false;
+  if (warp == 0) {
+    // ---------------- TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    int uses[kResKB] = {};  // runs that have loaded slot kb
+    bool ok = true;
+    for (int r = blockIdx.x; r < n_runs && ok; r += gridDim.x) {
+      int g, nt, mb, me;
+      run_of(r, g, nt, mb, me);
+      const int k0 = s_koff[g], nkb = (s_koff[g + 1] - k0) / BK;
+      const int abase = p.aoffs ? __ldg(p.aoffs + g) : k0;  // K rows of A
+      const int bbase = p.boffs ? __ldg(p.boffs + g) : k0;  // K rows of B
+      {  // the run's B k-blocks into the slots
+#pragma unroll
+        for (int kb = 0; kb < kResKB; ++kb) {
+          if (kb >= nkb || !ok) break;
+          if (uses[kb] > 0)  // the slot's last run has finished its MMAs
+            ok = __all_sync(0xffffffffu, wait_bounded(bempty0 + 8 * kb, uint32_t(uses[kb] - 1) & 1u,
+                                                      s_abort, p.status, wlimit));
+          if (!ok) break;
+          if (lane == 0) {
+            const uint32_t fb = bfull0 + 8 * kb;
+            const uint32_t dB = smem_u32(sB + kb * R::B_BYTES);
+            mbar_expect_tx(fb, R::B_BYTES);
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(dB + i * 8192, &tmB, nt * BN + 64 * i, bbase + kb * BK, fb);
+          }
+          __syncwarp();
+          b_issued |= 1u << kb;
+          b_par = (b_par & ~(1u << kb)) | ((uint32_t(uses[kb]) & 1u) << kb);
+          ++uses[kb];
+        }
+      }
+      for (int mi = mb; mi < me && ok; ++mi) {
+        const int acol = mi * BM;  // A's columns: the tile's output rows within the group
+        for (int kb = 0; kb < nkb && ok; ++kb) {
+          ok = __all_sync(0xffffffffu, wait_bounded(aempty0 + 8 * stage, phase ^ 1u, s_abort, p.status, wlimit));
+          if (!ok) break;
+          if (lane == 0) {
+            const uint32_t fb = afull0 + 8 * stage;
+            const uint32_t dA = smem_u32(sA + stage * R::A_BYTES);
+            mbar_expect_tx(fb, R::A_BYTES);
+#pragma unroll
+            for (int i = 0; i < BM / 64; ++i)
+              tma_load_2d(dA + i * 8192, &tmA, acol + 64 * i, abase + kb * BK, fb);
+          }
+          __syncwarp();
+          a_issued |= 1u << stage;
+          a_par = (a_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == R::A_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    constexpr uint32_t kIdesc = idesc_bf16(BM, BN) | (3u << 15);  // MN-major A and B
+    int stage = 0;
+    uint32_t phase = 0;
+    int uses[kResKB] = {};  // runs whose B this thread has waited for, per slot
+    bool ok = true;
+    int i = 0;
+    for (int r = blockIdx.x; r < n_runs && ok; r += gridDim.x) {
+      int g, nt, mb, me;
+      run_of(r, g, nt, mb, me);
+      const int nkb = (s_koff[g + 1] - s_koff[g]) / BK;
+      for (int mi = mb; mi < me && ok; ++mi, ++i) {
+        const bool first = mi == mb;     // the run's first tile: wait for its B
+        const bool last = mi == me - 1;  // the run's last tile: release its B slots after the MMAs
+        const int acc = i & 1;
+        const uint32_t use = uint32_t(i >> 1) & 1u;
+        ok = __all_sync(0xffffffffu, wait_bounded(tempty0 + 8 * acc, use ^ 1u, s_abort, p.status, wlimit));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + uint32_t(acc * BN);
+#pragma unroll
+        for (int kb = 0; kb < kResKB; ++kb) {
+          if (kb >= nkb) break;
+          if (first) {
+            ok = __all_sync(0xffffffffu, wait_bounded(bfull0 + 8 * kb, uint32_t(uses[kb]) & 1u, s_abort,
+                                                      p.status, wlimit));
+            if (!ok) break;
+            ++uses[kb];
+          }
+          ok = __all_sync(0xffffffffu, wait_bounded(afull0 + 8 * stage, phase, s_abort, p.status, wlimit));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a0 = smem_u32(sA + stage * R::A_BYTES);
+            const uint32_t b0 = smem_u32(sB + kb * R::B_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_bf16(d, mn_sw128_desc(a0 + kk * 2048), mn_sw128_desc(b0 + kk * 2048), kIdesc,
+                       (kb | kk) != 0 ? 1u : 0u);
+            mma_commit(aempty0 + 8 * stage);
+            if (last) mma_commit(bempty0 + 8 * kb);
+          }
+          __syncwarp();
+          mma_any = true;
+          if (++stage == R::A_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok && lane == 0) mma_commit(tfull0 + 8 * acc);
+        __syncwarp();
+      }
+    }
+    if (!ok && mma_any && lane == 0) {  // every MMA issued must finish before TMEM is freed
+      mma_commit(drain_bar);
+      wait_drain(drain_bar, 0u);
+    }
+    mma_drained = !ok && mma_any;
+    __syncwarp();
+  } else {
+    // ---------------- epilogue warps 2 .. 5: TMEM lanes 32q .. 32q + 31
+    const int q = warp & 3;
+    int stg_buf = 0;
+    int i = 0;
+    bool ok = true;
+    for (int r = blockIdx.x; r < n_runs && ok; r += gridDim.x) {
+      int g, nt, mb, me;
+      run_of(r, g, nt, mb, me);
+      for (int mi = mb; mi < me; ++mi, ++i) {
+        const int m0 = g * p.c1 + mi * BM;
+        const int rows = min(BM, p.c1 - mi * BM);
+        const int acc = i & 1;
+        const uint32_t use = uint32_t(i >> 1) & 1u;
+        ok = __all_sync(0xffffffffu, wait_bounded(tfull0 + 8 * acc, use, s_abort, p.status, wlimit));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
+        const bool zero = s_koff[g + 1] == s_koff[g];  // no MMA ran for this tile
+        const int r0 = q * 32;
+        const int nvr = rows - r0 < 0 ? 0 : (rows - r0 > 32 ? 32 : rows - r0);
+        epilogue_f32_tma<BN, 32, 2>(p, &tmO, &tmO2, tbase, int64_t(m0) + r0, nvr, nt, zero,
+                                    sStg + q * 2 * 4096, lane, stg_buf);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_relaxed(tempty0 + 8 * acc);
+      }
+    }
+    if (lane == 0) bulk_wait_all();  // every TMA store has read its staging buffer
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*s_abort) {
+    // whichever role gave up, every load issued lands and every MMA issued finishes before
+    // shared and tensor memory are released
+    if (warp == 0 && lane == 0) {
+      for (int s = 0; s < R::A_STAGES; ++s)
+        if ((a_issued >> s) & 1u) wait_drain(afull0 + 8 * s, (a_par >> s) & 1u);
+      for (int kb = 0; kb < kResKB; ++kb)
+        if ((b_issued >> kb) & 1u) wait_drain(bfull0 + 8 * kb, (b_par >> kb) & 1u);
+    }
+    if (warp == 1 && lane == 0 && mma_any && !mma_drained) {
+      mma_commit(drain_bar);
+      wait_drain(drain_bar, 0u);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 2 * BN);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1195,6 +1491,63 @@ int run_gemm(const GemmDesc& d, cudaStream_t st) {
   return MOE_OK;
 }
 
+// wgrad_resident_kernel's launch: the K-ragged MN-major operands as run_gemm maps them,
+// fp32 outputs in 32 x 32 boxes, one CTA per SM (at most one per tile).
+int run_wgrad_resident(const GemmDesc& d, cudaStream_t st) {
+  using R = ResCfg;
+  if (!d.koffs || d.c1 < 1 || d.groups < 1 || d.groups > kMaxGroups || d.b_tiled)
+    return MOE_ERR_INVALID_ARG;
+  if (d.c1 % 64 || d.N % 8 || d.a_krows < 1 || d.b_krows < 1) return MOE_ERR_UNSUPPORTED;
+  if (d.epi != EPI_F32_BIAS || d.ldo != d.N) return MOE_ERR_UNSUPPORTED;
+  CUtensorMap ta, tb, to, to2;
+  int rc;
+  if ((rc = make_map(&ta, d.A, d.a_krows, d.c1, 64)) != MOE_OK) return rc;
+  if ((rc = make_map(&tb, d.B, d.b_krows, d.N, 64)) != MOE_OK) return rc;
+  memset(&to, 0, sizeof(to));
+  memset(&to2, 0, sizeof(to2));
+  const int64_t out_rows = int64_t(d.groups) * d.c1 / (d.out2 ? 2 : 1);
+  if ((rc = make_map_f32_out(&to, d.out, out_rows, d.N, 32)) != MOE_OK) return rc;
+  if (d.out2 && (rc = make_map_f32_out(&to2, d.out2, out_rows, d.N, 32)) != MOE_OK) return rc;
+  KParams p;
+  memset(&p, 0, sizeof(p));
+  p.groups = d.groups;
+  p.rows_cap = int64_t(d.groups) * d.c1;
+  p.N = d.N;
+  p.K = d.K;
+  p.n_tiles = (d.N + R::BN - 1) / R::BN;
+  p.out = d.out;
+  p.ldo = d.ldo;
+  p.n_valid = d.n_valid;
+  p.status = d.status;
+  p.koffs = d.koffs;
+  p.c1 = d.c1;
+  p.out2 = d.out2;
+  p.aoffs = d.aoffs;
+  p.boffs = d.boffs;
+  MOE_CUDA_CHECK(cudaFuncSetAttribute(wgrad_resident_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, R::SMEM));
+  const int64_t runs =
+      int64_t(d.groups) * (((d.c1 + BM - 1) / BM + kRunM - 1) / kRunM) * p.n_tiles;
+  if (runs * kRunM > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  int64_t units = num_sms();
+  if (units > runs) units = runs;
+  if (units < 1) units = 1;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(unsigned(units));
+  lc.blockDim = dim3(192);
+  lc.dynamicSmemBytes = R::SMEM;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (pdl_enabled()) {  // see launch_kernel
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+  }
+  MOE_CUDA_CHECK(cudaLaunchKernelEx(&lc, wgrad_resident_kernel, ta, tb, to, to2, p));
+  return MOE_OK;
+}
+
 }  // namespace
 
 int make_tma_map_rows(CUtensorMap* m, const void* base, int64_t rows, int K, int box_rows) {
@@ -1218,6 +1571,10 @@ int launch_gemm_bf16(const GemmDesc& d, cudaStream_t st) {
     // 3.53 ms with pairs, preset 2 1.75 -> 2.03 ms)
     const bool pair = d.N > 128 && d.c1 >= 256 && int64_t(d.K) >= 768 * int64_t(d.groups);
     if (d.mn) {  // MN-major operands (row-major activations read in place)
+      // short K ranges known to the caller and at least two m-tiles a group: the tiles of a
+      // (group, N tile) share their B, which then stays resident (wgrad_resident_kernel)
+      if (!pair && d.N > 128 && d.k_max > 0 && d.k_max <= kResKB * BK && d.c1 >= 2 * BM)
+        return run_wgrad_resident(d, st);
       if (d.N > 128) return pair ? run_gemm<256, EPI_F32_BIAS, true, true, true>(d, st)
                                  : run_gemm<256, EPI_F32_BIAS, false, true, true>(d, st);
       if (d.N > 64) return run_gemm<128, EPI_F32_BIAS, false, true, true>(d, st);

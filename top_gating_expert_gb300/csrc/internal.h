@@ -234,6 +234,9 @@ struct GemmDesc {
   int64_t a_krows = 0, b_krows = 0;
   const int32_t* aoffs = nullptr;
   const int32_t* boffs = nullptr;
+  // K-ragged mode: a bound the caller knows on every group's K range (0: none known). With
+  // at most 256 a group, MN-major 256-wide outputs run the resident-B kernel
+  int k_max = 0;
 };
 int launch_gemm_bf16(const GemmDesc& d, cudaStream_t st);
 // 2-D tensor map over a row-major bf16 [rows, K] matrix, boxes of 64 columns x box_rows rows,
