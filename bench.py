@@ -365,7 +365,7 @@ def backward_summary(cfg, R, S, world, f_ms, b_ms, P) -> dict:
     # algorithmic bytes: every input read once (dy, x, the logits, W_g, the transposed weight
     # packs, the packed W_in again for the SwiGLU recompute, the stored h) and every output
     # written once (the fp32 weight gradients, dx)
-    b2 = 2
+    b2 = 2 if cfg["dtype"] == "bf16" else 4
     in_bytes = (b2 * (2 * S * M + E * M + E * (F + H) * M + (E * F * M if f1 == 2 else 0)
                       + R * H) + 4 * S * E)
     if Hc:
@@ -373,6 +373,16 @@ def backward_summary(cfg, R, S, world, f_ms, b_ms, P) -> dict:
     bwd_bytes = in_bytes + grad_bytes + b2 * S * M
     t_bytes = bwd_bytes / (P["hbm"] * 1e9) * 1e3
     t_flops = flops / (P["tc_sustained"] * 1e12) * 1e3
+    if cfg["dtype"] != "bf16":  # the fp32 path: plain FMA on a tiny layer, no roofline
+        return {
+            "what": "moe_layer_backward (fp32, plain FMA): gradients of sum(dy*y) + 0.01 aux + "
+                    "0.001 z w.r.t. x, W_g, every expert weight; forward = moe_layer_forward "
+                    "keeping its logits; L2 flushed before each step",
+            "ms_per_step": round(b_ms, 5), "forward_ms_per_step": round(f_ms, 5),
+            "train_tokens_per_s": round(S * world / ((f_ms + b_ms) * 1e-3), 1),
+            "algorithmic_flops": flops, "algorithmic_bytes": int(bwd_bytes),
+            "bound": "latency", "roofline_frac": None,
+        }
     return {
         "what": "moe_layer_backward: gradients of sum(dy*y) + 0.01 aux + 0.001 z w.r.t. x, "
                 "W_g, every expert weight (fp32), routing fixed; forward = moe_layer_forward "
@@ -567,7 +577,7 @@ def run_preset(args, n, cfg, rank, world, dev, flush, barrier, *, headline: bool
     # ---- the backward pass (a training step): a layer that keeps its logits, forward then
     # moe_layer_backward on the same inputs, L2 flushed before each step
     bwd = None
-    if cfg["dtype"] == "bf16" and not args.no_backward:
+    if not args.no_backward:
         log(f"preset {n}: backward")
         del x_perm, h_perm, y_perm
         tl = moe.MoeLayer(cfg, inp.host, device=dev)

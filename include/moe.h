@@ -345,12 +345,12 @@ int moe_layer_forward(const moe_config_t* cfg, const void* x, const void* W_g, c
 /* ---------------------------------------------------------------- the backward pass */
 
 /*
- * Transposed weights for the backward's data-gradient GEMMs, packed tile-major like the
- * forward's (element counts as moe_packed_sizes' w_in / w_out):
+ * Transposed weights for the backward's data-gradient GEMMs (element counts as
+ * moe_packed_sizes' w_in / w_out):
  *   Wt_out_packed  logical [E, H, M]: W_out[e] transposed (gradient through GEMM 2);
  *   Wt_in_packed   logical [E, M, H] (ReLU) or [E, M, 2H] (SwiGLU, the K order of the forward's
  *                  interleaved pack): W_in[e] (and W_up[e]) transposed.
- * bf16 only.
+ * bf16: packed tile-major like the forward's; fp32: plain row-major in the logical shape.
  */
 int moe_pack_weights_backward(const moe_config_t* cfg, const void* W_in, const void* W_up,
                               const void* W_out, void* Wt_in_packed, void* Wt_out_packed,
@@ -382,7 +382,7 @@ typedef struct {
  * reaches the router only through the expert scores, its counts being constants; §2:
  * z-loss) with the routing decisions held fixed. A dropped assignment gives its gate no
  * gradient. Every gate normalisation (MOE_GATE_*); uniform assignment (ids that do not come
- * from the logits) gives MOE_ERR_UNSUPPORTED; bf16 only.
+ * from the logits) gives MOE_ERR_UNSUPPORTED. bf16 and fp32 layers.
  * Inputs from the forward: logits (the forward's logits_out, [S, E]), r (its routing
  * outputs) and fwd_ws (the MOE_WS_LAYER workspace of that moe_layer_forward call,
  * unchanged since: it holds x_perm, h and the shared experts' h). residual: 1 if the
@@ -394,6 +394,9 @@ typedef struct {
  * gradient, the SwiGLU derivative, GEMM 1's data gradient (tcgen05); the weights'
  * gradients as K-ragged tcgen05 GEMMs over per-expert 64-padded transposed rows; the
  * router's gradient (dlogits, then dx, dW_g, dbias); dx summed in fp32 and rounded once.
+ * fp32 layers (the small-layer path) take the same steps on plain FMA, one thread an
+ * output element, every sum (over d_model, d_ff, an expert's rows, the experts or the
+ * tokens) in a fixed order.
  */
 int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, const void* W_g,
                        const void* W_in_packed, const void* Wt_in_packed, const void* Wt_out_packed,

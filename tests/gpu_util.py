@@ -122,3 +122,31 @@ def near_tie_tokens(logits: np.ndarray, k: int, gap: float = 1e-6) -> np.ndarray
     """Tokens whose top-(k+1) logits have a consecutive gap below `gap`."""
     s = -np.sort(-np.asarray(logits, np.float64), axis=1)[:, : k + 1]
     return np.nonzero((np.diff(-s, axis=1) < gap).any(axis=1))[0]
+
+
+def relu_band(x_rows, W_in):
+    """(row, unit) pairs whose fp64 pre-activation lies within the fp32-accumulation bound
+    of zero, and that bound (module docstring)."""
+    xr, W = np.asarray(x_rows, np.float64), np.asarray(W_in, np.float64)
+    K = xr.shape[1]
+    a = xr @ W.T
+    bound = 2.0 * K * 2.0 ** -24 * (np.abs(xr) @ np.abs(W).T)
+    return np.abs(a) <= bound, bound
+
+
+def check_close(gpu, ref, rtol, dev, what):
+    """R14 (|g - r| <= rtol (|r| + rms(r row))) plus the widening `dev` (0 where no ambiguous
+    mask decision reaches the element). Returns how many elements the widening touched."""
+    g = np.asarray(gpu, np.float64)
+    r = np.asarray(ref, np.float64)
+    r2 = r.reshape(-1, r.shape[-1])
+    g2 = g.reshape(r2.shape)
+    d2 = np.broadcast_to(np.asarray(dev, np.float64), r.shape).reshape(r2.shape)
+    rms = np.sqrt(np.mean(r2 * r2, axis=1, keepdims=True))
+    err = np.abs(g2 - r2)
+    lim = rtol * (np.abs(r2) + rms)
+    bad = err > lim + d2
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements outside tolerance "
+                           f"(first at {np.argwhere(bad)[0].tolist()}, err "
+                           f"{err[bad][0]:.3e}, limit {lim[bad][0]:.3e} + {d2[bad][0]:.3e})")
+    return int(np.count_nonzero(d2 > 0))

@@ -174,8 +174,11 @@ def test_backward_host_checks(native_lib):
     assert L.moe_layer_backward(ctypes.byref(c), *args(), *tail(fwd_bytes=16)) == -3
     g0 = N.MoeGrads(**{f: (1 << 20) for f in N.GRAD_FIELDS}); g0.dW_in = None
     assert L.moe_layer_backward(ctypes.byref(c), *args(), *tail(grads=g0)) == -1
+    # fp32 layers have a backward too (plain FMA); its checks come before any launch as well
     c32 = moe.make_config(PRESETS[1])
-    assert L.moe_layer_backward(ctypes.byref(c32), *args(), *tail()) == -2   # bf16 only
+    b32 = moe.workspace_bytes(c32, N.MOE_WS_BACKWARD)
+    assert L.moe_layer_backward(ctypes.byref(c32), *args(), *tail(ws_bytes=b32 - 256)) == -3
+    assert L.moe_layer_backward(ctypes.byref(c32), *args(dy=None), *tail(ws_bytes=b32)) == -1
     cu = moe.make_config(preset(2, uniform_assignment=1, random_routing=0))
     assert L.moe_layer_backward(ctypes.byref(cu), *args(), *tail()) == -2    # forward-only ids
-    assert L.moe_pack_weights_backward(ctypes.byref(c32), fake, fake, fake, fake, fake, None) == -2
+    assert L.moe_pack_weights_backward(ctypes.byref(c32), None, fake, fake, fake, fake, None) == -1

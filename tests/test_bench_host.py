@@ -128,3 +128,17 @@ def test_traffic_lookup_is_null_once_the_source_changes(tmp_path, monkeypatch):
     assert bench.traffic_for("expert_down", 2) is None  # taken on another source
     assert bench.traffic_for("expert_up", 3) is None    # no row for that preset
     assert bench.traffic_for("no_such_kernel", 2) is None
+
+
+def test_backward_summary_bounds():
+    """bf16 backwards take the larger of their byte and flop times as their roofline; the
+    fp32 path's (plain FMA on a tiny layer) reports its latency and no roofline fraction."""
+    from top_gating_expert_gb300.inputs import PRESETS
+    P = {"hbm": 6000.0, "tc": 2000.0, "tc_sustained": 1800.0, "source": "test"}
+    b2 = bench.backward_summary(PRESETS[2], 27000, 16384, 1, 0.45, 1.4, P)
+    assert b2["bound"] == "hbm" and 0 < b2["roofline_frac"] < 1
+    b3 = bench.backward_summary(PRESETS[3], 16384, 8192, 1, 3.2, 9.9, P)
+    assert b3["bound"] == "tensor" and 0 < b3["roofline_frac"] < 1
+    b1 = bench.backward_summary(PRESETS[1], 512, 256, 1, 0.05, 0.1, P)
+    assert b1["bound"] == "latency" and b1["roofline_frac"] is None
+    assert b1["train_tokens_per_s"] == round(256 / 0.15e-3, 1)

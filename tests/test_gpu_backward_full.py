@@ -29,40 +29,12 @@ import torch
 
 from oracle import moe_backward as B
 from oracle import moe_oracle as O
-from gpu_util import RTOL, oracle_cfg, to_np
+from gpu_util import RTOL, check_close, oracle_cfg, relu_band, to_np
 from top_gating_expert_gb300 import moe
 from top_gating_expert_gb300.inputs import PRESETS, make_inputs
 
 pytestmark = pytest.mark.gpu
 AUX, Z = 0.7, 0.3
-
-
-def relu_band(x_rows, W_in):
-    """(row, unit) pairs whose fp64 pre-activation lies within the fp32-accumulation bound
-    of zero, and that bound (module docstring)."""
-    xr, W = np.asarray(x_rows, np.float64), np.asarray(W_in, np.float64)
-    K = xr.shape[1]
-    a = xr @ W.T
-    bound = 2.0 * K * 2.0 ** -24 * (np.abs(xr) @ np.abs(W).T)
-    return np.abs(a) <= bound, bound
-
-
-def check_close(gpu, ref, rtol, dev, what):
-    """R14 (|g - r| <= rtol (|r| + rms(r row))) plus the widening `dev` (0 where no ambiguous
-    mask decision reaches the element). Returns how many elements the widening touched."""
-    g = np.asarray(gpu, np.float64)
-    r = np.asarray(ref, np.float64)
-    r2 = r.reshape(-1, r.shape[-1])
-    g2 = g.reshape(r2.shape)
-    d2 = np.broadcast_to(np.asarray(dev, np.float64), r.shape).reshape(r2.shape)
-    rms = np.sqrt(np.mean(r2 * r2, axis=1, keepdims=True))
-    err = np.abs(g2 - r2)
-    lim = rtol * (np.abs(r2) + rms)
-    bad = err > lim + d2
-    assert not bad.any(), (f"{what}: {int(bad.sum())} elements outside tolerance "
-                           f"(first at {np.argwhere(bad)[0].tolist()}, err "
-                           f"{err[bad][0]:.3e}, limit {lim[bad][0]:.3e} + {d2[bad][0]:.3e})")
-    return int(np.count_nonzero(d2 > 0))
 
 
 @pytest.mark.parametrize("n", [2, 4, 5])

@@ -446,14 +446,14 @@ int moe_pack_weights_backward(const moe_config_t* cfg, const void* W_in, const v
   Prep p;
   int rc = prepare(cfg, &p);
   if (rc != MOE_OK) return rc;
-  if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   const bool sw = cfg->act == MOE_ACT_SWIGLU;
   if (!W_in || !W_out || !Wt_in_packed || !Wt_out_packed || (sw && !W_up)) return MOE_ERR_INVALID_ARG;
-  rc = launch_pack_transposed(0, 0, cfg->E, cfg->H, cfg->M, cfg->M, cfg->H, 1, W_out, nullptr,
-                              Wt_out_packed, stream);
+  // fp32: the same transposes, row-major (the plain-FMA kernels read them a row a thread)
+  auto pack = cfg->dtype == MOE_BF16 ? launch_pack_transposed : launch_pack_transposed_f32;
+  rc = pack(0, 0, cfg->E, cfg->H, cfg->M, cfg->M, cfg->H, 1, W_out, nullptr, Wt_out_packed, stream);
   if (rc != MOE_OK) return rc;
-  return launch_pack_transposed(1, sw, cfg->E, cfg->M, sw ? 2 * cfg->H : cfg->H, cfg->M, cfg->H, 1,
-                                W_in, W_up, Wt_in_packed, stream);
+  return pack(1, sw, cfg->E, cfg->M, sw ? 2 * cfg->H : cfg->H, cfg->M, cfg->H, 1, W_in, W_up,
+              Wt_in_packed, stream);
 }
 
 int moe_pack_shared_weights_backward(const moe_config_t* cfg, const void* Ws_in, const void* Ws_up,
@@ -462,17 +462,17 @@ int moe_pack_shared_weights_backward(const moe_config_t* cfg, const void* Ws_in,
   Prep p;
   int rc = prepare(cfg, &p);
   if (rc != MOE_OK) return rc;
-  if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (cfg->n_shared < 1) return MOE_ERR_INVALID_ARG;
   const bool sw = cfg->act == MOE_ACT_SWIGLU;
   if (!Ws_in || !Ws_out || !Wst_in_packed || !Wst_out_packed || (sw && !Ws_up))
     return MOE_ERR_INVALID_ARG;
   const int Hc = cfg->n_shared * cfg->H_shared;
-  rc = launch_pack_transposed(0, 0, 1, Hc, cfg->M, cfg->M, cfg->H_shared, cfg->n_shared, Ws_out,
-                              nullptr, Wst_out_packed, stream);
+  auto pack = cfg->dtype == MOE_BF16 ? launch_pack_transposed : launch_pack_transposed_f32;
+  rc = pack(0, 0, 1, Hc, cfg->M, cfg->M, cfg->H_shared, cfg->n_shared, Ws_out, nullptr,
+            Wst_out_packed, stream);
   if (rc != MOE_OK) return rc;
-  return launch_pack_transposed(1, sw, 1, cfg->M, sw ? 2 * Hc : Hc, cfg->M, Hc, 1, Ws_in, Ws_up,
-                                Wst_in_packed, stream);
+  return pack(1, sw, 1, cfg->M, sw ? 2 * Hc : Hc, cfg->M, Hc, 1, Ws_in, Ws_up, Wst_in_packed,
+              stream);
 }
 
 // One expert FFN's backward on (ragged or dense) row segments, the steps moe_layer_backward
@@ -550,6 +550,72 @@ int weight_grad_mn(const void* A, int64_t a_krows, const int32_t* aoffs, int c1,
   return launch_gemm_bf16(d, st);
 }
 
+// moe_layer_backward for fp32 layers: the bf16 path's steps on plain-FMA kernels
+// (backward_f32.cu), with the transposed weights row-major and every sum in a fixed order.
+int layer_backward_f32(const moe_config_t& c, const Prep& p, const void* x, const void* dy,
+                       const void* W_g, const void* W_in_packed, const void* Wt_in_packed,
+                       const void* Wt_out_packed, const void* Ws_in_packed,
+                       const void* Wst_in_packed, const void* Wst_out_packed, const float* logits,
+                       const moe_route_out_t& r, const char* fw, char* w, const WsLayoutBwd& B,
+                       const RouterBwdBufs& rb, int residual, float aux_coef, float z_coef,
+                       const moe_grads_t& grads, unsigned* status, cudaStream_t stream) {
+  const bool sw = c.act == MOE_ACT_SWIGLU;
+  const int64_t R = p.R_max;
+  const int F = sw ? 2 * c.H : c.H;
+  int rc;
+  // routed experts: data gradients over the expert segments
+  if ((rc = launch_dispatch(c, R, dy, r.token_of, r.expert_offsets, w + B.dy_perm, stream)) != MOE_OK)
+    return rc;
+  FfnBwdF32 f;
+  f.x_rows = fw + p.L.x_perm; f.rows_cap = R; f.offsets = r.expert_offsets; f.groups = c.E;
+  f.dense_rows = 0; f.M = c.M; f.Hn = c.H; f.swiglu = sw ? 1 : 0;
+  f.W_in_packed = W_in_packed; f.Wt_in = Wt_in_packed; f.Wt_out = Wt_out_packed;
+  f.dy_rows = w + B.dy_perm; f.w = r.w_perm; f.h = fw + p.L.h_perm; f.dh = w + B.dh;
+  f.dab = w + B.dab; f.gpart = reinterpret_cast<float*>(w + B.gpart); f.n_tiles = B.n_tiles2;
+  f.dx_rows = w + B.dx_perm;
+  if ((rc = ffn_backward_data_f32(f, stream)) != MOE_OK) return rc;
+  // routed experts: dW_out = (w dy)^T h, dW_in = da^T x (dW_up = db^T x), each expert's rows
+  if ((rc = weight_grad_f32(w + B.dy_perm, c.M, r.w_perm, 0, fw + p.L.h_perm, c.H,
+                            r.expert_offsets, c.E, 0, c.M, c.H, grads.dW_out, stream)) != MOE_OK)
+    return rc;
+  if ((rc = weight_grad_f32(w + B.dab, F, nullptr, sw ? 1 : 0, fw + p.L.x_perm, c.M,
+                            r.expert_offsets, c.E, 0, c.H, c.M, grads.dW_in, stream)) != MOE_OK)
+    return rc;
+  if (sw && (rc = weight_grad_f32(w + B.dab, F, nullptr, 2, fw + p.L.x_perm, c.M, r.expert_offsets,
+                                  c.E, 0, c.H, c.M, grads.dW_up, stream)) != MOE_OK)
+    return rc;
+  // the router: dlogits from the gates' gradients, aux and z; then dx, dW_g, dbias
+  if ((rc = launch_router_backward(c, logits, r, reinterpret_cast<const float*>(w + B.gpart),
+                                   B.n_tiles2, aux_coef, z_coef, rb, x, W_g, grads.dW_g,
+                                   grads.dbias, status, stream)) != MOE_OK)
+    return rc;
+  // shared experts: one dense segment of all S tokens, weight 1
+  void* dxs = nullptr;
+  if (c.n_shared > 0) {
+    const int Hc = c.n_shared * c.H_shared, Fs = sw ? 2 * Hc : Hc;
+    FfnBwdF32 s;
+    s.x_rows = x; s.rows_cap = c.S; s.offsets = nullptr; s.groups = 1; s.dense_rows = c.S;
+    s.M = c.M; s.Hn = Hc; s.swiglu = sw ? 1 : 0;
+    s.W_in_packed = Ws_in_packed; s.Wt_in = Wst_in_packed; s.Wt_out = Wst_out_packed;
+    s.dy_rows = dy; s.w = nullptr; s.h = fw + p.L.h_shared; s.dh = w + B.dhs; s.dab = w + B.dabs;
+    s.gpart = nullptr; s.n_tiles = 1; s.dx_rows = w + B.dxs;
+    if ((rc = ffn_backward_data_f32(s, stream)) != MOE_OK) return rc;
+    if ((rc = weight_grad_f32(dy, c.M, nullptr, 0, fw + p.L.h_shared, Hc, nullptr, 1, c.S, c.M,
+                              Hc, grads.dWs_out, stream)) != MOE_OK)
+      return rc;
+    if ((rc = weight_grad_f32(w + B.dabs, Fs, nullptr, sw ? 1 : 0, x, c.M, nullptr, 1, c.S, Hc,
+                              c.M, grads.dWs_in, stream)) != MOE_OK)
+      return rc;
+    if (sw && (rc = weight_grad_f32(w + B.dabs, Fs, nullptr, 2, x, c.M, nullptr, 1, c.S, Hc, c.M,
+                                    grads.dWs_up, stream)) != MOE_OK)
+      return rc;
+    dxs = w + B.dxs;
+  }
+  // dx = sum over kept choices of the rows' gradients (+ shared) (+ dy) + the router's
+  return launch_combine(c, w + B.dx_perm, r.row, dxs, residual ? dy : nullptr, grads.dx, R, stream,
+                        rb.dx_r);
+}
+
 int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, const void* W_g,
                        const void* W_in_packed, const void* Wt_in_packed, const void* Wt_out_packed,
                        const void* Ws_in_packed, const void* Wst_in_packed,
@@ -561,7 +627,6 @@ int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, c
   int rc = prepare(cfg, &p);
   if (rc != MOE_OK) return rc;
   const moe_config_t& c = *cfg;
-  if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (c.uniform_assignment) return MOE_ERR_UNSUPPORTED;
   if (c.E > 256) return MOE_ERR_UNSUPPORTED;
   const bool sw = c.act == MOE_ACT_SWIGLU;
@@ -584,6 +649,20 @@ int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, c
   unsigned* status = reinterpret_cast<unsigned*>(w + B.status);
   const int64_t R = p.R_max;
   const int F = sw ? 2 * c.H : c.H;
+  // the router's buffers (its GEMMs' operands on the bf16 path)
+  int32_t* poff_s = reinterpret_cast<int32_t*>(w + B.poff_s);
+  RouterBwdBufs rb;
+  rb.dlogits = reinterpret_cast<float*>(w + B.dlogits);
+  rb.dlb = w + B.dlb; rb.wgT = w + B.wgT;
+  rb.dx_r = reinterpret_cast<float*>(w + B.dx_r);
+  rb.koff_e = reinterpret_cast<int32_t*>(w + B.koff_e); rb.koff_s = poff_s; rb.Sp = B.Sp;
+  rb.koff_split = reinterpret_cast<int32_t*>(w + B.koff_split);
+  rb.dwg_part = reinterpret_cast<float*>(w + B.dwg_part);
+  rb.max_split = WsLayoutBwd::kMaxSplit;
+  if (c.dtype == MOE_F32)
+    return layer_backward_f32(c, p, x, dy, W_g, W_in_packed, Wt_in_packed, Wt_out_packed,
+                              Ws_in_packed, Wst_in_packed, Wst_out_packed, logits, *r, fw, w, B,
+                              rb, residual, aux_coef, z_coef, *grads, status, stream);
 
   // routed experts: data gradients (tcgen05 GEMMs over the expert segments)
   if ((rc = launch_dispatch(c, R, dy, r->token_of, r->expert_offsets, w + B.dy_perm, stream)) != MOE_OK)
@@ -622,17 +701,8 @@ int moe_layer_backward(const moe_config_t* cfg, const void* x, const void* dy, c
     return rc;
   // K = all S tokens (padded to 64) for the router's dW_g and the shared experts: the tensors
   // end at row S, so the padding reads as zeros
-  int32_t* poff_s = reinterpret_cast<int32_t*>(w + B.poff_s);
   if ((rc = launch_pad_offsets(nullptr, 1, c.S, poff_s, stream)) != MOE_OK) return rc;
   // the router: dlogits from the gates' gradients, aux and z; then dx, dW_g (tcgen05), dbias
-  RouterBwdBufs rb;
-  rb.dlogits = reinterpret_cast<float*>(w + B.dlogits);
-  rb.dlb = w + B.dlb; rb.wgT = w + B.wgT;
-  rb.dx_r = reinterpret_cast<float*>(w + B.dx_r);
-  rb.koff_e = reinterpret_cast<int32_t*>(w + B.koff_e); rb.koff_s = poff_s; rb.Sp = B.Sp;
-  rb.koff_split = reinterpret_cast<int32_t*>(w + B.koff_split);
-  rb.dwg_part = reinterpret_cast<float*>(w + B.dwg_part);
-  rb.max_split = WsLayoutBwd::kMaxSplit;
   if ((rc = launch_router_backward(c, logits, *r, reinterpret_cast<const float*>(w + B.gpart),
                                    B.n_tiles2, aux_coef, z_coef, rb, x, W_g, grads->dW_g,
                                    grads->dbias, status, stream)) != MOE_OK)

@@ -464,6 +464,19 @@ int launch_pack_transposed(int mode, int swiglu, int groups, int N, int K, int M
   return MOE_OK;
 }
 
+// dbias = the column sums of dlogits, in a fixed order (the partials reuse the dW_g partial
+// buffer); nothing without dbias
+int router_dbias(const moe_config_t& c, const RouterBwdBufs& b, float* dbias, cudaStream_t st) {
+  if (!dbias) return MOE_OK;
+  const int nch = (c.S + 255) / 256;
+  int rc;
+  if ((rc = launch_kernel(colsum_partial_kernel, dim3(unsigned(nch)), dim3(256), 0, st,
+                          static_cast<const float*>(b.dlogits), c.S, c.E, b.dwg_part)) != MOE_OK)
+    return rc;
+  return launch_kernel(sum_partials_kernel, dim3(unsigned((c.E + 255) / 256)), dim3(256), 0, st,
+                       static_cast<const float*>(b.dwg_part), nch, int64_t(c.E), int64_t(c.E), dbias);
+}
+
 int launch_router_backward(const moe_config_t& c, const float* logits, const moe_route_out_t& r,
                            const float* gpart, int n_tiles, float aux_coef, float z_coef,
                            const RouterBwdBufs& b, const void* x, const void* W_g, float* dW_g,
@@ -481,6 +494,10 @@ int launch_router_backward(const moe_config_t& c, const float* logits, const moe
                        gpart, n_tiles, r.counts_routed, c.S, c.G, c.E, c.k, c.gate_norm, c.gate_p, aux_coef,
                        z_coef, b.dlogits, static_cast<__nv_bfloat16*>(b.dlb), Ep);
   if (rc != MOE_OK) return rc;
+  if (c.dtype == MOE_F32) {  // the fp32 path: dx_r and dW_g on plain FMA (backward_f32.cu)
+    if ((rc = router_grads_f32(c, b.dlogits, x, W_g, b.dx_r, dW_g, st)) != MOE_OK) return rc;
+    return router_dbias(c, b, dbias, st);
+  }
   // K ranges of the two router GEMMs: [0, Ep) and [0, Sp)
   if ((rc = launch_pad_offsets(nullptr, 1, c.E, b.koff_e, st)) != MOE_OK) return rc;
   if ((rc = launch_pad_offsets(nullptr, 1, c.S, b.koff_s, st)) != MOE_OK) return rc;
@@ -524,13 +541,7 @@ int launch_router_backward(const moe_config_t& c, const float* logits, const moe
                           static_cast<const float*>(b.dwg_part), nsplit, len, int64_t(Ep) * c.M,
                           dW_g)) != MOE_OK)
     return rc;
-  if (!dbias) return MOE_OK;
-  const int nch = (c.S + 255) / 256;  // the bias partials reuse the dW_g partial buffer
-  if ((rc = launch_kernel(colsum_partial_kernel, dim3(unsigned(nch)), dim3(256), 0, st,
-                          static_cast<const float*>(b.dlogits), c.S, c.E, b.dwg_part)) != MOE_OK)
-    return rc;
-  return launch_kernel(sum_partials_kernel, dim3(unsigned((c.E + 255) / 256)), dim3(256), 0, st,
-                       static_cast<const float*>(b.dwg_part), nch, int64_t(c.E), int64_t(c.E), dbias);
+  return router_dbias(c, b, dbias, st);
 }
 
 }  // namespace moe

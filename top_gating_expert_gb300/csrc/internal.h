@@ -125,18 +125,19 @@ inline WsLayoutBwd ws_layout_bwd(const moe_config_t& c, int C) {
   B.Sp = (int64_t(c.S) + 63) / 64 * 64;
   const int bn2 = gemm_bn(c.H, EPI_DGRAD2);
   B.n_tiles2 = bn2 > 0 ? 2 * (c.H / bn2) : 1;  // two column halves a tile
+  const size_t eb = c.dtype == MOE_BF16 ? 2 : 4;  // the row buffers' element size
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t at = o; o = align256(o + bytes); return at; };
   B.status = take(256);
-  B.dy_perm = take(size_t(R) * c.M * 2);
-  B.dh = take(sw ? size_t(R) * c.H * 2 : 0);
-  B.dab = take(size_t(R + 64) * F * 2);  // + 64 zeroed rows (read past the last segment)
+  B.dy_perm = take(size_t(R) * c.M * eb);
+  B.dh = take(sw ? size_t(R) * c.H * eb : 0);
+  B.dab = take(size_t(R + 64) * F * eb);  // + 64 zeroed rows (read past the last segment)
   B.gpart = take(size_t(R) * B.n_tiles2 * 4);
-  B.dx_perm = take(size_t(R) * c.M * 2);
+  B.dx_perm = take(size_t(R) * c.M * eb);
   B.poff = take(size_t(c.E + 1) * 4);
   B.poff_s = take(2 * 4);
-  B.wdyP = take(size_t(B.Rp) * c.M * 2);
-  B.xP = take(size_t(B.Rp) * c.M * 2);
+  B.wdyP = take(size_t(B.Rp) * c.M * eb);
+  B.xP = take(size_t(B.Rp) * c.M * eb);
   B.dlogits = take(size_t(c.S) * c.E * 4);
   B.dx_r = take(size_t(c.S) * c.M * 4);
   const size_t Ep = (size_t(c.E) + 63) / 64 * 64;
@@ -148,9 +149,9 @@ inline WsLayoutBwd ws_layout_bwd(const moe_config_t& c, int C) {
   const size_t nch = (size_t(c.S) + 255) / 256;
   const size_t part_floats = size_t(WsLayoutBwd::kMaxSplit) * Ep * c.M;
   B.dwg_part = take((part_floats > nch * c.E ? part_floats : nch * c.E) * 4);
-  B.dhs = take(sw ? size_t(c.S) * Hc * 2 : 0);
-  B.dabs = take(size_t(c.S) * Fs * 2);
-  B.dxs = take(Hc ? size_t(c.S) * c.M * 2 : 0);
+  B.dhs = take(sw ? size_t(c.S) * Hc * eb : 0);
+  B.dabs = take(size_t(c.S) * Fs * eb);
+  B.dxs = take(Hc ? size_t(c.S) * c.M * eb : 0);
   B.bytes = o;
   return B;
 }
@@ -283,6 +284,40 @@ int launch_router_backward(const moe_config_t& c, const float* logits, const moe
                            const float* gpart, int n_tiles, float aux_coef, float z_coef,
                            const RouterBwdBufs& b, const void* x, const void* W_g, float* dW_g,
                            float* dbias, unsigned* status, cudaStream_t st);
+
+// backward_f32.cu: the fp32 path's backward on plain FMA.
+// One expert FFN's data gradients on (ragged or dense) row segments, fp32 row-major: D =
+// dy_rows . W_out into dab, the gate partials (gpart[r][0], the other n_tiles - 1 entries 0),
+// da (ReLU: masked by h > 0) or dh then (da | db) in the forward pack's column order
+// (SwiGLU), dx_rows = (da | db) . W_in.
+struct FfnBwdF32 {
+  const void* x_rows; int64_t rows_cap; const int32_t* offsets; int groups; int dense_rows;
+  int M, Hn, swiglu;
+  const void* W_in_packed;  // the forward's fp32 pack [groups][F][M] (SwiGLU recompute)
+  const void* Wt_in;        // [groups][M][F]
+  const void* Wt_out;       // [groups][Hn][M]
+  const void* dy_rows;      // [rows_cap][M]
+  const float* w;           // per-row gate (null: 1)
+  const void* h;            // the forward's hidden rows [rows_cap][Hn]
+  void* dh;                 // SwiGLU scratch [rows_cap][Hn]
+  void* dab;                // [rows_cap][F]
+  float* gpart; int n_tiles;
+  void* dx_rows;            // [rows_cap][M]
+};
+int ffn_backward_data_f32(const FfnBwdF32& f, cudaStream_t st);
+// out[g][a][b] = sum over group g's rows r, in order, of s_r P[r][pc(a)] Q[r][b]; pmode 0:
+// pc(a) = a; 1 / 2: the SwiGLU gate / up column of unit a in the forward pack's order
+int weight_grad_f32(const void* P, int ldP, const float* scale, int pmode, const void* Q, int ldQ,
+                    const int32_t* offsets, int groups, int dense_rows, int A, int Bn, float* out,
+                    cudaStream_t st);
+// the router's dx_r = dlogits . W_g and dW_g = dlogits^T x
+int router_grads_f32(const moe_config_t& c, const float* dlogits, const void* x, const void* W_g,
+                     float* dx_r, float* dW_g, cudaStream_t st);
+// the backward's transposed weights for fp32, row-major [groups][N][K] (the index rules of
+// launch_pack_transposed)
+int launch_pack_transposed_f32(int mode, int swiglu, int groups, int N, int K, int M, int Hp,
+                               int parts, const void* W, const void* W2, void* dst,
+                               cudaStream_t st);
 
 int num_sms();
 
