@@ -2,8 +2,9 @@
 (oracle/moe_backward.py): every gradient at R14's fp32 tolerance (rtol 1e-5), on small
 layers of each kind the fp32 path runs. The kinds are the tiny GShard preset itself; ReLU
 with groups, capacity, random routing and a router bias; SwiGLU dropless top-3 with a
-residual; shared experts (SwiGLU, and ReLU at ragged sizes, d_model 68 and d_ff 132). The
-oracle routes from the GPU's logits, so both sides hold the same routing decisions.
+residual; SwiGLU with p-norm gates; shared experts (SwiGLU, and ReLU at ragged sizes,
+d_model 68 and d_ff 132). The oracle routes from the GPU's logits, so both sides hold the
+same routing decisions.
 
 The ReLU mask is a decision that floating point takes. The GPU masks by the sign of its
 fp32 h; the oracle by the sign of the fp64 pre-activation a. The two can differ only at
@@ -52,6 +53,9 @@ CASES = {
                                     H_shared=128), True),
     "relu_shared_ragged_k1": (_cfg(S=300, E=4, M=68, H=132, k=1, capacity_factor=1.5, n_shared=1,
                                    H_shared=68), False),
+    # p-norm gates (the router's backward through gate_norm), top-3 with a capacity
+    "swiglu_pnorm2_capacity_k3": (_cfg(S=256, k=3, act="swiglu", capacity_factor=1.0,
+                                       gate_norm="pnorm", gate_p=2.0), False),
 }
 
 
